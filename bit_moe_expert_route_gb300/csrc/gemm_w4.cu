@@ -1,0 +1,516 @@
+// Grouped GEMM with groupwise affine 4-bit weights dequantised on chip.
+//
+// "Fused dequantization inside the grouped GEMM": the packed weights are
+// unpacked one tile at a time into on-chip memory just before the multiply,
+// and the expanded weights are never written back to memory
+// ("Perplexity's Lily Beats MLX-LM by 1.35x Running Qwen3.6 on Apple
+// Silicon", section "Prefill optimizations", first bullet).
+//
+// GB300 design (one persistent CTA per SM, warp-specialised):
+//   * Swap-AB: the MMA's M side (128) is a tile of weight rows (output
+//     features), the N side is a tile of up to block_n token rows; D lives in
+//     tensor memory (TMEM), fp32. A tile of work is (block-map entry, 128-row
+//     slice of N); the block map is read on the device, so the grid never
+//     depends on the routing result.
+//   * warp 0       TMA producer: packed-code tiles (128 rows x 64 codes =
+//                  4 KB per projection) into a ring of shared-memory stages.
+//   * warp 1       allocates TMEM and issues tcgen05.mma (one thread).
+//   * warps 4-7    dequantise: thread m owns weight row m; it turns 64 codes
+//                  into bf16 RNE(scale*q + bias) and writes them into the
+//                  128-byte-swizzled K-major A operand.
+//   * warps 8-11   gather: token rows (through row_index) are copied with
+//                  16-byte cp.async into the swizzled K-major B operand;
+//                  rows past the tile's end are zero-filled.
+//   * warps 12-15  epilogue: tcgen05.ld of the accumulators, then
+//                  NONE (fp32 store), SWIGLU (bf16 silu(g)*u) or COMBINE
+//                  (row_scale * y added into the output row).
+//   Accumulators are double buffered so the epilogue of one tile overlaps the
+//   MMAs of the next. Every wait is bounded; a CTA that gives up records
+//   MOE_DEV_TIMEOUT, drains what it issued, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kTileM = 128;      // weight rows per tile (MMA M)
+constexpr int kKB = 64;          // codes per k-block (= quantisation group)
+constexpr int kQBytes = kTileM * kKB / 2;   // packed tile: 4 KB
+constexpr int kABytes = kTileM * kKB * 2;   // dequantised tile: 16 KB
+constexpr int kSQ = 4;           // packed-code stages
+constexpr int kSmemBudget = 200 * 1024;
+
+template <int BN, int NMAT>
+struct Cfg {
+  static constexpr int kBBytes = BN * kKB * 2;
+  static constexpr int kStage = NMAT * kABytes + kBBytes;
+  static constexpr int kQRing = kSQ * NMAT * kQBytes;
+  static constexpr int kSA0 = (kSmemBudget - kQRing) / kStage;
+  static constexpr int kSA = kSA0 > 6 ? 6 : kSA0;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kSA * NMAT * kABytes;
+  static constexpr int kOffQ = kOffB + kSA * kBBytes;
+  static constexpr int kOffBar = kOffQ + kQRing;
+  static constexpr int kBarBytes = 8 * (2 * kSQ + 2 * kSA + 5) + 16;
+  static constexpr int kSmem = kOffBar + kBarBytes + 1024;  // + alignment slack
+  static constexpr int kTmemCols0 = 2 * NMAT * BN;
+  static constexpr int kTmemCols = kTmemCols0 <= 32 ? 32 : kTmemCols0 <= 64 ? 64
+                                   : kTmemCols0 <= 128 ? 128 : kTmemCols0 <= 256 ? 256 : 512;
+  static_assert(kSA >= 2, "not enough shared memory for two stages");
+  static_assert(kTmemCols0 <= 512, "accumulators exceed TMEM");
+};
+
+struct KParams {
+  CUtensorMap tm[4];  // packed codes: W[0], W[1], X[0], X[1]
+  GemmParams g;
+};
+
+struct TileInfo {
+  int group, row0, rows, mt;
+  bool ok;
+};
+
+MOE_DEVINL TileInfo load_tile(const GemmParams& g, int unit, int MT) {
+  TileInfo t;
+  const int4 m = reinterpret_cast<const int4*>(g.block_map)[unit / MT];
+  t.group = m.x;
+  t.row0 = m.y;
+  t.rows = m.z;
+  t.mt = unit % MT;
+  const bool extra = g.X[0].q != nullptr;
+  t.ok = m.x >= 0 && (m.x < g.n_groups || (extra && m.x == g.n_groups)) && m.y >= 0 &&
+         m.z >= 1 && m.z <= g.block_n && (int64_t)m.y + m.z <= g.n_rows;
+  return t;
+}
+
+MOE_DEVINL int num_units(const GemmParams& g, int MT) {
+  int nt = *g.num_tiles;
+  if (nt < 0) nt = 0;
+  if (nt > g.max_tiles) nt = g.max_tiles;
+  return nt * MT;
+}
+
+// Dequantise one packed word (8 codes, low nibble first) into 8 bf16 values
+// RNE(scale * q + bias), returned as 4 bf16x2 words in K order.
+// The codes become exact bf16 integers through the bit pattern of 128 + q
+// (0x4300 | q), minus 128; scale * q + bias is then one fused bf16x2 fma
+// (single rounding). Codes are paired (i, i+4) by mask-and-shift and
+// regrouped into (2i, 2i+1) order with byte permutes.
+MOE_DEVINL uint4 dequant_word(uint32_t w, __nv_bfloat162 s2, __nv_bfloat162 b2) {
+  const __nv_bfloat162 m128 = __floats2bfloat162_rn(-128.f, -128.f);
+  const __nv_bfloat162 one = __floats2bfloat162_rn(1.f, 1.f);
+  uint32_t p[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t v = ((w >> (4 * i)) & 0x000F000Fu) | 0x43004300u;  // {128+q_i, 128+q_{i+4}}
+    __nv_bfloat162 q2 = __hfma2(*reinterpret_cast<const __nv_bfloat162*>(&v), one, m128);
+    __nv_bfloat162 r = __hfma2(s2, q2, b2);
+    p[i] = *reinterpret_cast<uint32_t*>(&r);
+  }
+  // p[i] = {w_i, w_{i+4}}; want {w0,w1},{w2,w3},{w4,w5},{w6,w7}
+  uint4 o;
+  o.x = __byte_perm(p[0], p[1], 0x5410);
+  o.y = __byte_perm(p[2], p[3], 0x5410);
+  o.z = __byte_perm(p[0], p[1], 0x7632);
+  o.w = __byte_perm(p[2], p[3], 0x7632);
+  return o;
+}
+
+template <int BN, int NMAT, int EPI>
+__global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_constant__ KParams kp) {
+  using C = Cfg<BN, NMAT>;
+  const GemmParams& g = kp.g;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = q_full + kSQ;
+  uint64_t* a_full = q_empty + kSQ;
+  uint64_t* a_empty = a_full + C::kSA;
+  uint64_t* acc_full = a_empty + C::kSA;   // [2]
+  uint64_t* acc_empty = acc_full + 2;      // [2]
+  uint64_t* drain = acc_empty + 2;         // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int MT = g.N / kTileM;
+  const int KB = g.K / kKB;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kSQ; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 128);
+    }
+    for (int i = 0; i < C::kSA; ++i) {
+      mbar_init(&a_full[i], 256);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&kp.tm[0]);
+    if (NMAT == 2) tma_prefetch_desc(&kp.tm[1]);
+    if (g.X[0].q) {
+      tma_prefetch_desc(&kp.tm[2]);
+      if (NMAT == 2) tma_prefetch_desc(&kp.tm[3]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int units = num_units(g, MT);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t policy = l2_policy_evict_last();
+      uint32_t it = 0;
+      bool alive = true;
+      for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
+        const TileInfo t = load_tile(g, u, MT);
+        if (!t.ok) {
+          report(g.status, MOE_DEV_BAD_TILE, 31, u / MT);
+          continue;
+        }
+        const bool ext = t.group == g.n_groups;
+        const int row = (ext ? 0 : t.group * g.N) + t.mt * kTileM;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % kSQ;
+          if (!mbar_wait(&q_empty[s], ((it / kSQ) & 1) ^ 1, abort_flag, g.status, 1)) {
+            alive = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&q_full[s], NMAT * kQBytes);
+#pragma unroll
+          for (int j = 0; j < NMAT; ++j)
+            tma_load_2d(smem + C::kOffQ + (s * NMAT + j) * kQBytes, &kp.tm[(ext ? 2 : 0) + j],
+                        kb * (kKB / 8), row, &q_full[s], policy);
+        }
+      }
+      // drain: every issued load must land before the CTA exits
+      const uint32_t n_issued = it;
+      for (uint32_t j = n_issued > (uint32_t)kSQ ? n_issued - kSQ : 0; j < n_issued; ++j)
+        mbar_wait(&q_full[j % kSQ], (j / kSQ) & 1, abort_flag, g.status, 2);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kTileM, BN);
+      uint32_t it = 0, acc_it = 0;
+      bool alive = true;
+      for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
+        const TileInfo t = load_tile(g, u, MT);
+        if (!t.ok) continue;
+        const uint32_t buf = acc_it & 1;
+        if (!mbar_wait(&acc_empty[buf], ((acc_it >> 1) & 1) ^ 1, abort_flag, g.status, 3)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * (NMAT * BN);
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % C::kSA;
+          if (!mbar_wait(&a_full[s], (it / C::kSA) & 1, abort_flag, g.status, 4)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t b_addr = smem_u32(smem + C::kOffB + s * C::kBBytes);
+#pragma unroll
+          for (int j = 0; j < NMAT; ++j) {
+            const uint32_t a_addr = smem_u32(smem + C::kOffA + (s * NMAT + j) * kABytes);
+#pragma unroll
+            for (int kk = 0; kk < kKB / 16; ++kk)
+              tc_mma_bf16(d_tmem + j * BN, smem_desc_sw128(a_addr + kk * 32),
+                          smem_desc_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0);
+          }
+          tc_commit(&a_empty[s]);
+        }
+        if (!alive) break;
+        tc_commit(&acc_full[buf]);
+        ++acc_it;
+      }
+      // drain: all issued MMAs complete before TMEM is freed
+      tc_commit(drain);
+      mbar_wait(drain, 0, abort_flag, g.status, 5);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ dequantise
+    const int m = threadIdx.x - 128;  // weight row inside the tile
+    uint32_t it = 0;
+    bool alive = true;
+    for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
+      const TileInfo t = load_tile(g, u, MT);
+      if (!t.ok) continue;
+      const bool ext = t.group == g.n_groups;
+      const int64_t row = (ext ? 0 : (int64_t)t.group * g.N) + t.mt * kTileM + m;
+      const uint16_t* sc[NMAT];
+      const uint16_t* bi[NMAT];
+#pragma unroll
+      for (int j = 0; j < NMAT; ++j) {
+        const GemmW4& w = ext ? g.X[j] : g.W[j];
+        sc[j] = w.scale + row * KB;
+        bi[j] = w.bias + row * KB;
+      }
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        __nv_bfloat162 s2[NMAT], b2[NMAT];
+#pragma unroll
+        for (int j = 0; j < NMAT; ++j) {
+          const uint16_t sv = __ldg(sc[j] + kb), bv = __ldg(bi[j] + kb);
+          const uint32_t s32 = (uint32_t)sv * 0x10001u, b32 = (uint32_t)bv * 0x10001u;
+          s2[j] = *reinterpret_cast<const __nv_bfloat162*>(&s32);
+          b2[j] = *reinterpret_cast<const __nv_bfloat162*>(&b32);
+        }
+        const int sq = it % kSQ;
+        if (!mbar_wait(&q_full[sq], (it / kSQ) & 1, abort_flag, g.status, 6)) {
+          alive = false;
+          break;
+        }
+        uint4 qw[NMAT][2];
+#pragma unroll
+        for (int j = 0; j < NMAT; ++j) {
+          const uint4* src =
+              reinterpret_cast<const uint4*>(smem + C::kOffQ + (sq * NMAT + j) * kQBytes + m * 32);
+          qw[j][0] = src[0];
+          qw[j][1] = src[1];
+        }
+        mbar_arrive(&q_empty[sq]);
+        const int sa = it % C::kSA;
+        if (!mbar_wait(&a_empty[sa], ((it / C::kSA) & 1) ^ 1, abort_flag, g.status, 7)) {
+          alive = false;
+          break;
+        }
+#pragma unroll
+        for (int j = 0; j < NMAT; ++j) {
+          uint8_t* a_tile = smem + C::kOffA + (sa * NMAT + j) * kABytes;
+          const uint32_t words[8] = {qw[j][0].x, qw[j][0].y, qw[j][0].z, qw[j][0].w,
+                                     qw[j][1].x, qw[j][1].y, qw[j][1].z, qw[j][1].w};
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(a_tile + sw128_offset(m, c)) =
+                dequant_word(words[c], s2[j], b2[j]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&a_full[sa]);
+      }
+    }
+  } else if (warp >= 8 && warp < 12) {
+    // ------------------------------------------------------------ gather B
+    constexpr int kRowsPerThread = (BN * 8 + 127) / 128;  // 16-byte chunks per thread
+    const int gt = threadIdx.x - 256;
+    const int c = gt & 7;           // chunk of the 128-byte row slice
+    const int n_first = gt >> 3;    // first row handled; rows n_first + 16*i
+    uint32_t it = 0;
+    bool alive = true;
+    bool pending = false;
+    int pending_sa = 0;
+    for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
+      const TileInfo t = load_tile(g, u, MT);
+      if (!t.ok) continue;
+      int64_t src_row[kRowsPerThread];
+      bool valid[kRowsPerThread];
+#pragma unroll
+      for (int i = 0; i < kRowsPerThread; ++i) {
+        const int n = n_first + 16 * i;
+        valid[i] = n < BN && n < t.rows;
+        src_row[i] = 0;
+        if (valid[i]) {
+          const int64_t r = t.row0 + n;
+          const int64_t a = g.row_index ? (int64_t)g.row_index[r] : r;
+          if (a < 0 || a >= g.A_rows) {
+            report(g.status, MOE_DEV_BAD_ROW, 32, (int)r);
+            valid[i] = false;
+          } else {
+            src_row[i] = a;
+          }
+        }
+      }
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int sa = it % C::kSA;
+        if (!mbar_wait(&a_empty[sa], ((it / C::kSA) & 1) ^ 1, abort_flag, g.status, 8)) {
+          alive = false;
+          break;
+        }
+        const uint32_t b_tile = smem_u32(smem + C::kOffB + sa * C::kBBytes);
+#pragma unroll
+        for (int i = 0; i < kRowsPerThread; ++i) {
+          const int n = n_first + 16 * i;
+          if (n < BN) {
+            const uint16_t* src = g.A + src_row[i] * g.K + kb * kKB + c * 8;
+            cp_async_16(b_tile + sw128_offset(n, c), src, valid[i] ? 16u : 0u);
+          }
+        }
+        cp_async_commit();
+        if (pending) {
+          cp_async_wait<1>();
+          fence_proxy_async_smem();
+          mbar_arrive(&a_full[pending_sa]);
+        }
+        pending = true;
+        pending_sa = sa;
+      }
+    }
+    cp_async_wait<0>();
+    if (pending) {
+      fence_proxy_async_smem();
+      mbar_arrive(&a_full[pending_sa]);
+    }
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp & 3;             // TMEM lane quarter
+    const int m = ew * 32 + lane;        // weight row inside the tile
+    constexpr int CH = BN < 32 ? BN : 32;
+    uint32_t acc_it = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const TileInfo t = load_tile(g, u, MT);
+      if (!t.ok) continue;
+      const uint32_t buf = acc_it & 1;
+      if (!mbar_wait(&acc_full[buf], (acc_it >> 1) & 1, abort_flag, g.status, 9)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(ew * 32) << 16) + buf * (NMAT * BN);
+      const int64_t col = (int64_t)t.mt * kTileM + m;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += CH) {
+        uint32_t v0[32], v1[32];
+        if constexpr (CH == 32) {
+          tmem_ld_32x32b_x32(taddr + c0, v0);
+          if (NMAT == 2) tmem_ld_32x32b_x32(taddr + BN + c0, v1);
+        } else {
+          uint32_t h0[16], h1[16];
+          tmem_ld_32x32b_x16(taddr + c0, h0);
+          if (NMAT == 2) tmem_ld_32x32b_x16(taddr + BN + c0, h1);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            v0[i] = h0[i];
+            v1[i] = NMAT == 2 ? h1[i] : 0u;
+          }
+        }
+        tc_wait_ld();
+#pragma unroll
+        for (int i = 0; i < CH; ++i) {
+          const int n = c0 + i;
+          if (n >= t.rows) break;
+          const int64_t r = (int64_t)t.row0 + n;
+          const float a = __uint_as_float(v0[i]);
+          if constexpr (EPI == MOE_EPI_NONE) {
+            static_cast<float*>(g.C)[r * g.ldc + col] = a;
+          } else if constexpr (EPI == MOE_EPI_SWIGLU) {
+            const float uval = __uint_as_float(v1[i]);
+            const float hval = a / (1.f + __expf(-a)) * uval;
+            const __nv_bfloat16 hb = __float2bfloat16_rn(hval);
+            static_cast<uint16_t*>(g.C)[r * g.ldc + col] = *reinterpret_cast<const uint16_t*>(&hb);
+          } else {
+            const int orow = __ldg(g.out_row + r);
+            if (orow < 0 || orow >= g.C_rows) {
+              report(g.status, MOE_DEV_BAD_ROW, 33, (int)r);
+            } else {
+              atomicAdd(static_cast<float*>(g.C) + (int64_t)orow * g.ldc + col,
+                        __ldg(g.row_scale + r) * a);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[buf]);
+      ++acc_it;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Packed codes viewed as a 2-D uint32 tensor [rows][K/8]; box 8 words x 128 rows.
+bool make_q_map(CUtensorMap* tm, const uint32_t* q, int64_t rows, int K) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(K / 8) * 4};
+  const cuuint32_t box[2] = {kKB / 8, kTileM};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(q), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int NMAT, int EPI>
+cudaError_t launch_t(const KParams& kp, cudaStream_t s) {
+  using C = Cfg<BN, NMAT>;
+  auto kern = gemm_w4_kernel<BN, NMAT, EPI>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (err != cudaSuccess) return err;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t max_units = (int64_t)kp.g.max_tiles * (kp.g.N / kTileM);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, max_units));
+  kern<<<grid, kThreads, C::kSmem, s>>>(kp);
+  return cudaGetLastError();
+}
+
+template <int NMAT, int EPI>
+cudaError_t launch_bn(const KParams& kp, cudaStream_t s) {
+  switch (kp.g.block_n) {
+    case 16: return launch_t<16, NMAT, EPI>(kp, s);
+    case 32: return launch_t<32, NMAT, EPI>(kp, s);
+    case 64: return launch_t<64, NMAT, EPI>(kp, s);
+    case 128: return launch_t<128, NMAT, EPI>(kp, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t gemm_w4_launch(const GemmParams& p, cudaStream_t s) {
+  KParams kp;
+  memset(&kp, 0, sizeof kp);
+  kp.g = p;
+  const int nmat = p.epilogue == MOE_EPI_SWIGLU ? 2 : 1;
+  for (int j = 0; j < nmat; ++j) {
+    if (!make_q_map(&kp.tm[j], p.W[j].q, (int64_t)p.n_groups * p.N, p.K))
+      return cudaErrorInvalidValue;
+    if (p.X[0].q && !make_q_map(&kp.tm[2 + j], p.X[j].q, p.N, p.K)) return cudaErrorInvalidValue;
+  }
+  switch (p.epilogue) {
+    case MOE_EPI_NONE: return launch_bn<1, MOE_EPI_NONE>(kp, s);
+    case MOE_EPI_SWIGLU: return launch_bn<2, MOE_EPI_SWIGLU>(kp, s);
+    case MOE_EPI_COMBINE: return launch_bn<1, MOE_EPI_COMBINE>(kp, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace moe

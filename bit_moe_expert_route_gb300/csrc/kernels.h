@@ -1,0 +1,104 @@
+// Internal launch interfaces of the CUDA kernels (host side, C++).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- routing
+constexpr int kRouteTPB = 128;  // tokens per block of the top-k and scatter kernels
+
+struct RouteParams {
+  const float* logits;     // [T][E]
+  const float* bias;       // [E] or null
+  int T, E, k, block_n, with_shared;
+  // optional shared-expert gate (moe_forward): gate_logit[t] = x_t . wsg
+  const uint16_t* x;       // [T][d] bf16 or null
+  const float* wsg;        // [d]
+  int d;
+  float* gate_logit;       // [T]
+  // outputs
+  int32_t* ids;            // [T][k]
+  float* w;                // [T][k]
+  int32_t* counts;         // [E]
+  int32_t* offsets;        // [E+1]
+  int32_t* perm;           // [T*k]
+  int32_t* inv_perm;       // [T*k]
+  int32_t* row_token;      // [T*k (+T)]
+  float* row_weight;       // [T*k (+T)] or null
+  int32_t* block_map;      // [max_tiles][4]
+  int32_t* num_tiles;      // [1]
+  int max_tiles;
+  // scratch
+  int32_t* blk;            // [nblk][E]
+  int32_t* status;
+};
+
+inline int route_nblk(int T) { return (T + kRouteTPB - 1) / kRouteTPB; }
+cudaError_t route_launch(const RouteParams& p, cudaStream_t s);
+
+// ---------------------------------------------------------------- router GEMM
+// logits[t][e] = sum_k x[t][k] * Wr[k][e]   (fp32 accumulate)
+cudaError_t router_gemm_launch(const uint16_t* x, const float* Wr, int T, int d, int E,
+                               float* logits, cudaStream_t s);
+
+// ---------------------------------------------------------------- grouped GEMM
+struct GemmW4 {
+  const uint32_t* q;
+  const uint16_t* scale;
+  const uint16_t* bias;
+};
+
+struct GemmParams {
+  const uint16_t* A;        // [A_rows][K] bf16
+  int64_t A_rows;
+  int K;
+  const int32_t* row_index; // [n_rows] or null
+  int64_t n_rows;
+  GemmW4 W[2];              // routed stack (W[1] = up for SwiGLU)
+  GemmW4 X[2];              // extra group (index n_groups), q == null if absent
+  int n_groups;
+  int N;
+  const int32_t* block_map;
+  const int32_t* num_tiles;
+  int max_tiles;
+  int block_n;
+  int epilogue;
+  const float* row_scale;
+  const int32_t* out_row;
+  void* C;
+  int64_t C_rows;
+  int64_t ldc;
+  int32_t* status;
+};
+
+cudaError_t gemm_w4_launch(const GemmParams& p, cudaStream_t s);
+
+// ---------------------------------------------------------------- elementwise
+cudaError_t f32_to_bf16_launch(const float* in, uint16_t* out, int64_t n, cudaStream_t s);
+
+// ---------------------------------------------------------------- decode
+struct DecodeParams {
+  const uint16_t* x;        // [d]
+  moe_weights_t w;
+  int d, E, k, f;
+  bool shared;
+  uint16_t* out;            // [d]
+  // workspace
+  float* logits;            // [E]
+  float* gate_logit;        // [1]
+  float* part;              // router partial sums [nsplit][E + 1]
+  int32_t* ids;             // [k]
+  float* wts;               // [k]
+  float* h;                 // [k+1][f]
+  uint32_t* counter;        // [1] last-block-done counter (self-resetting)
+  int32_t* status;
+};
+int decode_router_splits(int d);
+cudaError_t decode_launch(const DecodeParams& p, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,489 @@
+// C ABI of libmoe_gb300: argument validation, workspace layouts and the
+// launch sequences of the routing, grouped-GEMM, whole-layer and decode
+// entry points declared in include/moe.h.
+#include <algorithm>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+using moe::kStatusWords;
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return (major == 10 && minor == 3) ? MOE_OK : MOE_ERR_ARCH;
+}
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  (void)cudaGetLastError();  // clear a non-sticky launch error
+  return MOE_ERR_CUDA;
+}
+
+bool valid_block_n(int bn, bool route) {
+  return bn == 16 || bn == 32 || bn == 64 || bn == 128 || (route && bn == 256);
+}
+
+// Sequential workspace carve-out.
+struct Carve {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carve(void* b) : base(static_cast<uint8_t*>(b)) {}
+  template <class T>
+  T* take(size_t count) {
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += align_up(count * sizeof(T));
+    return p;
+  }
+};
+
+struct RouteWs {
+  int32_t* status;
+  int32_t* blk;
+  size_t bytes;
+};
+
+RouteWs route_ws(void* ws, int T, int E) {
+  Carve c(ws);
+  RouteWs r;
+  r.status = c.take<int32_t>(kStatusWords);
+  r.blk = c.take<int32_t>((size_t)moe::route_nblk(T) * E);
+  r.bytes = c.off;
+  return r;
+}
+
+bool shape_ok(const moe_shape_t* s, bool need_tokens) {
+  if (!s) return false;
+  if (s->T < 0 || (need_tokens && s->T < 1)) return false;
+  if (s->group != 64) return false;
+  if (s->d_model < 128 || s->d_model % 128) return false;
+  if (s->d_ff < 128 || s->d_ff % 128) return false;
+  if (s->n_experts < 1 || s->n_experts > 1024 || s->n_experts % 8) return false;
+  if (s->top_k < 1 || s->top_k > 32 || s->top_k > s->n_experts) return false;
+  if ((int64_t)s->T * (s->top_k + 1) >= (int64_t)1 << 30) return false;
+  return true;
+}
+
+struct FwdWs {
+  moe_forward_views_t v;
+  int32_t* blk;  // routing scratch [route_nblk(T)][E]
+  size_t bytes;
+};
+
+FwdWs forward_ws(void* ws, const moe_shape_t* s, int bn) {
+  const int T = s->T, E = s->n_experts, k = s->top_k;
+  const int64_t rows = (int64_t)T * k + T;
+  Carve c(ws);
+  FwdWs r;
+  memset(&r.v, 0, sizeof r.v);
+  r.v.max_tiles = moe_max_tiles(T, E, k, bn, 1);
+  r.v.block_n = bn;
+  r.v.status = c.take<int32_t>(kStatusWords);
+  r.v.logits = c.take<float>((size_t)T * E);
+  r.v.gate_logit = c.take<float>(T);
+  r.v.topk_ids = c.take<int32_t>((size_t)T * k);
+  r.v.topk_w = c.take<float>((size_t)T * k);
+  r.v.counts = c.take<int32_t>(E);
+  r.v.offsets = c.take<int32_t>(E + 1);
+  r.v.perm = c.take<int32_t>((size_t)T * k);
+  r.v.inv_perm = c.take<int32_t>((size_t)T * k);
+  r.v.row_token = c.take<int32_t>(rows);
+  r.v.row_weight = c.take<float>(rows);
+  r.v.block_map = c.take<int32_t>((size_t)r.v.max_tiles * 4);
+  r.v.num_tiles = c.take<int32_t>(1);
+  r.blk = c.take<int32_t>((size_t)moe::route_nblk(T) * E);
+  r.v.h = c.take<uint16_t>((size_t)rows * s->d_ff);
+  r.v.out_acc = c.take<float>((size_t)T * s->d_model);
+  r.bytes = c.off;
+  return r;
+}
+
+struct DecWs {
+  moe_decode_views_t v;
+  float* part;
+  uint32_t* counter;
+  size_t bytes;
+};
+
+DecWs decode_ws(void* ws, const moe_shape_t* s) {
+  const int E = s->n_experts, k = s->top_k;
+  Carve c(ws);
+  DecWs r;
+  memset(&r.v, 0, sizeof r.v);
+  r.v.status = c.take<int32_t>(kStatusWords);
+  r.counter = reinterpret_cast<uint32_t*>(r.v.status + 16);
+  r.v.logits = c.take<float>(E);
+  r.v.gate_logit = c.take<float>(1);
+  r.v.topk_ids = c.take<int32_t>(k);
+  r.v.topk_w = c.take<float>(k + 1);
+  r.v.h = c.take<float>((size_t)(k + 1) * s->d_ff);
+  r.part = c.take<float>((size_t)moe::decode_router_splits(s->d_model) * (E + 1));
+  r.bytes = c.off;
+  return r;
+}
+
+bool w4_ok(const moe_w4_t& w) {
+  return w.q && w.scale && w.bias && aligned(w.q, 16) && aligned(w.scale, 4) && aligned(w.bias, 4);
+}
+
+int check_weights(const moe_weights_t* w, const moe_shape_t* s) {
+  if (!w || !w->router) return MOE_ERR_NULL;
+  const moe_w4_t* all[6] = {&w->gate, &w->up, &w->down, &w->sh_gate, &w->sh_up, &w->sh_down};
+  const int n = w->shared_gate ? 6 : 3;
+  for (int i = 0; i < n; ++i) {
+    if (!all[i]->q || !all[i]->scale || !all[i]->bias) return MOE_ERR_NULL;
+    if (!w4_ok(*all[i])) return MOE_ERR_ALIGN;
+  }
+  if (!aligned(w->router, 16) || (w->router_bias && !aligned(w->router_bias, 4)) ||
+      (w->shared_gate && !aligned(w->shared_gate, 16)))
+    return MOE_ERR_ALIGN;
+  if (w->shared_gate && s->d_ff_shared != s->d_ff) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_NULL: return "a required pointer is NULL";
+    case MOE_ERR_ALIGN: return "a pointer is not aligned as required";
+    case MOE_ERR_SHAPE: return "unsupported or inconsistent sizes";
+    case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MOE_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case MOE_ERR_DEVICE: return "a kernel recorded a fault in the device status word";
+    case MOE_ERR_ARCH: return "the current device is not a compute capability 10.3 GPU";
+    case 100 + MOE_DEV_OK: return "device: ok";
+    case 100 + MOE_DEV_BAD_TILE: return "device: block-map entry out of range";
+    case 100 + MOE_DEV_BAD_ROW: return "device: row index out of range";
+    case 100 + MOE_DEV_TIMEOUT: return "device: bounded wait ran out";
+    case 100 + MOE_DEV_BAD_EXPERT: return "device: expert id out of range";
+    default: return "unknown status";
+  }
+}
+
+int moe_version(void) { return 100; }
+
+int moe_pick_block_n(int T, int n_experts, int top_k) {
+  if (T <= 0 || n_experts <= 0) return 16;
+  const double per_expert = (double)T * top_k / n_experts;
+  if (per_expert <= 16) return 16;
+  if (per_expert <= 32) return 32;
+  if (per_expert <= 64) return 64;
+  return 128;
+}
+
+int moe_max_tiles(int T, int n_experts, int top_k, int block_n, int with_shared) {
+  if (T < 0 || block_n <= 0) return 0;
+  return (int)(cdiv((int64_t)T * top_k, block_n) + n_experts +
+               (with_shared ? cdiv(T, block_n) : 0));
+}
+
+size_t moe_route_workspace_bytes(int T, int n_experts) {
+  if (T < 0 || n_experts < 1) return 0;
+  return route_ws(nullptr, T, n_experts).bytes;
+}
+
+int moe_route(const float* logits, const float* logit_bias, int T, int n_experts, int top_k,
+              int block_n, int with_shared, int32_t* topk_ids, float* topk_w, int32_t* counts,
+              int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* row_token,
+              float* row_weight, int32_t* block_map, int32_t* num_tiles, int max_tiles, void* ws,
+              size_t ws_bytes, void* stream) {
+  if (T < 0 || n_experts < 1 || n_experts > 1024 || top_k < 1 || top_k > 32 ||
+      top_k > n_experts || !valid_block_n(block_n, true) || (int64_t)T * (top_k + 1) >= (1 << 30))
+    return MOE_ERR_SHAPE;
+  if (!counts || !offsets || !num_tiles) return MOE_ERR_NULL;
+  if (T > 0 && (!logits || !topk_ids || !topk_w || !perm || !inv_perm || !row_token || !block_map))
+    return MOE_ERR_NULL;
+  if (max_tiles < moe_max_tiles(T, n_experts, top_k, block_n, with_shared)) return MOE_ERR_SHAPE;
+  if (!aligned(block_map, 16) || !aligned(logits, 4)) return MOE_ERR_ALIGN;
+  const RouteWs rw = route_ws(ws, T, n_experts);
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < rw.bytes) return MOE_ERR_WORKSPACE;
+  int rc = check_device();
+  if (rc != MOE_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((rc = cuda_status(cudaMemsetAsync(rw.status, 0, kStatusWords * 4, s))) != MOE_OK) return rc;
+  if (T == 0) {  // nothing routed: empty histogram, zero offsets, no tiles
+    if ((rc = cuda_status(cudaMemsetAsync(counts, 0, n_experts * 4, s))) != MOE_OK) return rc;
+    if ((rc = cuda_status(cudaMemsetAsync(offsets, 0, (n_experts + 1) * 4, s))) != MOE_OK) return rc;
+    return cuda_status(cudaMemsetAsync(num_tiles, 0, 4, s));
+  }
+  moe::RouteParams p;
+  memset(&p, 0, sizeof p);
+  p.logits = logits;
+  p.bias = logit_bias;
+  p.T = T;
+  p.E = n_experts;
+  p.k = top_k;
+  p.block_n = block_n;
+  p.with_shared = with_shared ? 1 : 0;
+  p.ids = topk_ids;
+  p.w = topk_w;
+  p.counts = counts;
+  p.offsets = offsets;
+  p.perm = perm;
+  p.inv_perm = inv_perm;
+  p.row_token = row_token;
+  p.row_weight = row_weight;
+  p.block_map = block_map;
+  p.num_tiles = num_tiles;
+  p.max_tiles = max_tiles;
+  p.blk = rw.blk;
+  p.status = rw.status;
+  return cuda_status(moe::route_launch(p, s));
+}
+
+size_t moe_gemm_workspace_bytes(void) { return kStatusWords * 4; }
+
+int moe_grouped_gemm_w4a16(const uint16_t* A, int64_t A_rows, int K, const int32_t* row_index,
+                           int64_t n_rows, const moe_w4_t* W, int n_groups, int N,
+                           const moe_w4_t* W_extra, const int32_t* block_map,
+                           const int32_t* num_tiles, int max_tiles, int block_n, int epilogue,
+                           const float* row_scale, const int32_t* out_row, void* C,
+                           int64_t C_rows, int64_t ldc, void* ws, size_t ws_bytes, void* stream) {
+  if (epilogue != MOE_EPI_NONE && epilogue != MOE_EPI_SWIGLU && epilogue != MOE_EPI_COMBINE)
+    return MOE_ERR_SHAPE;
+  if (K < 64 || K % 64 || N < 128 || N % 128 || n_groups < 1 || A_rows < 0 || n_rows < 0 ||
+      max_tiles < 0 || !valid_block_n(block_n, false) || ldc < N || C_rows < 0)
+    return MOE_ERR_SHAPE;
+  if (epilogue != MOE_EPI_COMBINE && C_rows < n_rows) return MOE_ERR_SHAPE;
+  if (!A || !W || !block_map || !num_tiles || !C) return MOE_ERR_NULL;
+  if (epilogue == MOE_EPI_COMBINE && (!row_scale || !out_row)) return MOE_ERR_NULL;
+  const int nmat = epilogue == MOE_EPI_SWIGLU ? 2 : 1;
+  for (int j = 0; j < nmat; ++j) {
+    if (!W[j].q || !W[j].scale || !W[j].bias) return MOE_ERR_NULL;
+    if (!w4_ok(W[j])) return MOE_ERR_ALIGN;
+    if (W_extra) {
+      if (!W_extra[j].q || !W_extra[j].scale || !W_extra[j].bias) return MOE_ERR_NULL;
+      if (!w4_ok(W_extra[j])) return MOE_ERR_ALIGN;
+    }
+  }
+  if (!aligned(A, 16) || !aligned(block_map, 16) || !aligned(C, 16)) return MOE_ERR_ALIGN;
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < moe_gemm_workspace_bytes()) return MOE_ERR_WORKSPACE;
+  int rc = check_device();
+  if (rc != MOE_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* status = static_cast<int32_t*>(ws);
+  if ((rc = cuda_status(cudaMemsetAsync(status, 0, kStatusWords * 4, s))) != MOE_OK) return rc;
+  if (max_tiles == 0 || n_rows == 0) return MOE_OK;
+  moe::GemmParams p;
+  memset(&p, 0, sizeof p);
+  p.A = A;
+  p.A_rows = A_rows;
+  p.K = K;
+  p.row_index = row_index;
+  p.n_rows = n_rows;
+  for (int j = 0; j < nmat; ++j) {
+    p.W[j] = {W[j].q, W[j].scale, W[j].bias};
+    if (W_extra) p.X[j] = {W_extra[j].q, W_extra[j].scale, W_extra[j].bias};
+  }
+  p.n_groups = n_groups;
+  p.N = N;
+  p.block_map = block_map;
+  p.num_tiles = num_tiles;
+  p.max_tiles = max_tiles;
+  p.block_n = block_n;
+  p.epilogue = epilogue;
+  p.row_scale = row_scale;
+  p.out_row = out_row;
+  p.C = C;
+  p.C_rows = C_rows;
+  p.ldc = ldc;
+  p.status = status;
+  return cuda_status(moe::gemm_w4_launch(p, s));
+}
+
+size_t moe_workspace_bytes(const moe_shape_t* shape, int block_n) {
+  if (!shape_ok(shape, false)) return 0;
+  if (block_n == 0) block_n = moe_pick_block_n(shape->T, shape->n_experts, shape->top_k);
+  if (!valid_block_n(block_n, false)) return 0;
+  return forward_ws(nullptr, shape, block_n).bytes;
+}
+
+int moe_forward_views(void* ws, size_t ws_bytes, const moe_shape_t* shape, int block_n,
+                      moe_forward_views_t* views) {
+  if (!shape_ok(shape, false)) return MOE_ERR_SHAPE;
+  if (block_n == 0) block_n = moe_pick_block_n(shape->T, shape->n_experts, shape->top_k);
+  if (!valid_block_n(block_n, false)) return MOE_ERR_SHAPE;
+  if (!views) return MOE_ERR_NULL;
+  const FwdWs fw = forward_ws(ws, shape, block_n);
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < fw.bytes) return MOE_ERR_WORKSPACE;
+  *views = fw.v;
+  return MOE_OK;
+}
+
+int moe_forward(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* shape, int block_n,
+                uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+  if (!shape_ok(shape, false)) return MOE_ERR_SHAPE;
+  if (block_n == 0) block_n = moe_pick_block_n(shape->T, shape->n_experts, shape->top_k);
+  if (!valid_block_n(block_n, false)) return MOE_ERR_SHAPE;
+  const int T = shape->T, E = shape->n_experts, k = shape->top_k, d = shape->d_model,
+            f = shape->d_ff;
+  int rc = check_weights(w, shape);
+  if (rc != MOE_OK) return rc;
+  if (T > 0 && (!x || !out)) return MOE_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(out, 16)) return MOE_ERR_ALIGN;
+  const FwdWs fw = forward_ws(ws, shape, block_n);
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < fw.bytes) return MOE_ERR_WORKSPACE;
+  if ((rc = check_device()) != MOE_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const moe_forward_views_t& v = fw.v;
+  if ((rc = cuda_status(cudaMemsetAsync(v.status, 0, kStatusWords * 4, s))) != MOE_OK) return rc;
+  if (T == 0) return MOE_OK;
+  const bool shared = w->shared_gate != nullptr;
+  const int64_t rows = (int64_t)T * k + (shared ? T : 0);
+
+  // 1. router logits
+  if ((rc = cuda_status(moe::router_gemm_launch(x, w->router, T, d, E, v.logits, s))) != MOE_OK)
+    return rc;
+  // 2. top-k, shared gate, histogram, scan, scatter, block map
+  moe::RouteParams rp;
+  memset(&rp, 0, sizeof rp);
+  rp.logits = v.logits;
+  rp.bias = w->router_bias;
+  rp.T = T;
+  rp.E = E;
+  rp.k = k;
+  rp.block_n = block_n;
+  rp.with_shared = shared ? 1 : 0;
+  rp.x = shared ? x : nullptr;
+  rp.wsg = w->shared_gate;
+  rp.d = d;
+  rp.gate_logit = v.gate_logit;
+  rp.ids = v.topk_ids;
+  rp.w = v.topk_w;
+  rp.counts = v.counts;
+  rp.offsets = v.offsets;
+  rp.perm = v.perm;
+  rp.inv_perm = v.inv_perm;
+  rp.row_token = v.row_token;
+  rp.row_weight = v.row_weight;
+  rp.block_map = v.block_map;
+  rp.num_tiles = v.num_tiles;
+  rp.max_tiles = v.max_tiles;
+  rp.blk = fw.blk;
+  rp.status = v.status;
+  if ((rc = cuda_status(moe::route_launch(rp, s))) != MOE_OK) return rc;
+  // 3. gate/up grouped GEMM with SwiGLU -> h (rows in expert order, shared rows last)
+  moe::GemmParams g;
+  memset(&g, 0, sizeof g);
+  g.A = x;
+  g.A_rows = T;
+  g.K = d;
+  g.row_index = v.row_token;
+  g.n_rows = rows;
+  g.W[0] = {w->gate.q, w->gate.scale, w->gate.bias};
+  g.W[1] = {w->up.q, w->up.scale, w->up.bias};
+  if (shared) {
+    g.X[0] = {w->sh_gate.q, w->sh_gate.scale, w->sh_gate.bias};
+    g.X[1] = {w->sh_up.q, w->sh_up.scale, w->sh_up.bias};
+  }
+  g.n_groups = E;
+  g.N = f;
+  g.block_map = v.block_map;
+  g.num_tiles = v.num_tiles;
+  g.max_tiles = v.max_tiles;
+  g.block_n = block_n;
+  g.epilogue = MOE_EPI_SWIGLU;
+  g.C = v.h;
+  g.C_rows = rows;
+  g.ldc = f;
+  g.status = v.status;
+  if ((rc = cuda_status(moe::gemm_w4_launch(g, s))) != MOE_OK) return rc;
+  // 4. down grouped GEMM, weighted combine into the fp32 accumulator
+  if ((rc = cuda_status(cudaMemsetAsync(v.out_acc, 0, (size_t)T * d * 4, s))) != MOE_OK) return rc;
+  moe::GemmParams g2 = g;
+  g2.A = v.h;
+  g2.A_rows = rows;
+  g2.K = f;
+  g2.row_index = nullptr;
+  g2.W[0] = {w->down.q, w->down.scale, w->down.bias};
+  g2.W[1] = {};
+  g2.X[0] = shared ? moe::GemmW4{w->sh_down.q, w->sh_down.scale, w->sh_down.bias} : moe::GemmW4{};
+  g2.X[1] = {};
+  g2.N = d;
+  g2.epilogue = MOE_EPI_COMBINE;
+  g2.row_scale = v.row_weight;
+  g2.out_row = v.row_token;
+  g2.C = v.out_acc;
+  g2.C_rows = T;
+  g2.ldc = d;
+  if ((rc = cuda_status(moe::gemm_w4_launch(g2, s))) != MOE_OK) return rc;
+  // 5. bf16 output
+  return cuda_status(moe::f32_to_bf16_launch(v.out_acc, out, (int64_t)T * d, s));
+}
+
+size_t moe_decode_workspace_bytes(const moe_shape_t* shape) {
+  if (!shape_ok(shape, false)) return 0;
+  return decode_ws(nullptr, shape).bytes;
+}
+
+int moe_decode_views(void* ws, size_t ws_bytes, const moe_shape_t* shape,
+                     moe_decode_views_t* views) {
+  if (!shape_ok(shape, false)) return MOE_ERR_SHAPE;
+  if (!views) return MOE_ERR_NULL;
+  const DecWs dw = decode_ws(ws, shape);
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < dw.bytes) return MOE_ERR_WORKSPACE;
+  *views = dw.v;
+  return MOE_OK;
+}
+
+int moe_decode_gemv_w4(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* shape,
+                       uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+  if (!shape_ok(shape, true) || shape->T != 1) return MOE_ERR_SHAPE;
+  int rc = check_weights(w, shape);
+  if (rc != MOE_OK) return rc;
+  if (!x || !out) return MOE_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(out, 4)) return MOE_ERR_ALIGN;
+  const DecWs dw = decode_ws(ws, shape);
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < dw.bytes) return MOE_ERR_WORKSPACE;
+  if ((rc = check_device()) != MOE_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((rc = cuda_status(cudaMemsetAsync(dw.v.status, 0, kStatusWords * 4, s))) != MOE_OK) return rc;
+  moe::DecodeParams p;
+  memset(&p, 0, sizeof p);
+  p.x = x;
+  p.w = *w;
+  p.d = shape->d_model;
+  p.E = shape->n_experts;
+  p.k = shape->top_k;
+  p.f = shape->d_ff;
+  p.shared = w->shared_gate != nullptr;
+  p.out = out;
+  p.logits = dw.v.logits;
+  p.gate_logit = dw.v.gate_logit;
+  p.part = dw.part;
+  p.ids = dw.v.topk_ids;
+  p.wts = dw.v.topk_w;
+  p.h = dw.v.h;
+  p.counter = dw.counter;
+  p.status = dw.v.status;
+  return cuda_status(moe::decode_launch(p, s));
+}
+
+int moe_get_device_status(const void* ws, void* stream, int32_t* device_status) {
+  if (!ws || !device_status) return MOE_ERR_NULL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  int rc = cuda_status(cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, s));
+  if (rc != MOE_OK) return rc;
+  if ((rc = cuda_status(cudaStreamSynchronize(s))) != MOE_OK) return rc;
+  *device_status = v;
+  return v == MOE_DEV_OK ? MOE_OK : MOE_ERR_DEVICE;
+}
+
+}  // extern "C"

@@ -1,0 +1,297 @@
+// GPU-resident expert routing: top-k selection and weights, per-block
+// histograms, a scan that yields per-expert offsets and the block map, and a
+// stable, atomics-free scatter of the (token, slot) assignments into expert
+// order. ("Perplexity's Lily Beats MLX-LM by 1.35x Running Qwen3.6 on Apple
+// Silicon", section "Prefill optimizations", second bullet: histogram,
+// prefix scan, scatter and block-map build all stay on the GPU.)
+//
+// Three launches, no host round trip:
+//   1. route_topk_kernel    one warp per token: top-k by warp argmax (value
+//                           descending, ties to the lower id), softmax over the
+//                           selected logits, optional shared-expert gate,
+//                           per-block expert histogram (shared-memory counts).
+//   2. route_scan_kernel    one CTA: per-(block, expert) bases, counts,
+//                           offsets, tile offsets and the block map.
+//   3. route_scatter_kernel per block: stable rank of each assignment inside
+//                           its warp slice by __match_any_sync + popc, then
+//                           perm / inv_perm / row_token / row_weight.
+#include <climits>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+
+template <int NPL>  // logits per lane: E <= 32 * NPL
+__global__ void __launch_bounds__(kThreads) route_topk_kernel(RouteParams p) {
+  extern __shared__ int hist[];  // [E]
+  for (int e = threadIdx.x; e < p.E; e += kThreads) hist[e] = 0;
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t_begin = blockIdx.x * kRouteTPB;
+  const int t_end = min(p.T, t_begin + kRouteTPB);
+  for (int t = t_begin + warp; t < t_end; t += kWarps) {
+    float z[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = i * 32 + lane;
+      float v = 0.f;
+      if (e < p.E) {
+        v = p.logits[(size_t)t * p.E + e];
+        if (p.bias) v = v + p.bias[e];  // fp32 add, as the decision precision
+      }
+      z[i] = v;
+    }
+    uint32_t taken = 0;
+    float my_z = 0.f;
+    int my_e = 0;
+    for (int j = 0; j < p.k; ++j) {
+      float bv = 0.f;
+      int be = INT_MAX;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int e = i * 32 + lane;
+        const bool ok = e < p.E && !((taken >> i) & 1u);
+        if (ok && (be == INT_MAX || z[i] > bv)) {
+          bv = z[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(kFull, bv, off);
+        const int oe = __shfl_xor_sync(kFull, be, off);
+        if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (lane == j) {
+        my_z = bv;
+        my_e = be;
+      }
+    }
+    const float zmax = __shfl_sync(kFull, my_z, 0);
+    const float ex = lane < p.k ? expf(my_z - zmax) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+    if (lane < p.k) {
+      const size_t a = (size_t)t * p.k + lane;
+      p.ids[a] = my_e;
+      p.w[a] = ex / sum;
+      atomicAdd(&hist[my_e], 1);
+    }
+    if (p.x) {  // shared-expert gate logit x_t . w_sg and sigmoid gate
+      float acc = 0.f;
+      const uint4* xr = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.d);
+      const float4* wr = reinterpret_cast<const float4*>(p.wsg);
+      for (int c = lane; c < p.d / 8; c += 32) {
+        const uint4 xv = xr[c];
+        const float4 w0 = wr[2 * c], w1 = wr[2 * c + 1];
+        const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
+        const float ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc = fmaf(__uint_as_float(xs[i] << 16), ws[2 * i], acc);
+          acc = fmaf(__uint_as_float(xs[i] & 0xFFFF0000u), ws[2 * i + 1], acc);
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
+      if (lane == 0) {
+        p.gate_logit[t] = acc;
+        if (p.row_weight) p.row_weight[(size_t)p.T * p.k + t] = 1.f / (1.f + expf(-acc));
+      }
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < p.E; e += kThreads) p.blk[(size_t)blockIdx.x * p.E + e] = hist[e];
+}
+
+// Exclusive scan over the CTA (blockDim.x == 1024). Returns the exclusive
+// prefix of `v`; *total (shared memory) receives the sum of all values.
+__device__ int block_exclusive_scan_1024(int v, int* total) {
+  __shared__ int warp_sums[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(kFull, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int s = warp_sums[lane];
+    int si = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(kFull, si, off);
+      if (lane >= off) si += o;
+    }
+    warp_sums[lane] = si - s;  // exclusive prefix of the warp totals
+    if (lane == 31) *total = si;
+  }
+  __syncthreads();
+  const int r = incl - v + warp_sums[warp];
+  __syncthreads();  // warp_sums is reused by the next call
+  return r;
+}
+
+__global__ void __launch_bounds__(1024) route_scan_kernel(RouteParams p, int nblk) {
+  __shared__ int s_off[1025];
+  __shared__ int s_cnt[1024];
+  __shared__ int s_toff[1025];
+  __shared__ int s_total;
+  __shared__ int s_tiles;
+  const int e = threadIdx.x;
+  int total = 0;
+  if (e < p.E) {
+    for (int b = 0; b < nblk; ++b) {
+      const size_t i = (size_t)b * p.E + e;
+      const int c = p.blk[i];
+      p.blk[i] = total;  // exclusive base of block b inside expert e
+      total += c;
+    }
+    p.counts[e] = total;
+    s_cnt[e] = total;
+  }
+  const int off = block_exclusive_scan_1024(e < p.E ? total : 0, &s_total);
+  if (e < p.E) {
+    p.offsets[e] = off;
+    s_off[e] = off;
+  }
+  if (e == 0) {
+    p.offsets[p.E] = s_total;
+    s_off[p.E] = s_total;
+  }
+  const int bn = p.block_n;
+  const int nt = e < p.E ? (total + bn - 1) / bn : 0;
+  const int toff = block_exclusive_scan_1024(nt, &s_tiles);
+  if (e < p.E) s_toff[e] = toff;
+  if (e == 0) s_toff[p.E] = s_tiles;
+  __syncthreads();
+  const int routed_tiles = s_tiles;
+  const int shared_tiles = p.with_shared ? (p.T + bn - 1) / bn : 0;
+  int num = routed_tiles + shared_tiles;
+  if (num > p.max_tiles) {
+    if (e == 0) report(p.status, MOE_DEV_BAD_TILE, 11, num);
+    num = p.max_tiles;
+  }
+  if (e == 0) *p.num_tiles = num;
+  const int kT = p.T * p.k;
+  for (int i = e; i < num; i += blockDim.x) {
+    int4 m;
+    if (i < routed_tiles) {
+      // last expert g with s_toff[g] <= i (experts without tiles share offsets)
+      int lo = 0, hi = p.E - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_toff[mid] <= i) lo = mid; else hi = mid - 1;
+      }
+      const int j = i - s_toff[lo];
+      m.x = lo;
+      m.y = s_off[lo] + j * bn;
+      m.z = min(bn, s_cnt[lo] - j * bn);
+    } else {
+      const int j = i - routed_tiles;
+      m.x = p.E;
+      m.y = kT + j * bn;
+      m.z = min(bn, p.T - j * bn);
+    }
+    m.w = 0;
+    reinterpret_cast<int4*>(p.block_map)[i] = m;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) route_scatter_kernel(RouteParams p) {
+  extern __shared__ int wbase[];  // [kWarps][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t a0 = (int64_t)blockIdx.x * kRouteTPB * p.k;
+  const int64_t a1 = min((int64_t)p.T, (int64_t)(blockIdx.x + 1) * kRouteTPB) * p.k;
+  const int64_t span = (a1 - a0 + kWarps - 1) / kWarps;
+  const int64_t w0 = a0 + warp * span;
+  const int64_t w1 = min(a1, w0 + span);
+
+  for (int i = threadIdx.x; i < kWarps * p.E; i += kThreads) wbase[i] = 0;
+  __syncthreads();
+  int* mine = wbase + warp * p.E;
+  for (int64_t a = w0 + lane; a < w1; a += 32) {
+    const int e = p.ids[a];
+    if (e >= 0 && e < p.E) atomicAdd(&mine[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < p.E; e += kThreads) {
+    int base = p.offsets[e] + p.blk[(size_t)blockIdx.x * p.E + e];
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = wbase[w * p.E + e];
+      wbase[w * p.E + e] = base;
+      base += c;
+    }
+  }
+  __syncthreads();
+  for (int64_t c0 = w0; c0 < w1; c0 += 32) {
+    const int64_t a = c0 + lane;
+    const bool valid = a < w1;
+    int e = valid ? p.ids[a] : -1 - lane;
+    if (valid && (e < 0 || e >= p.E)) {
+      report(p.status, MOE_DEV_BAD_EXPERT, 12, (int)a);
+      e = -100 - lane;
+    }
+    const uint32_t m = __match_any_sync(kFull, e);
+    int pos = 0;
+    if (e >= 0) {
+      pos = mine[e] + __popc(m & lanemask_lt());
+      p.perm[pos] = (int32_t)a;
+      p.inv_perm[a] = pos;
+      p.row_token[pos] = (int32_t)(a / p.k);
+      if (p.row_weight) p.row_weight[pos] = p.w[a];
+    }
+    __syncwarp();
+    if (e >= 0 && lane == 31 - __clz(m)) mine[e] += __popc(m);
+    __syncwarp();
+  }
+  if (p.with_shared) {
+    const int t_begin = blockIdx.x * kRouteTPB;
+    const int t_end = min(p.T, t_begin + kRouteTPB);
+    for (int t = t_begin + threadIdx.x; t < t_end; t += kThreads)
+      p.row_token[(size_t)p.T * p.k + t] = t;
+  }
+}
+
+}  // namespace
+
+cudaError_t route_launch(const RouteParams& p, cudaStream_t s) {
+  const int nblk = route_nblk(p.T);
+  const size_t hist_bytes = (size_t)p.E * sizeof(int);
+  const int npl = (p.E + 31) / 32;
+  if (npl <= 1) route_topk_kernel<1><<<nblk, kThreads, hist_bytes, s>>>(p);
+  else if (npl <= 2) route_topk_kernel<2><<<nblk, kThreads, hist_bytes, s>>>(p);
+  else if (npl <= 4) route_topk_kernel<4><<<nblk, kThreads, hist_bytes, s>>>(p);
+  else if (npl <= 8) route_topk_kernel<8><<<nblk, kThreads, hist_bytes, s>>>(p);
+  else if (npl <= 16) route_topk_kernel<16><<<nblk, kThreads, hist_bytes, s>>>(p);
+  else route_topk_kernel<32><<<nblk, kThreads, hist_bytes, s>>>(p);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  route_scan_kernel<<<1, 1024, 0, s>>>(p, nblk);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const size_t wb_bytes = (size_t)kWarps * p.E * sizeof(int);
+  if (wb_bytes > 48 * 1024) {
+    err = cudaFuncSetAttribute(route_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)wb_bytes);
+    if (err != cudaSuccess) return err;
+  }
+  route_scatter_kernel<<<nblk, kThreads, wb_bytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

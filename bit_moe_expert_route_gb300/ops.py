@@ -1,0 +1,302 @@
+"""ctypes binding of libmoe_gb300 (include/moe.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels. PyTorch provides device memory and the current stream. The library
+must have been built (``python -m bit_moe_expert_route_gb300.build``); if it
+is missing, the first call raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+from .synth import LayerShape
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+SO_PATH = os.path.join(_PKG, "libmoe_gb300.so")
+
+EPI_NONE, EPI_SWIGLU, EPI_COMBINE = 0, 1, 2
+DEV_OK, DEV_BAD_TILE, DEV_BAD_ROW, DEV_TIMEOUT, DEV_BAD_EXPERT = 0, 1, 2, 3, 4
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} failed: {code} ({status_string(code)})")
+        self.code = code
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("T", "d_model", "n_experts", "top_k", "d_ff", "d_ff_shared", "group")]
+
+    @classmethod
+    def of(cls, shape: LayerShape, T: int):
+        return cls(T, shape.d_model, shape.n_experts, shape.top_k, shape.d_ff,
+                   shape.d_ff_shared, shape.group)
+
+
+class W4(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("bias", ctypes.c_void_p)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [(n, W4) for n in ("gate", "up", "down", "sh_gate", "sh_up", "sh_down")] + [
+        ("router", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
+        ("shared_gate", ctypes.c_void_p)]
+
+
+class ForwardViews(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "logits", "gate_logit", "topk_ids", "topk_w", "counts", "offsets", "perm", "inv_perm",
+        "row_token", "row_weight", "block_map", "num_tiles", "h", "out_acc", "status")] + [
+        ("max_tiles", ctypes.c_int32), ("block_n", ctypes.c_int32)]
+
+
+class DecodeViews(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("logits", "gate_logit", "topk_ids", "topk_w", "h", "status")]
+
+
+_lib = None
+
+
+def lib():
+    """Load the CUDA library (no fallback: a missing library is an error)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(SO_PATH):
+            raise RuntimeError(
+                f"{SO_PATH} is missing; build it with `python -m bit_moe_expert_route_gb300.build`")
+        L = ctypes.CDLL(SO_PATH)
+        vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_status_string.argtypes = [i32]
+        L.moe_version.restype = i32
+        L.moe_pick_block_n.argtypes = [i32, i32, i32]
+        L.moe_max_tiles.argtypes = [i32, i32, i32, i32, i32]
+        L.moe_route_workspace_bytes.restype = sz
+        L.moe_route_workspace_bytes.argtypes = [i32, i32]
+        L.moe_route.argtypes = [vp, vp, i32, i32, i32, i32, i32] + [vp] * 10 + [i32, vp, sz, vp]
+        L.moe_gemm_workspace_bytes.restype = sz
+        L.moe_grouped_gemm_w4a16.argtypes = [vp, i64, i32, vp, i64, vp, i32, i32, vp, vp, vp, i32,
+                                             i32, i32, vp, vp, vp, i64, i64, vp, sz, vp]
+        L.moe_workspace_bytes.restype = sz
+        L.moe_workspace_bytes.argtypes = [vp, i32]
+        L.moe_forward_views.argtypes = [vp, sz, vp, i32, vp]
+        L.moe_forward.argtypes = [vp, vp, vp, i32, vp, vp, sz, vp]
+        L.moe_decode_workspace_bytes.restype = sz
+        L.moe_decode_workspace_bytes.argtypes = [vp]
+        L.moe_decode_views.argtypes = [vp, sz, vp, vp]
+        L.moe_decode_gemv_w4.argtypes = [vp, vp, vp, vp, vp, sz, vp]
+        L.moe_get_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().moe_status_string(int(code)).decode()
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise MoeError(fn, rc)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def device_status(ws: torch.Tensor, stream=None) -> int:
+    v = ctypes.c_int32(0)
+    rc = lib().moe_get_device_status(_p(ws), _stream(stream), ctypes.byref(v))
+    if rc not in (0, -6):
+        raise MoeError("moe_get_device_status", rc)
+    return int(v.value)
+
+
+# ------------------------------------------------------------------ weights on the device
+def to_device(a, device="cuda") -> torch.Tensor | None:
+    """numpy -> device tensor with the same bytes (uint16 -> int16, uint32 -> int32)."""
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    elif a.dtype == np.uint32:
+        a = a.view(np.int32)
+    return torch.from_numpy(a).to(device)
+
+
+class DeviceLayer:
+    """One layer's weights resident on the GPU plus the moe_weights_t that points at them."""
+
+    def __init__(self, host: dict, shape: LayerShape, device="cuda"):
+        self.shape = shape
+        self.t = {}
+        for name in ("gate", "up", "down", "sh_gate", "sh_up", "sh_down"):
+            w = host.get(name)
+            self.t[name] = None if w is None else tuple(to_device(a, device) for a in w)
+        for name in ("router", "router_bias", "shared_gate"):
+            self.t[name] = to_device(host.get(name), device)
+        W = Weights()
+        for name in ("gate", "up", "down", "sh_gate", "sh_up", "sh_down"):
+            w = self.t[name]
+            if w is not None:
+                setattr(W, name, W4(w[0].data_ptr(), w[1].data_ptr(), w[2].data_ptr()))
+        W.router = self.t["router"].data_ptr()
+        W.router_bias = None if self.t["router_bias"] is None else self.t["router_bias"].data_ptr()
+        W.shared_gate = None if self.t["shared_gate"] is None else self.t["shared_gate"].data_ptr()
+        self.weights = W
+
+    @property
+    def nbytes(self) -> int:
+        n = 0
+        for v in self.t.values():
+            if v is None:
+                continue
+            for a in (v if isinstance(v, tuple) else (v,)):
+                n += a.numel() * a.element_size()
+        return n
+
+
+# ------------------------------------------------------------------ entry points
+def max_tiles(T, n_experts, top_k, block_n, with_shared=True) -> int:
+    return lib().moe_max_tiles(T, n_experts, top_k, block_n, int(with_shared))
+
+
+def pick_block_n(T, n_experts, top_k) -> int:
+    return lib().moe_pick_block_n(T, n_experts, top_k)
+
+
+def route(logits: torch.Tensor, top_k: int, block_n: int, with_shared: bool = True,
+          bias: torch.Tensor | None = None, stream=None) -> dict:
+    """moe_route on fp32 logits [T, E]; returns the routing arrays as device tensors."""
+    T, E = logits.shape
+    dev = logits.device
+    mt = max_tiles(T, E, top_k, block_n, with_shared)
+    i32 = dict(dtype=torch.int32, device=dev)
+    r = dict(
+        topk_ids=torch.empty(T, top_k, **i32),
+        topk_w=torch.empty(T, top_k, dtype=torch.float32, device=dev),
+        counts=torch.empty(E, **i32),
+        offsets=torch.empty(E + 1, **i32),
+        perm=torch.empty(T * top_k, **i32),
+        inv_perm=torch.empty(T * top_k, **i32),
+        row_token=torch.empty(T * top_k + (T if with_shared else 0), **i32),
+        row_weight=torch.empty(T * top_k, dtype=torch.float32, device=dev),
+        block_map=torch.zeros(max(mt, 1), 4, **i32),
+        num_tiles=torch.zeros(1, **i32),
+    )
+    ws = workspace(lib().moe_route_workspace_bytes(T, E), dev)
+    rc = lib().moe_route(
+        _p(logits), _p(bias), T, E, top_k, block_n, int(with_shared), _p(r["topk_ids"]),
+        _p(r["topk_w"]), _p(r["counts"]), _p(r["offsets"]), _p(r["perm"]), _p(r["inv_perm"]),
+        _p(r["row_token"]), _p(r["row_weight"]), _p(r["block_map"]), _p(r["num_tiles"]), mt,
+        _p(ws), ws.numel(), _stream(stream))
+    _check("moe_route", rc)
+    r["max_tiles"] = mt
+    r["ws"] = ws
+    return r
+
+
+def grouped_gemm_w4a16(A, W, n_groups, N, block_map, num_tiles, max_tiles_, block_n, epilogue,
+                       row_index=None, n_rows=None, W_extra=None, row_scale=None, out_row=None,
+                       C=None, C_rows=None, stream=None):
+    """moe_grouped_gemm_w4a16. W / W_extra: list of (q, scale, bias) device tensors."""
+    A_rows, K = A.shape
+    if n_rows is None:
+        n_rows = row_index.numel() if row_index is not None else A_rows
+    Ws = (W4 * len(W))(*[W4(q.data_ptr(), s.data_ptr(), b.data_ptr()) for q, s, b in W])
+    Wx = None
+    if W_extra is not None:
+        Wx = (W4 * len(W_extra))(*[W4(q.data_ptr(), s.data_ptr(), b.data_ptr())
+                                  for q, s, b in W_extra])
+    if C is None:
+        dt = torch.bfloat16 if epilogue == EPI_SWIGLU else torch.float32
+        C = torch.zeros(C_rows if C_rows is not None else n_rows, N, dtype=dt, device=A.device)
+    ws = workspace(lib().moe_gemm_workspace_bytes(), A.device)
+    rc = lib().moe_grouped_gemm_w4a16(
+        _p(A), A_rows, K, _p(row_index), n_rows, ctypes.cast(Ws, ctypes.c_void_p), n_groups, N,
+        None if Wx is None else ctypes.cast(Wx, ctypes.c_void_p), _p(block_map), _p(num_tiles),
+        max_tiles_, block_n, epilogue, _p(row_scale), _p(out_row), _p(C), C.shape[0],
+        C.stride(0), _p(ws), ws.numel(), _stream(stream))
+    _check("moe_grouped_gemm_w4a16", rc)
+    return C, ws
+
+
+class Forward:
+    """moe_forward with a reusable workspace for one (shape, T, block_n)."""
+
+    def __init__(self, layer: DeviceLayer, T: int, block_n: int = 0, device="cuda"):
+        self.layer = layer
+        self.T = T
+        self.shape = Shape.of(layer.shape, T)
+        self.block_n = block_n or pick_block_n(T, layer.shape.n_experts, layer.shape.top_k)
+        nbytes = lib().moe_workspace_bytes(ctypes.byref(self.shape), self.block_n)
+        if nbytes == 0:
+            raise MoeError("moe_workspace_bytes", -3)
+        self.ws = workspace(nbytes, device)
+        self.views = ForwardViews()
+        _check("moe_forward_views", lib().moe_forward_views(
+            _p(self.ws), self.ws.numel(), ctypes.byref(self.shape), self.block_n,
+            ctypes.byref(self.views)))
+
+    def __call__(self, x: torch.Tensor, out: torch.Tensor | None = None, stream=None):
+        if out is None:
+            out = torch.empty(self.T, self.layer.shape.d_model, dtype=torch.bfloat16,
+                              device=x.device)
+        rc = lib().moe_forward(_p(x), ctypes.byref(self.layer.weights), ctypes.byref(self.shape),
+                               self.block_n, _p(out), _p(self.ws), self.ws.numel(),
+                               _stream(stream))
+        _check("moe_forward", rc)
+        return out
+
+    def view(self, name: str, shape, dtype) -> torch.Tensor:
+        """A device tensor aliasing one of the workspace intermediates."""
+        base = self.ws.data_ptr()
+        off = getattr(self.views, name) - base
+        n = int(np.prod(shape))
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return self.ws[off:off + nbytes].view(dtype).view(*shape)
+
+
+class Decode:
+    """moe_decode_gemv_w4 (T = 1) with a reusable workspace."""
+
+    def __init__(self, layer: DeviceLayer, device="cuda"):
+        self.layer = layer
+        self.shape = Shape.of(layer.shape, 1)
+        nbytes = lib().moe_decode_workspace_bytes(ctypes.byref(self.shape))
+        if nbytes == 0:
+            raise MoeError("moe_decode_workspace_bytes", -3)
+        self.ws = workspace(nbytes, device)
+        self.views = DecodeViews()
+        _check("moe_decode_views", lib().moe_decode_views(
+            _p(self.ws), self.ws.numel(), ctypes.byref(self.shape), ctypes.byref(self.views)))
+
+    def __call__(self, x: torch.Tensor, out: torch.Tensor | None = None, stream=None):
+        if out is None:
+            out = torch.empty(self.layer.shape.d_model, dtype=torch.bfloat16, device=x.device)
+        rc = lib().moe_decode_gemv_w4(_p(x), ctypes.byref(self.layer.weights),
+                                      ctypes.byref(self.shape), _p(out), _p(self.ws),
+                                      self.ws.numel(), _stream(stream))
+        _check("moe_decode_gemv_w4", rc)
+        return out
+
+    def view(self, name: str, shape, dtype) -> torch.Tensor:
+        off = getattr(self.views, name) - self.ws.data_ptr()
+        n = int(np.prod(shape))
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return self.ws[off:off + nbytes].view(dtype).view(*shape)

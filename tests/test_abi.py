@@ -1,0 +1,109 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/moe.h declares, and rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from bit_moe_expert_route_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()
+    from bit_moe_expert_route_gb300 import ops
+    return ops.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(moe_[a-z0-9_]+)\s*\(",
+                       src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for fn in ("moe_route", "moe_grouped_gemm_w4a16", "moe_forward", "moe_decode_gemv_w4"):
+        assert fn in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_status_strings(L):
+    from bit_moe_expert_route_gb300 import ops
+    assert ops.status_string(0) == "ok"
+    for code in (-1, -2, -3, -4, -5, -6, -7, 101, 102, 103, 104):
+        assert ops.status_string(code) not in ("", "unknown status")
+    assert ops.status_string(12345) == "unknown status"
+
+
+def test_block_n_and_tile_bounds(L):
+    from bit_moe_expert_route_gb300 import ops
+    assert ops.pick_block_n(64, 256, 8) == 16
+    assert ops.pick_block_n(512, 256, 8) == 16
+    assert ops.pick_block_n(4096, 256, 8) == 128
+    assert ops.pick_block_n(32768, 256, 8) == 128
+    assert ops.max_tiles(3, 4, 2, 2, True) == 3 + 4 + 2
+    assert ops.max_tiles(32768, 256, 8, 128, True) == 2048 + 256 + 256
+
+
+def test_workspace_sizes(L):
+    from bit_moe_expert_route_gb300 import ops
+    from bit_moe_expert_route_gb300.synth import LayerShape
+    sh = ops.Shape.of(LayerShape(), 4096)
+    n = L.moe_workspace_bytes(ctypes.byref(sh), 128)
+    T, E, k, d, f = 4096, 256, 8, 2048, 512
+    assert n >= T * E * 4 + (T * k + T) * f * 2 + T * d * 4
+    assert n % 256 == 0
+    bad = ops.Shape(4096, 2048, 256, 8, 512, 512, 32)  # group 32 unsupported
+    assert L.moe_workspace_bytes(ctypes.byref(bad), 128) == 0
+    assert L.moe_workspace_bytes(ctypes.byref(sh), 48) == 0  # block_n 48 unsupported
+    assert L.moe_decode_workspace_bytes(ctypes.byref(ops.Shape.of(LayerShape(), 1))) > 0
+    assert L.moe_route_workspace_bytes(32768, 256) >= 256 * 256 * 4
+
+
+def test_bad_arguments_are_rejected_on_the_host(L):
+    vp = ctypes.c_void_p
+    fake = vp(0x10000)  # never dereferenced: every call below fails validation first
+    # unsupported top_k
+    assert L.moe_route(fake, None, 8, 16, 17, 16, 1, *([fake] * 10), 100, fake, 1 << 20,
+                       None) == -3
+    # unsupported block_n
+    assert L.moe_route(fake, None, 8, 16, 2, 24, 1, *([fake] * 10), 100, fake, 1 << 20,
+                       None) == -3
+    # max_tiles below the bound
+    assert L.moe_route(fake, None, 8, 16, 2, 16, 1, *([fake] * 10), 1, fake, 1 << 20,
+                       None) == -3
+    # NULL output
+    assert L.moe_route(fake, None, 8, 16, 2, 16, 1, *([fake] * 9), None, 100, fake, 1 << 20,
+                       None) == -1
+    # workspace too small
+    assert L.moe_route(fake, None, 8, 16, 2, 16, 1, *([fake] * 10), 100, fake, 16, None) == -4
+    # misaligned workspace
+    assert L.moe_route(fake, None, 8, 16, 2, 16, 1, *([fake] * 10), 100, vp(0x10004), 1 << 20,
+                       None) == -4
+    # grouped GEMM: N not a multiple of 128, bad epilogue, misaligned A
+    W = (ctypes.c_void_p * 3)(0x10000, 0x10000, 0x10000)
+    args = lambda A, N, epi: (A, 10, 128, None, 10, ctypes.cast(W, vp), 4, N, None, fake, fake,
+                              10, 16, epi, fake, fake, fake, 10, N, fake, 1 << 20, None)
+    assert L.moe_grouped_gemm_w4a16(*args(fake, 100, 0)) == -3
+    assert L.moe_grouped_gemm_w4a16(*args(fake, 128, 7)) == -3
+    assert L.moe_grouped_gemm_w4a16(*args(vp(0x10002), 128, 0)) == -2
+    # forward: NULL weights, bad shape
+    from bit_moe_expert_route_gb300 import ops
+    sh = ops.Shape(4, 2048, 256, 8, 512, 512, 64)
+    assert L.moe_forward(fake, None, ctypes.byref(sh), 0, fake, fake, 1 << 30, None) == -1
+    sh_bad = ops.Shape(4, 2000, 256, 8, 512, 512, 64)
+    assert L.moe_forward(fake, None, ctypes.byref(sh_bad), 0, fake, fake, 1 << 30, None) == -3
+    # decode requires T == 1
+    sh2 = ops.Shape(2, 2048, 256, 8, 512, 512, 64)
+    assert L.moe_decode_gemv_w4(fake, None, ctypes.byref(sh2), fake, fake, 1 << 20, None) == -3

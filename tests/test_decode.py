@@ -1,0 +1,86 @@
+"""moe_decode_gemv_w4 (T = 1) against the oracle.
+
+The GPU's fp32 router logits are checked against the oracle's (they differ
+only in summation order), then the oracle runs the layer on the GPU's logits
+so both sides take the same top-k decision; ids must match exactly and the
+bf16 output must satisfy max|err| <= 2e-2 rms(ref), rel-L2 <= 5e-3."""
+import numpy as np
+import pytest
+
+from bit_moe_expert_route_gb300 import synth
+from gpu_util import FULL, bf16_np, to_np, tolerance_check
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def layer():
+    from bit_moe_expert_route_gb300 import ops
+    host = synth.layer_weights(FULL, seed=0, layer=0)
+    return host, ops.DeviceLayer(host, FULL)
+
+
+def check_one(orc, host, dec, x):
+    out = dec(torch.from_numpy(x.view(np.int16)).cuda().view(-1))
+    torch.cuda.synchronize()
+    from bit_moe_expert_route_gb300 import ops
+    assert ops.device_status(dec.ws) == 0
+    lg = to_np(dec.view("logits", (1, FULL.n_experts), torch.float32))
+    ids = to_np(dec.view("topk_ids", (1, FULL.top_k), torch.int32))
+    ref_free = orc.moe_forward(x, host, FULL)
+    np.testing.assert_allclose(lg, ref_free["logits"], rtol=1e-5, atol=2e-5)
+    ref = orc.moe_forward(x, host, FULL, logits_in=lg)
+    assert np.array_equal(ids, ref["ids"])
+    w = to_np(dec.view("topk_w", (1, FULL.top_k + 1), torch.float32))
+    np.testing.assert_allclose(w[:, :FULL.top_k], ref["w"], rtol=2e-6)
+    np.testing.assert_allclose(w[0, FULL.top_k], ref["gate"][0], rtol=2e-6)
+    ok, info = tolerance_check(bf16_np(out).reshape(1, -1), ref["out"])
+    assert ok, info
+
+
+def test_decode_matches_oracle(orc, layer):
+    from bit_moe_expert_route_gb300 import ops
+    host, dl = layer
+    dec = ops.Decode(dl)
+    for step in range(3):
+        x = synth.tokens(FULL, 1, seed=0, layer=0, off=step, tensor=synth.X_DECODE)
+        check_one(orc, host, dec, x)
+
+
+def test_decode_graph_replay_matches_eager(layer):
+    from bit_moe_expert_route_gb300 import ops
+    host, dl = layer
+    dec = ops.Decode(dl)
+    x = torch.from_numpy(synth.tokens(FULL, 1, seed=1).view(np.int16)).cuda().view(-1)
+    eager = dec(x).clone()
+    out = torch.empty_like(eager)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        dec(x, out)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        dec(x, out)
+    out.zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+
+
+def test_decode_without_shared_expert(orc):
+    from bit_moe_expert_route_gb300 import ops
+    from bit_moe_expert_route_gb300.synth import LayerShape
+    shape = LayerShape(d_model=256, n_experts=32, top_k=4, d_ff=128, d_ff_shared=128)
+    host = synth.layer_weights(shape, seed=5, shared=False)
+    dl = ops.DeviceLayer(host, shape)
+    dec = ops.Decode(dl)
+    x = synth.tokens(shape, 1, seed=5)
+    out = dec(torch.from_numpy(x.view(np.int16)).cuda().view(-1))
+    torch.cuda.synchronize()
+    lg = to_np(dec.view("logits", (1, 32), torch.float32))
+    ref = orc.moe_forward(x, host, shape, logits_in=lg)
+    ok, info = tolerance_check(bf16_np(out).reshape(1, -1), ref["out"])
+    assert ok, info
