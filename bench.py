@@ -1,0 +1,471 @@
+#!/usr/bin/env python3
+"""Benchmark of the 4-bit MoE layer on GB300.
+
+Headline workload (one JSON line on rank 0): batch-1 decode through 40
+independent MoE layers of the Qwen3.6-35B-A3B-style shape (d_model 2048, 256
+experts, top-8, d_ff 512, one shared expert, group-64 affine 4-bit weights;
+distinct seeded weights per layer, ~18 GB resident so L2 cannot hold them),
+a fresh token per layer per step. One step = one token through all 40 layers
+(router GEMV + top-8, gate/up GEMV + SwiGLU, down GEMV + weighted combine for
+the 8 routed and the shared expert). metric = tokens/s.
+
+The same line carries the prefill configurations (T = 512, 4096, 32768 with a
+Zipf router bias) under "prefill", each with its own tensor-pipe roofline.
+
+--impl reference times the CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s (batch-1 decode, 40 layers) at 1 GB300 + % roofline"
+N_LAYERS = 40
+SELECTED_BYTES_PER_LAYER = 9 * 1_769_472      # 8 routed + shared expert: q + scale + bias
+ROUTER_BYTES_PER_LAYER = 2048 * 256 * 4 + 2048 * 4
+FLOP_PER_TOKEN = 9 * 3 * 2 * 2048 * 512        # 56,623,104
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill configurations")
+    ap.add_argument("--prefill-iters", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world):
+    import torch
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period}"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            m = json.load(f)
+        return dict(hbm_gbs=float(m["hbm_gbs"]), bf16=float(m["bf16_tflops"]),
+                    bf16_sustained=float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
+                    source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------ helpers
+def gpu_graph(fn, stream):
+    """Capture fn() (a sequence of library calls) into a CUDA graph on `stream`."""
+    import torch
+    with torch.cuda.stream(stream):
+        fn()  # warm-up outside capture (sets kernel attributes, loads modules)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def timed_replays(g, stream, iters, flush):
+    """Per-iteration device time of a graph replay, L2 flushed before each one.
+    The flush is enqueued before the start event, so it also keeps the GPU busy
+    while the replay is being issued."""
+    import torch
+    times = []
+    with torch.cuda.stream(stream):
+        for _ in range(iters):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            times.append((e0, e1))
+    stream.synchronize()
+    return [a.elapsed_time(b) * 1e-3 for a, b in times]
+
+
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+# ------------------------------------------------------------------ decode (headline)
+def decode_layers(shape, seed, n_layers, keep_host):
+    from bit_moe_expert_route_gb300 import ops, synth
+    layers, decs, hosts = [], [], []
+    for l in range(n_layers):
+        host = synth.layer_weights(shape, seed=seed, layer=l)
+        dl = ops.DeviceLayer(host, shape)
+        layers.append(dl)
+        decs.append(ops.Decode(dl))
+        if l < keep_host:
+            hosts.append(host)
+    return layers, decs, hosts
+
+
+def run_decode(args, world, peaks):
+    import numpy as np
+    import torch
+    from bit_moe_expert_route_gb300 import synth
+    shape = synth.LayerShape()
+    d, L = shape.d_model, N_LAYERS
+    keep = 0 if args.no_cpu_baseline or world > 1 else 2
+    layers, decs, hosts = decode_layers(shape, seed=0, n_layers=L, keep_host=keep)
+    nsteps = args.warmup + args.steps
+    x_host = torch.empty(nsteps, L, d, dtype=torch.int16).pin_memory()
+    for l in range(L):
+        xs = synth.tokens(shape, nsteps, seed=0, layer=l, tensor=synth.X_DECODE)
+        x_host[:, l].copy_(torch.from_numpy(xs.view(np.int16)))
+    x_dev = x_host.cuda()
+    x_stage = torch.empty(L, d, dtype=torch.int16, device="cuda")
+    out_stage = torch.empty(L, d, dtype=torch.int16, device="cuda")
+    out_host = torch.empty(nsteps, L, d, dtype=torch.int16).pin_memory()
+    stream = torch.cuda.Stream()
+
+    def step():
+        for l in range(L):
+            decs[l](x_stage[l], out_stage[l].view(torch.bfloat16))
+
+    g = gpu_graph(step, stream)
+    with torch.cuda.stream(stream):
+        for s in range(args.warmup):
+            x_stage.copy_(x_dev[s], non_blocking=True)
+            g.replay()
+    stream.synchronize()
+
+    # device-resident inputs: K steps between two events
+    clocks = ClockSampler(torch.cuda.current_device())
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for s in range(args.warmup, nsteps):
+            x_stage.copy_(x_dev[s], non_blocking=True)
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    t_dev = max_over_ranks(e0.elapsed_time(e1) * 1e-3, world)
+
+    # end to end: pinned host input -> device, layers, device -> pinned host output
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for s in range(args.warmup, nsteps):
+            x_stage.copy_(x_host[s], non_blocking=True)
+            g.replay()
+            out_host[s].copy_(out_stage, non_blocking=True)
+        f1.record(stream)
+    stream.synchronize()
+    t_e2e = max_over_ranks(f0.elapsed_time(f1) * 1e-3, world)
+    assert bool(torch.isfinite(out_stage.view(torch.bfloat16).float()).all())
+
+    K = args.steps
+    step_s = t_dev / K
+    achieved = L * SELECTED_BYTES_PER_LAYER / step_s / 1e9
+    res = dict(
+        value=world * K / t_dev, ms_per_step=step_s * 1e3,
+        e2e=dict(value=world * K / t_e2e, unit="tokens/s", h2d_bytes_per_step=L * d * 2,
+                 d2h_bytes_per_step=L * d * 2),
+        gpu_launches=3 * L * K,
+        roofline=dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"],
+                      unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4),
+                      traffic=TRAFFIC.get("decode_layer"),
+                      kernel="decode layer: router GEMV+top-8, gate/up GEMV+SwiGLU, "
+                             "down GEMV+combine (3 launches)",
+                      bytes_per_layer=SELECTED_BYTES_PER_LAYER,
+                      router_bytes_per_layer_not_counted=ROUTER_BYTES_PER_LAYER,
+                      peak_source=peaks["source"]),
+        clocks=clk,
+    )
+    if keep:
+        res["cpu_baseline"] = decode_cpu_baseline(hosts, shape)
+    del layers, decs, g
+    torch.cuda.empty_cache()
+    return res
+
+
+def decode_cpu_baseline(hosts, shape, steps_per_layer=48):
+    """The oracle on a bounded sample: `steps_per_layer` decode tokens through each
+    kept layer (tokens are independent, so the oracle's OpenMP loop spreads them
+    over the host cores). Reported as tokens/s through 40 layers."""
+    from bit_moe_expert_route_gb300 import synth
+    from oracle import Oracle
+    orc = Oracle()
+    t = 0.0
+    n = 0
+    for l, host in enumerate(hosts):
+        x = synth.tokens(shape, steps_per_layer, seed=0, layer=l, tensor=synth.X_DECODE)
+        t0 = time.perf_counter()
+        orc.moe_forward(x, host, shape)
+        t += time.perf_counter() - t0
+        n += steps_per_layer
+    per_token_40 = t / n * N_LAYERS
+    return dict(value=round(1.0 / per_token_40, 4), unit="tokens/s", cores=os.cpu_count(),
+                kind="oracle", cpu=cpu_model(),
+                sample=f"{len(hosts)} layers x {steps_per_layer} decode tokens, oracle "
+                       f"(fp64, OpenMP over tokens), {t:.1f} s; scaled to 40 layers")
+
+
+# ------------------------------------------------------------------ prefill configurations
+def run_prefill(T, zipf, host0, args, peaks):
+    import numpy as np
+    import torch
+    from bit_moe_expert_route_gb300 import ops, synth
+    shape = synth.LayerShape()
+    E, k, d, f = shape.n_experts, shape.top_k, shape.d_model, shape.d_ff
+    host = dict(host0, router_bias=synth.zipf_router_bias(E) if zipf else None)
+    dl = ops.DeviceLayer(host, shape)
+    fwd = ops.Forward(dl, T)
+    x = torch.from_numpy(synth.tokens(shape, T, seed=0).view(np.int16)).cuda()
+    out = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.Stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")  # > L2 (129 MB)
+    g = gpu_graph(lambda: fwd(x, out), stream)
+    for _ in range(3):
+        g.replay()
+    t_layer = statistics.median(timed_replays(g, stream, args.prefill_iters, flush))
+
+    rows = T * k + T
+    mt, bn = fwd.views.max_tiles, fwd.block_n
+    bm = fwd.view("block_map", (mt, 4), torch.int32)
+    nt = fwd.view("num_tiles", (1,), torch.int32)
+    rt = fwd.view("row_token", (rows,), torch.int32)
+    h = fwd.view("h", (rows, f), torch.bfloat16)
+    rw = fwd.view("row_weight", (rows,), torch.float32)
+    acc = fwd.view("out_acc", (T, d), torch.float32)
+    t = dl.t
+    g1 = gpu_graph(lambda: ops.grouped_gemm_w4a16(
+        x, [t["gate"], t["up"]], E, f, bm, nt, mt, bn, ops.EPI_SWIGLU, row_index=rt, n_rows=rows,
+        W_extra=[t["sh_gate"], t["sh_up"]], C=h), stream)
+    g2 = gpu_graph(lambda: ops.grouped_gemm_w4a16(
+        h, [t["down"]], E, d, bm, nt, mt, bn, ops.EPI_COMBINE, n_rows=rows,
+        W_extra=[t["sh_down"]], row_scale=rw, out_row=rt, C=acc), stream)
+    t1 = statistics.median(timed_replays(g1, stream, args.prefill_iters, flush))
+    t2 = statistics.median(timed_replays(g2, stream, args.prefill_iters, flush))
+    f1 = 2 * 2 * d * f * rows
+    f2 = 2 * f * d * rows
+    achieved = (f1 + f2) / (t1 + t2) / 1e12
+    counts = fwd.view("counts", (E,), torch.int32).cpu().numpy()
+    weight_bytes = 257 * 1_769_472
+    res = dict(
+        T=T, router_bias="zipf 1.5*ln(1/rank)" if zipf else None, block_n=bn,
+        tokens_per_s=round(T / t_layer, 1), ms=round(t_layer * 1e3, 4),
+        layer_tflops=round(FLOP_PER_TOKEN * T / t_layer / 1e12, 2),
+        layer_frac_of_bf16_peak=round(FLOP_PER_TOKEN * T / t_layer / 1e12 / peaks["bf16"], 4),
+        weights_hbm_frac=round(weight_bytes / t_layer / 1e9 / peaks["hbm_gbs"], 4),
+        gpu_launches=7,
+        roofline=dict(bound="tensor", achieved=round(achieved, 1), peak=peaks["bf16"],
+                      unit="TFLOP/s", frac=round(achieved / peaks["bf16"], 4),
+                      traffic=TRAFFIC.get(f"gemm_T{T}"),
+                      kernel="grouped W4A16 GEMMs (gate/up+SwiGLU, down+combine)",
+                      gateup_ms=round(t1 * 1e3, 4), down_ms=round(t2 * 1e3, 4),
+                      flop_per_token=FLOP_PER_TOKEN, peak_source=peaks["source"]),
+        expert_counts=dict(min=int(counts.min()), max=int(counts.max()),
+                           zero=int((counts == 0).sum()), mean=float(counts.mean())),
+        l2="flushed (512 MB write) before every timed iteration",
+    )
+    del g, g1, g2, fwd, dl
+    torch.cuda.empty_cache()
+    return res
+
+
+# ------------------------------------------------------------------ reference arm (CPU oracle)
+def reference_arm(args):
+    """The oracle, as it stands, on the host cores: each step is one decode token
+    through one layer (layers cycled), steps spread over a thread pool (the
+    oracle releases the GIL); tokens/s is scaled to 40 layers."""
+    os.environ["OMP_NUM_THREADS"] = "1"
+    import concurrent.futures as cf
+    from bit_moe_expert_route_gb300 import synth
+    from oracle import Oracle
+    shape = synth.LayerShape()
+    orc = Oracle()
+    n_host = 4
+    hosts = [synth.layer_weights(shape, seed=0, layer=l) for l in range(n_host)]
+    cores = os.cpu_count() or 1
+
+    def one(s):
+        l = s % n_host
+        x = synth.tokens(shape, 1, seed=0, layer=l, off=s, tensor=synth.X_DECODE)
+        orc.moe_forward(x, hosts[l], shape)
+
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        list(ex.map(one, range(args.warmup)))
+        t0 = time.perf_counter()
+        list(ex.map(one, range(args.warmup, args.warmup + args.steps)))
+        wall = time.perf_counter() - t0
+    value = args.steps / wall / N_LAYERS
+    return {
+        "impl": "reference", "metric": BASELINE_METRIC, "value": round(value, 4),
+        "unit": "tokens/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(wall / args.steps * N_LAYERS * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": CONFIG,
+        "cpu_baseline": dict(value=round(value, 4), unit="tokens/s", cores=cores, kind="oracle",
+                             cpu=cpu_model(),
+                             sample=f"{args.steps} decode tokens, each through one of {n_host} "
+                                    "layers (cycled), scaled to 40 layers"),
+        "e2e": dict(value=round(value, 4), unit="tokens/s", h2d_bytes_per_step=0,
+                    d2h_bytes_per_step=0),
+    }
+
+
+BASELINE_METRIC = "MoE-layer tokens/s (prefill T=512/4096/32768; batch-1 decode) at 1 GB300 + % roofline"
+CONFIG = {
+    "workload": "batch-1 decode: T=1 through 40 independent MoE layers (d_model 2048, 256 experts, "
+                "top-8, d_ff 512, shared expert 512, group-64 affine 4-bit weights; distinct seeded "
+                "weights per layer, ~18 GB resident), fresh token per layer per step",
+    "layers": N_LAYERS, "tokens_per_step": 1, "l2": "weights (18 GB) larger than L2",
+    "parallelism": "replicas",
+}
+
+# DRAM bytes per launch unit from the committed ncu summaries (profiles/); None
+# until counters for the current kernels are taken.
+TRAFFIC: dict = {}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(args)), flush=True)
+        return 0
+    import torch
+    torch.cuda.set_device(local)
+    dist_init(world)
+    from bit_moe_expert_route_gb300 import build as B
+    if rank == 0 and not B.up_to_date():
+        B.build()
+    barrier(world)
+    peaks = measured_peaks()
+    res = run_decode(args, world, peaks)
+    prefill = []
+    if not args.no_prefill:
+        from bit_moe_expert_route_gb300 import synth
+        host0 = synth.layer_weights(synth.LayerShape(), seed=0, layer=0)
+        for T, zipf in ((512, False), (4096, False), (32768, True)):
+            prefill.append(run_prefill(T, zipf, host0, args, peaks))
+    line = {
+        "metric": BASELINE_METRIC, "value": round(res["value"], 2), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(res["ms_per_step"], 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "w4a16 (fp32 accumulate)",
+        "data": "synthetic (seeded generators; random-init weights of the layer shape)",
+        "config": CONFIG, "e2e": res["e2e"], "gpu_launches": res["gpu_launches"],
+        "roofline": res["roofline"], "clocks": res["clocks"],
+    }
+    if "cpu_baseline" in res:
+        line["cpu_baseline"] = res["cpu_baseline"]
+    if prefill:
+        line["prefill"] = prefill
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    barrier(world)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

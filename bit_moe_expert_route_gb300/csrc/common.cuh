@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "moe.h"
 
@@ -215,6 +216,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | (1u << 7)                      // A format: bf16
          | (1u << 10)                     // B format: bf16
          | ((uint32_t)(N >> 3) << 17)     // N / 8
+         | ((uint32_t)(M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor, kind::f16: f16 A and B, fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4)                        // D format: f32
+         | ((uint32_t)(N >> 3) << 17)     // N / 8   (A, B format 0 = f16)
          | ((uint32_t)(M >> 4) << 24);    // M / 16
 }
 

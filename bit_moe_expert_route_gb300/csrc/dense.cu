@@ -19,7 +19,8 @@ constexpr int kRK = 32;   // K step
 // owns tokens ty*8..ty*8+7 and experts tx*4..tx*4+3 of the CTA tile.
 __global__ void __launch_bounds__(256) router_gemm_kernel(const uint16_t* __restrict__ x,
                                                           const float* __restrict__ Wr, int T,
-                                                          int d, int E, float* __restrict__ logits) {
+                                                          int d, int E, float* __restrict__ logits,
+                                                          uint16_t* __restrict__ x16) {
   __shared__ __align__(16) float xs[kRK][kRM];
   __shared__ __align__(16) float ws[kRK][kRN];
   const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
@@ -31,6 +32,17 @@ __global__ void __launch_bounds__(256) router_gemm_kernel(const uint16_t* __rest
       uint4 v = make_uint4(0, 0, 0, 0);
       if (m0 + r < T) v = *reinterpret_cast<const uint4*>(x + (size_t)(m0 + r) * d + k0 + c);
       const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+      if (x16 && blockIdx.x == 0 && m0 + r < T) {  // f16 copy of x for the tensor-core path
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float lo = fminf(fmaxf(__uint_as_float(u[i] << 16), -65504.f), 65504.f);
+          const float hi = fminf(fmaxf(__uint_as_float(u[i] & 0xFFFF0000u), -65504.f), 65504.f);
+          const __half2 h2 = __floats2half2_rn(lo, hi);
+          o[i] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        *reinterpret_cast<uint4*>(x16 + (size_t)(m0 + r) * d + k0 + c) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         xs[c + 2 * i][r] = __uint_as_float(u[i] << 16);
@@ -85,9 +97,9 @@ __global__ void f32_to_bf16_kernel(const float4* __restrict__ in, uint2* __restr
 }  // namespace
 
 cudaError_t router_gemm_launch(const uint16_t* x, const float* Wr, int T, int d, int E,
-                               float* logits, cudaStream_t s) {
+                               float* logits, uint16_t* x16, cudaStream_t s) {
   dim3 grid((E + kRN - 1) / kRN, (T + kRM - 1) / kRM);
-  router_gemm_kernel<<<grid, 256, 0, s>>>(x, Wr, T, d, E, logits);
+  router_gemm_kernel<<<grid, 256, 0, s>>>(x, Wr, T, d, E, logits, x16);
   return cudaGetLastError();
 }
 

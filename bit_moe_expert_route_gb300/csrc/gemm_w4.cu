@@ -122,7 +122,52 @@ MOE_DEVINL uint4 dequant_word(uint32_t w, __nv_bfloat162 s2, __nv_bfloat162 b2) 
   return o;
 }
 
-template <int BN, int NMAT, int EPI>
+// Same, into f16: 0x6400 | q is 1024 + q exactly; minus 1024 gives q; then
+// RNE_f16(scale * q + bias) with one fused f16x2 fma.
+MOE_DEVINL uint4 dequant_word_f16(uint32_t w, __half2 s2, __half2 b2) {
+  const __half2 m1024 = __floats2half2_rn(-1024.f, -1024.f);
+  const __half2 one = __floats2half2_rn(1.f, 1.f);
+  uint32_t p[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t v = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;  // {1024+q_i, 1024+q_{i+4}}
+    __half2 q2 = __hfma2(*reinterpret_cast<const __half2*>(&v), one, m1024);
+    __half2 r = __hfma2(s2, q2, b2);
+    p[i] = *reinterpret_cast<uint32_t*>(&r);
+  }
+  uint4 o;
+  o.x = __byte_perm(p[0], p[1], 0x5410);
+  o.y = __byte_perm(p[2], p[3], 0x5410);
+  o.z = __byte_perm(p[0], p[1], 0x7632);
+  o.w = __byte_perm(p[2], p[3], 0x7632);
+  return o;
+}
+
+// bf16 bit pattern -> operand-format pair {v, v}
+template <bool F16>
+MOE_DEVINL uint32_t splat_operand(uint16_t bf16_bits) {
+  if constexpr (F16) {
+    const __half h = __float2half_rn(__uint_as_float((uint32_t)bf16_bits << 16));
+    const uint16_t hb = *reinterpret_cast<const uint16_t*>(&h);
+    return (uint32_t)hb * 0x10001u;
+  } else {
+    return (uint32_t)bf16_bits * 0x10001u;
+  }
+}
+
+// fp32 -> operand-format bits (RNE); f16 saturates to the largest finite value.
+template <bool F16>
+MOE_DEVINL uint16_t to_operand(float v) {
+  if constexpr (F16) {
+    const __half h = __float2half_rn(fminf(fmaxf(v, -65504.f), 65504.f));
+    return *reinterpret_cast<const uint16_t*>(&h);
+  } else {
+    const __nv_bfloat16 b = __float2bfloat16_rn(v);
+    return *reinterpret_cast<const uint16_t*>(&b);
+  }
+}
+
+template <int BN, int NMAT, int EPI, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_constant__ KParams kp) {
   using C = Cfg<BN, NMAT>;
   const GemmParams& g = kp.g;
@@ -214,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kTileM, BN);
+      constexpr uint32_t idesc = F16 ? idesc_f16_f32(kTileM, BN) : idesc_bf16_f32(kTileM, BN);
       uint32_t it = 0, acc_it = 0;
       bool alive = true;
       for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
@@ -269,13 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
         bi[j] = w.bias + row * KB;
       }
       for (int kb = 0; kb < KB; ++kb, ++it) {
-        __nv_bfloat162 s2[NMAT], b2[NMAT];
+        uint32_t s2[NMAT], b2[NMAT];
 #pragma unroll
         for (int j = 0; j < NMAT; ++j) {
-          const uint16_t sv = __ldg(sc[j] + kb), bv = __ldg(bi[j] + kb);
-          const uint32_t s32 = (uint32_t)sv * 0x10001u, b32 = (uint32_t)bv * 0x10001u;
-          s2[j] = *reinterpret_cast<const __nv_bfloat162*>(&s32);
-          b2[j] = *reinterpret_cast<const __nv_bfloat162*>(&b32);
+          s2[j] = splat_operand<F16>(__ldg(sc[j] + kb));
+          b2[j] = splat_operand<F16>(__ldg(bi[j] + kb));
         }
         const int sq = it % kSQ;
         if (!mbar_wait(&q_full[sq], (it / kSQ) & 1, abort_flag, g.status, 6)) {
@@ -302,9 +345,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
           const uint32_t words[8] = {qw[j][0].x, qw[j][0].y, qw[j][0].z, qw[j][0].w,
                                      qw[j][1].x, qw[j][1].y, qw[j][1].z, qw[j][1].w};
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(a_tile + sw128_offset(m, c)) =
-                dequant_word(words[c], s2[j], b2[j]);
+          for (int c = 0; c < 8; ++c) {
+            uint4 o;
+            if constexpr (F16)
+              o = dequant_word_f16(words[c], *reinterpret_cast<const __half2*>(&s2[j]),
+                                   *reinterpret_cast<const __half2*>(&b2[j]));
+            else
+              o = dequant_word(words[c], *reinterpret_cast<const __nv_bfloat162*>(&s2[j]),
+                               *reinterpret_cast<const __nv_bfloat162*>(&b2[j]));
+            *reinterpret_cast<uint4*>(a_tile + sw128_offset(m, c)) = o;
+          }
         }
         fence_proxy_async_smem();
         mbar_arrive(&a_full[sa]);
@@ -413,8 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
           } else if constexpr (EPI == MOE_EPI_SWIGLU) {
             const float uval = __uint_as_float(v1[i]);
             const float hval = a / (1.f + __expf(-a)) * uval;
-            const __nv_bfloat16 hb = __float2bfloat16_rn(hval);
-            static_cast<uint16_t*>(g.C)[r * g.ldc + col] = *reinterpret_cast<const uint16_t*>(&hb);
+            static_cast<uint16_t*>(g.C)[r * g.ldc + col] = to_operand<F16>(hval);
           } else {
             const int orow = __ldg(g.out_row + r);
             if (orow < 0 || orow >= g.C_rows) {
@@ -466,10 +515,10 @@ bool make_q_map(CUtensorMap* tm, const uint32_t* q, int64_t rows, int K) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int NMAT, int EPI>
+template <int BN, int NMAT, int EPI, bool F16>
 cudaError_t launch_t(const KParams& kp, cudaStream_t s) {
   using C = Cfg<BN, NMAT>;
-  auto kern = gemm_w4_kernel<BN, NMAT, EPI>;
+  auto kern = gemm_w4_kernel<BN, NMAT, EPI, F16>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (err != cudaSuccess) return err;
@@ -482,13 +531,23 @@ cudaError_t launch_t(const KParams& kp, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int NMAT, int EPI>
+template <int NMAT, int EPI, bool F16>
 cudaError_t launch_bn(const KParams& kp, cudaStream_t s) {
   switch (kp.g.block_n) {
-    case 16: return launch_t<16, NMAT, EPI>(kp, s);
-    case 32: return launch_t<32, NMAT, EPI>(kp, s);
-    case 64: return launch_t<64, NMAT, EPI>(kp, s);
-    case 128: return launch_t<128, NMAT, EPI>(kp, s);
+    case 16: return launch_t<16, NMAT, EPI, F16>(kp, s);
+    case 32: return launch_t<32, NMAT, EPI, F16>(kp, s);
+    case 64: return launch_t<64, NMAT, EPI, F16>(kp, s);
+    case 128: return launch_t<128, NMAT, EPI, F16>(kp, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <bool F16>
+cudaError_t launch_epi(const KParams& kp, cudaStream_t s) {
+  switch (kp.g.epilogue) {
+    case MOE_EPI_NONE: return launch_bn<1, MOE_EPI_NONE, F16>(kp, s);
+    case MOE_EPI_SWIGLU: return launch_bn<2, MOE_EPI_SWIGLU, F16>(kp, s);
+    case MOE_EPI_COMBINE: return launch_bn<1, MOE_EPI_COMBINE, F16>(kp, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -505,12 +564,7 @@ cudaError_t gemm_w4_launch(const GemmParams& p, cudaStream_t s) {
       return cudaErrorInvalidValue;
     if (p.X[0].q && !make_q_map(&kp.tm[2 + j], p.X[j].q, p.N, p.K)) return cudaErrorInvalidValue;
   }
-  switch (p.epilogue) {
-    case MOE_EPI_NONE: return launch_bn<1, MOE_EPI_NONE>(kp, s);
-    case MOE_EPI_SWIGLU: return launch_bn<2, MOE_EPI_SWIGLU>(kp, s);
-    case MOE_EPI_COMBINE: return launch_bn<1, MOE_EPI_COMBINE>(kp, s);
-    default: return cudaErrorInvalidValue;
-  }
+  return p.operand_f16 ? launch_epi<true>(kp, s) : launch_epi<false>(kp, s);
 }
 
 }  // namespace moe

@@ -43,8 +43,9 @@ cudaError_t route_launch(const RouteParams& p, cudaStream_t s);
 
 // ---------------------------------------------------------------- router GEMM
 // logits[t][e] = sum_k x[t][k] * Wr[k][e]   (fp32 accumulate)
+// Optionally also writes x16 = f16(x) (saturated), the tensor-core operand copy.
 cudaError_t router_gemm_launch(const uint16_t* x, const float* Wr, int T, int d, int E,
-                               float* logits, cudaStream_t s);
+                               float* logits, uint16_t* x16, cudaStream_t s);
 
 // ---------------------------------------------------------------- grouped GEMM
 struct GemmW4 {
@@ -68,6 +69,7 @@ struct GemmParams {
   int max_tiles;
   int block_n;
   int epilogue;
+  int operand_f16;          // 1: A and dequantised weights are f16; 0: bf16
   const float* row_scale;
   const int32_t* out_row;
   void* C;
@@ -91,14 +93,12 @@ struct DecodeParams {
   // workspace
   float* logits;            // [E]
   float* gate_logit;        // [1]
-  float* part;              // router partial sums [nsplit][E + 1]
   int32_t* ids;             // [k]
   float* wts;               // [k]
   float* h;                 // [k+1][f]
   uint32_t* counter;        // [1] last-block-done counter (self-resetting)
   int32_t* status;
 };
-int decode_router_splits(int d);
 cudaError_t decode_launch(const DecodeParams& p, cudaStream_t s);
 
 }  // namespace moe

@@ -104,6 +104,7 @@ FwdWs forward_ws(void* ws, const moe_shape_t* s, int bn) {
   r.v.block_map = c.take<int32_t>((size_t)r.v.max_tiles * 4);
   r.v.num_tiles = c.take<int32_t>(1);
   r.blk = c.take<int32_t>((size_t)moe::route_nblk(T) * E);
+  r.v.x16 = c.take<uint16_t>((size_t)T * s->d_model);
   r.v.h = c.take<uint16_t>((size_t)rows * s->d_ff);
   r.v.out_acc = c.take<float>((size_t)T * s->d_model);
   r.bytes = c.off;
@@ -112,7 +113,6 @@ FwdWs forward_ws(void* ws, const moe_shape_t* s, int bn) {
 
 struct DecWs {
   moe_decode_views_t v;
-  float* part;
   uint32_t* counter;
   size_t bytes;
 };
@@ -129,7 +129,6 @@ DecWs decode_ws(void* ws, const moe_shape_t* s) {
   r.v.topk_ids = c.take<int32_t>(k);
   r.v.topk_w = c.take<float>(k + 1);
   r.v.h = c.take<float>((size_t)(k + 1) * s->d_ff);
-  r.part = c.take<float>((size_t)moe::decode_router_splits(s->d_model) * (E + 1));
   r.bytes = c.off;
   return r;
 }
@@ -253,10 +252,11 @@ int moe_grouped_gemm_w4a16(const uint16_t* A, int64_t A_rows, int K, const int32
                            int64_t n_rows, const moe_w4_t* W, int n_groups, int N,
                            const moe_w4_t* W_extra, const int32_t* block_map,
                            const int32_t* num_tiles, int max_tiles, int block_n, int epilogue,
-                           const float* row_scale, const int32_t* out_row, void* C,
+                           int operand_format, const float* row_scale, const int32_t* out_row, void* C,
                            int64_t C_rows, int64_t ldc, void* ws, size_t ws_bytes, void* stream) {
   if (epilogue != MOE_EPI_NONE && epilogue != MOE_EPI_SWIGLU && epilogue != MOE_EPI_COMBINE)
     return MOE_ERR_SHAPE;
+  if (operand_format != MOE_OPERAND_BF16 && operand_format != MOE_OPERAND_F16) return MOE_ERR_SHAPE;
   if (K < 64 || K % 64 || N < 128 || N % 128 || n_groups < 1 || A_rows < 0 || n_rows < 0 ||
       max_tiles < 0 || !valid_block_n(block_n, false) || ldc < N || C_rows < 0)
     return MOE_ERR_SHAPE;
@@ -298,6 +298,7 @@ int moe_grouped_gemm_w4a16(const uint16_t* A, int64_t A_rows, int K, const int32
   p.max_tiles = max_tiles;
   p.block_n = block_n;
   p.epilogue = epilogue;
+  p.operand_f16 = operand_format == MOE_OPERAND_F16 ? 1 : 0;
   p.row_scale = row_scale;
   p.out_row = out_row;
   p.C = C;
@@ -348,7 +349,8 @@ int moe_forward(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* sh
   const int64_t rows = (int64_t)T * k + (shared ? T : 0);
 
   // 1. router logits
-  if ((rc = cuda_status(moe::router_gemm_launch(x, w->router, T, d, E, v.logits, s))) != MOE_OK)
+  if ((rc = cuda_status(moe::router_gemm_launch(x, w->router, T, d, E, v.logits, v.x16, s))) !=
+      MOE_OK)
     return rc;
   // 2. top-k, shared gate, histogram, scan, scatter, block map
   moe::RouteParams rp;
@@ -381,7 +383,7 @@ int moe_forward(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* sh
   // 3. gate/up grouped GEMM with SwiGLU -> h (rows in expert order, shared rows last)
   moe::GemmParams g;
   memset(&g, 0, sizeof g);
-  g.A = x;
+  g.A = v.x16;
   g.A_rows = T;
   g.K = d;
   g.row_index = v.row_token;
@@ -399,6 +401,7 @@ int moe_forward(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* sh
   g.max_tiles = v.max_tiles;
   g.block_n = block_n;
   g.epilogue = MOE_EPI_SWIGLU;
+  g.operand_f16 = 1;
   g.C = v.h;
   g.C_rows = rows;
   g.ldc = f;
@@ -466,7 +469,6 @@ int moe_decode_gemv_w4(const uint16_t* x, const moe_weights_t* w, const moe_shap
   p.out = out;
   p.logits = dw.v.logits;
   p.gate_logit = dw.v.gate_logit;
-  p.part = dw.part;
   p.ids = dw.v.topk_ids;
   p.wts = dw.v.topk_w;
   p.h = dw.v.h;

@@ -19,6 +19,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 SO_PATH = os.path.join(_PKG, "libmoe_gb300.so")
 
 EPI_NONE, EPI_SWIGLU, EPI_COMBINE = 0, 1, 2
+OPERAND_BF16, OPERAND_F16 = 0, 1
 DEV_OK, DEV_BAD_TILE, DEV_BAD_ROW, DEV_TIMEOUT, DEV_BAD_EXPERT = 0, 1, 2, 3, 4
 
 
@@ -51,7 +52,7 @@ class Weights(ctypes.Structure):
 class ForwardViews(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "logits", "gate_logit", "topk_ids", "topk_w", "counts", "offsets", "perm", "inv_perm",
-        "row_token", "row_weight", "block_map", "num_tiles", "h", "out_acc", "status")] + [
+        "row_token", "row_weight", "block_map", "num_tiles", "x16", "h", "out_acc", "status")] + [
         ("max_tiles", ctypes.c_int32), ("block_n", ctypes.c_int32)]
 
 
@@ -82,7 +83,7 @@ def lib():
         L.moe_route.argtypes = [vp, vp, i32, i32, i32, i32, i32] + [vp] * 10 + [i32, vp, sz, vp]
         L.moe_gemm_workspace_bytes.restype = sz
         L.moe_grouped_gemm_w4a16.argtypes = [vp, i64, i32, vp, i64, vp, i32, i32, vp, vp, vp, i32,
-                                             i32, i32, vp, vp, vp, i64, i64, vp, sz, vp]
+                                             i32, i32, i32, vp, vp, vp, i64, i64, vp, sz, vp]
         L.moe_workspace_bytes.restype = sz
         L.moe_workspace_bytes.argtypes = [vp, i32]
         L.moe_forward_views.argtypes = [vp, sz, vp, i32, vp]
@@ -213,8 +214,11 @@ def route(logits: torch.Tensor, top_k: int, block_n: int, with_shared: bool = Tr
 
 def grouped_gemm_w4a16(A, W, n_groups, N, block_map, num_tiles, max_tiles_, block_n, epilogue,
                        row_index=None, n_rows=None, W_extra=None, row_scale=None, out_row=None,
-                       C=None, C_rows=None, stream=None):
-    """moe_grouped_gemm_w4a16. W / W_extra: list of (q, scale, bias) device tensors."""
+                       C=None, C_rows=None, operand=None, stream=None):
+    """moe_grouped_gemm_w4a16. W / W_extra: list of (q, scale, bias) device tensors.
+    operand: OPERAND_F16 / OPERAND_BF16; by default taken from A's dtype (float16 -> f16)."""
+    if operand is None:
+        operand = OPERAND_F16 if A.dtype == torch.float16 else OPERAND_BF16
     A_rows, K = A.shape
     if n_rows is None:
         n_rows = row_index.numel() if row_index is not None else A_rows
@@ -224,13 +228,15 @@ def grouped_gemm_w4a16(A, W, n_groups, N, block_map, num_tiles, max_tiles_, bloc
         Wx = (W4 * len(W_extra))(*[W4(q.data_ptr(), s.data_ptr(), b.data_ptr())
                                   for q, s, b in W_extra])
     if C is None:
-        dt = torch.bfloat16 if epilogue == EPI_SWIGLU else torch.float32
+        dt = torch.float32
+        if epilogue == EPI_SWIGLU:
+            dt = torch.float16 if operand == OPERAND_F16 else torch.bfloat16
         C = torch.zeros(C_rows if C_rows is not None else n_rows, N, dtype=dt, device=A.device)
     ws = workspace(lib().moe_gemm_workspace_bytes(), A.device)
     rc = lib().moe_grouped_gemm_w4a16(
         _p(A), A_rows, K, _p(row_index), n_rows, ctypes.cast(Ws, ctypes.c_void_p), n_groups, N,
         None if Wx is None else ctypes.cast(Wx, ctypes.c_void_p), _p(block_map), _p(num_tiles),
-        max_tiles_, block_n, epilogue, _p(row_scale), _p(out_row), _p(C), C.shape[0],
+        max_tiles_, block_n, epilogue, operand, _p(row_scale), _p(out_row), _p(C), C.shape[0],
         C.stride(0), _p(ws), ws.numel(), _stream(stream))
     _check("moe_grouped_gemm_w4a16", rc)
     return C, ws

@@ -77,6 +77,14 @@ enum moe_epilogue {
   MOE_EPI_COMBINE = 2  /* C fp32 [out rows][N] += row_scale[row] * (A_row . W^T)  */
 };
 
+/* Tensor-core operand type of the grouped GEMM: activations A and the
+ * dequantised weights are both of this type (fp32 accumulation). */
+enum moe_operand_format {
+  MOE_OPERAND_BF16 = 0, /* A bf16; weights RNE_bf16(scale*q + bias) */
+  MOE_OPERAND_F16 = 1   /* A f16; weights RNE_f16(scale*q + bias); values must lie within
+                           the f16 range (|v| < 65504), larger ones saturate */
+};
+
 typedef struct {
   int32_t T;           /* tokens */
   int32_t d_model;     /* hidden size (K of gate/up, N of down) */
@@ -154,7 +162,8 @@ int moe_route(const float* logits, const float* logit_bias, int T, int n_experts
  * (tcgen05) kernel: packed tiles arrive by TMA, are unpacked to bf16 in
  * shared memory and multiplied with fp32 accumulation in tensor memory.
  *
- *   A           bf16 [A_rows][K] device, row-major (K contiguous).
+ *   A           [A_rows][K] device, row-major (K contiguous), bf16 or f16 as
+ *               operand_format says (moe_operand_format).
  *   row_index   int32 [n_rows]: A row of GEMM row r; NULL = r itself.
  *   W           MOE_EPI_SWIGLU: W[0] = gate, W[1] = up; otherwise W[0].
  *               Each a stack of n_groups experts: q [n_groups][N][K/8].
@@ -166,7 +175,7 @@ int moe_route(const float* logits, const float* logit_bias, int T, int n_experts
  *   epilogue    moe_epilogue.
  *   row_scale   COMBINE: fp32 [n_rows] factor of each GEMM row.
  *   out_row     COMBINE: int32 [n_rows] destination row of each GEMM row.
- *   C           NONE: fp32 [n_rows][ldc]; SWIGLU: bf16 [n_rows][ldc];
+ *   C           NONE: fp32 [n_rows][ldc]; SWIGLU: [n_rows][ldc] of the operand type;
  *               COMBINE: fp32 [C_rows][ldc], accumulated with atomic adds
  *               (order of the adds is not fixed). ldc >= N, in elements.
  *   N           output columns (multiple of 128); K multiple of 64.
@@ -178,7 +187,7 @@ int moe_grouped_gemm_w4a16(const uint16_t* A, int64_t A_rows, int K, const int32
                            int64_t n_rows, const moe_w4_t* W, int n_groups, int N,
                            const moe_w4_t* W_extra, const int32_t* block_map,
                            const int32_t* num_tiles, int max_tiles, int block_n, int epilogue,
-                           const float* row_scale, const int32_t* out_row, void* C,
+                           int operand_format, const float* row_scale, const int32_t* out_row, void* C,
                            int64_t C_rows, int64_t ldc, void* ws, size_t ws_bytes, void* stream);
 
 /*
@@ -188,9 +197,12 @@ int moe_grouped_gemm_w4a16(const uint16_t* A, int64_t A_rows, int K, const int32
  *   x    bf16 [T][d_model] device;  out bf16 [T][d_model] device.
  *   block_n  row-tile height (16/32/64/128) or 0 for moe_pick_block_n.
  *   ws   256-byte aligned, >= moe_workspace_bytes(shape, block_n) bytes.
- * Pipeline: router GEMM -> top-k + shared gate -> histogram -> scan ->
- * scatter + block map -> grouped GEMM (gate/up + SwiGLU) -> grouped GEMM
- * (down + weighted combine) -> bf16 output. The intermediate h is bf16.
+ * Pipeline: router GEMM (also writing an f16 copy of x) -> top-k + shared
+ * gate -> histogram -> scan -> scatter + block map -> grouped GEMM (gate/up +
+ * SwiGLU) -> grouped GEMM (down + weighted combine) -> bf16 output.
+ * The grouped GEMMs use f16 tensor-core operands (MOE_OPERAND_F16): x, the
+ * dequantised weights and the intermediate h are f16 (11-bit significand),
+ * accumulation is fp32. x, the weights and h must lie within the f16 range.
  */
 size_t moe_workspace_bytes(const moe_shape_t* shape, int block_n);
 int moe_forward(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* shape, int block_n,
@@ -210,7 +222,8 @@ typedef struct {
   float* row_weight;   /* [T*k + T] routing weight, then sigmoid gate */
   int32_t* block_map;  /* [max_tiles][4] */
   int32_t* num_tiles;  /* [1] */
-  uint16_t* h;         /* bf16 [T*k + T][d_ff] */
+  uint16_t* x16;       /* f16 [T][d_model]: x as the tensor-core operand */
+  uint16_t* h;         /* f16 [T*k + T][d_ff] */
   float* out_acc;      /* fp32 [T][d_model] */
   int32_t* status;     /* device status word */
   int32_t max_tiles;

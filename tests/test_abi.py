@@ -93,10 +93,12 @@ def test_bad_arguments_are_rejected_on_the_host(L):
                        None) == -4
     # grouped GEMM: N not a multiple of 128, bad epilogue, misaligned A
     W = (ctypes.c_void_p * 3)(0x10000, 0x10000, 0x10000)
-    args = lambda A, N, epi: (A, 10, 128, None, 10, ctypes.cast(W, vp), 4, N, None, fake, fake,
-                              10, 16, epi, fake, fake, fake, 10, N, fake, 1 << 20, None)
+    args = lambda A, N, epi, fmt=1: (A, 10, 128, None, 10, ctypes.cast(W, vp), 4, N, None, fake,
+                                     fake, 10, 16, epi, fmt, fake, fake, fake, 10, N, fake,
+                                     1 << 20, None)
     assert L.moe_grouped_gemm_w4a16(*args(fake, 100, 0)) == -3
     assert L.moe_grouped_gemm_w4a16(*args(fake, 128, 7)) == -3
+    assert L.moe_grouped_gemm_w4a16(*args(fake, 128, 0, 5)) == -3  # unknown operand format
     assert L.moe_grouped_gemm_w4a16(*args(vp(0x10002), 128, 0)) == -2
     # forward: NULL weights, bad shape
     from bit_moe_expert_route_gb300 import ops

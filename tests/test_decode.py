@@ -3,7 +3,8 @@
 The GPU's fp32 router logits are checked against the oracle's (they differ
 only in summation order), then the oracle runs the layer on the GPU's logits
 so both sides take the same top-k decision; ids must match exactly and the
-bf16 output must satisfy max|err| <= 2e-2 rms(ref), rel-L2 <= 5e-3."""
+bf16 output must satisfy max|err| <= 2e-2 rms(ref) (plus half a bf16 spacing
+for the final bf16 store), rel-L2 <= 5e-3."""
 import numpy as np
 import pytest
 
@@ -35,7 +36,7 @@ def check_one(orc, host, dec, x):
     w = to_np(dec.view("topk_w", (1, FULL.top_k + 1), torch.float32))
     np.testing.assert_allclose(w[:, :FULL.top_k], ref["w"], rtol=2e-6)
     np.testing.assert_allclose(w[0, FULL.top_k], ref["gate"][0], rtol=2e-6)
-    ok, info = tolerance_check(bf16_np(out).reshape(1, -1), ref["out"])
+    ok, info = tolerance_check(bf16_np(out).reshape(1, -1), ref["out"], bf16_output=True)
     assert ok, info
 
 
@@ -82,5 +83,5 @@ def test_decode_without_shared_expert(orc):
     torch.cuda.synchronize()
     lg = to_np(dec.view("logits", (1, 32), torch.float32))
     ref = orc.moe_forward(x, host, shape, logits_in=lg)
-    ok, info = tolerance_check(bf16_np(out).reshape(1, -1), ref["out"])
+    ok, info = tolerance_check(bf16_np(out).reshape(1, -1), ref["out"], bf16_output=True)
     assert ok, info

@@ -1,14 +1,15 @@
 """moe_grouped_gemm_w4a16 against references built from the oracle's
-dequantisation and a library matmul.
+dequantisation and a library matmul, for both tensor-core operand formats
+(f16, used by moe_forward, and bf16).
 
 * integer-exact: x in {-2..2}, scale 1, bias -8 -> every product and partial
   sum is an integer below 2^24, so the fp32 result is exact: bit-exact.
 * one-hot readout: A rows are unit vectors, so C reads back the weight the
-  tensor core saw, which must be RNE_bf16(scale*q + bias) bit for bit; this
-  pins the on-chip dequantisation and the operand layouts.
+  tensor core saw, which must be RNE(scale*q + bias) in the operand format,
+  bit for bit; this pins the on-chip dequantisation and the operand layouts.
 * SwiGLU and combine epilogues on random data, against fp64 references on the
-  same bf16 operands (fp32 accumulation order and the bf16 rounding of h are
-  the only differences).
+  same operands (fp32 accumulation order and the rounding of h are the only
+  differences).
 * block maps with ragged tiles, every block_n, an extra group (shared expert),
   empty work, and out-of-range entries that the kernel must reject.
 """
@@ -17,15 +18,38 @@ import pytest
 
 from bit_moe_expert_route_gb300 import synth
 from bit_moe_expert_route_gb300.synth import LayerShape
-from gpu_util import bf16_np, to_np
+from gpu_util import to_np
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
+
+FMTS = {"f16": 1, "bf16": 0}
 
 
 def dev(a):
     from bit_moe_expert_route_gb300 import ops
     return ops.to_device(a)
+
+
+def to_fmt(a, fmt):
+    """float array -> operand bit patterns (uint16), RNE."""
+    a = np.asarray(a, np.float32)
+    return a.astype(np.float16).view(np.uint16) if fmt == "f16" else synth.f32_to_bf16(a)
+
+
+def from_fmt(bits, fmt):
+    bits = np.asarray(bits, np.uint16)
+    if fmt == "f16":
+        return bits.view(np.float16).astype(np.float64)
+    return synth.bf16_to_f32(bits).astype(np.float64)
+
+
+def round_fmt(a, fmt):
+    return from_fmt(to_fmt(a, fmt), fmt)
+
+
+def c_np(C, fmt):
+    return from_fmt(to_np(C.view(torch.int16)).view(np.uint16), fmt)
 
 
 def routing(orc, T, E, k, bn, seed, with_shared=True):
@@ -34,14 +58,13 @@ def routing(orc, T, E, k, bn, seed, with_shared=True):
     return ids, orc.route_meta(ids, E, bn, with_shared)
 
 
-def deq_bf16(orc, proj, g):
-    """Weights of expert g as the tensor core sees them: RNE_bf16(scale*q + bias)."""
+def deq(orc, proj, g, fmt):
+    """Weights of expert g as the tensor core sees them: RNE(scale*q + bias) in fmt."""
     q, s, b = proj
-    w = orc.dequant(q[g], s[g], b[g], 64)
-    return synth.bf16_to_f32(synth.f32_to_bf16(w.astype(np.float32))).astype(np.float64)
+    return round_fmt(orc.dequant(q[g], s[g], b[g], 64), fmt)
 
 
-def gemm_call(A, projs, n_groups, N, m, bn, epi, row_index=None, extra=None, **kw):
+def gemm_call(A, projs, n_groups, N, m, bn, epi, fmt, row_index=None, extra=None, **kw):
     from bit_moe_expert_route_gb300 import ops
     bm = torch.zeros(max(len(m["block_map"]), 1), 4, dtype=torch.int32, device="cuda")
     if len(m["block_map"]):
@@ -50,24 +73,24 @@ def gemm_call(A, projs, n_groups, N, m, bn, epi, row_index=None, extra=None, **k
     W = [tuple(dev(a) for a in p) for p in projs]
     Wx = None if extra is None else [tuple(dev(a) for a in p) for p in extra]
     C, ws = ops.grouped_gemm_w4a16(A, W, n_groups, N, bm, nt, bm.shape[0], bn, epi,
-                                   row_index=row_index, W_extra=Wx, **kw)
+                                   row_index=row_index, W_extra=Wx, operand=FMTS[fmt], **kw)
     torch.cuda.synchronize()
     return C, ws
 
 
+@pytest.mark.parametrize("fmt", ["f16", "bf16"])
 @pytest.mark.parametrize("bn", [16, 32, 64, 128])
-def test_integer_exact_none_epilogue(orc, bn):
+def test_integer_exact_none_epilogue(orc, bn, fmt):
     from bit_moe_expert_route_gb300 import ops
-    shape = LayerShape(d_model=512, n_experts=8, top_k=2, d_ff=256)
     E, K, N, T, k = 8, 512, 256, 150, 2
     q = synth.q4(synth.key(1, 0, 300), E * N * K // 8).reshape(E, N, K // 8)
     s = np.full((E, N, K // 64), 0x3F80, np.uint16)   # 1.0
     b = np.full((E, N, K // 64), 0xC100, np.uint16)   # -8.0
     xi = synth.uniform_int(synth.key(1, 0, 301), T * K, 5).reshape(T, K) - 2
-    x = synth.f32_to_bf16(xi.astype(np.float32))
+    x = to_fmt(xi.astype(np.float32), fmt)
     ids, m = routing(orc, T, E, k, bn, seed=bn, with_shared=False)
     rt = torch.from_numpy(m["row_token"]).cuda()
-    C, ws = gemm_call(dev(x), [(q, s, b)], E, N, m, bn, ops.EPI_NONE, row_index=rt)
+    C, ws = gemm_call(dev(x), [(q, s, b)], E, N, m, bn, ops.EPI_NONE, fmt, row_index=rt)
     assert ops.device_status(ws) == 0
     got = to_np(C)
     for e in range(E):
@@ -75,79 +98,78 @@ def test_integer_exact_none_epilogue(orc, bn):
         rows = np.arange(m["offsets"][e], m["offsets"][e + 1])
         ref = xi[m["row_token"][rows]].astype(np.int64) @ W.T
         assert np.array_equal(got[rows], ref.astype(np.float32)), f"expert {e}"
-    del shape
 
 
-def test_one_hot_reads_back_dequantised_weights(orc):
+@pytest.mark.parametrize("fmt", ["f16", "bf16"])
+def test_one_hot_reads_back_dequantised_weights(orc, fmt):
     """C[r, n] = W_g[n, r % K] exactly: every (row, k) of two experts' gate weights."""
     from bit_moe_expert_route_gb300 import ops
     full = LayerShape()
     K, N, G = full.d_model, full.d_ff, 2
     q, s, b = synth.w4_projection(LayerShape(n_experts=G), seed=3, layer=0, p=0)
     A = np.zeros((K, K), np.uint16)
-    A[np.arange(K), np.arange(K)] = 0x3F80
+    A[np.arange(K), np.arange(K)] = to_fmt(np.ones(1), fmt)[0]
     bn = 128
     bmap = [[g, g * K + r0, min(bn, K - r0), 0] for g in range(G) for r0 in range(0, K, bn)]
     m = dict(block_map=np.array(bmap, np.int32), num_tiles=len(bmap))
     row_index = torch.from_numpy(np.tile(np.arange(K, dtype=np.int32), G)).cuda()
-    C, ws = gemm_call(dev(A), [(q, s, b)], G, N, m, bn, ops.EPI_NONE, row_index=row_index)
+    C, ws = gemm_call(dev(A), [(q, s, b)], G, N, m, bn, ops.EPI_NONE, fmt, row_index=row_index)
     assert ops.device_status(ws) == 0
     got = to_np(C).reshape(G, K, N)
     for g in range(G):
-        assert np.array_equal(got[g].T, deq_bf16(orc, (q, s, b), g).astype(np.float32)), g
+        assert np.array_equal(got[g].T, deq(orc, (q, s, b), g, fmt).astype(np.float32)), g
 
 
-@pytest.mark.parametrize("bn", [16, 128])
-def test_swiglu_epilogue_with_shared_group(orc, bn):
+@pytest.mark.parametrize("fmt,bn", [("f16", 16), ("f16", 128), ("bf16", 64)])
+def test_swiglu_epilogue_with_shared_group(orc, bn, fmt):
     from bit_moe_expert_route_gb300 import ops
     shape = LayerShape(d_model=1024, n_experts=16, top_k=4, d_ff=256, d_ff_shared=256)
     T, E, k, K, N = 333, 16, 4, 1024, 256
     w = synth.layer_weights(shape, seed=9)
-    x = synth.tokens(shape, T, seed=9)
+    X = round_fmt(synth.bf16_to_f32(synth.tokens(shape, T, seed=9)), fmt)
     ids, m = routing(orc, T, E, k, bn, seed=9 + bn)
     rt = torch.from_numpy(m["row_token"]).cuda()
-    C, ws = gemm_call(dev(x), [w["gate"], w["up"]], E, N, m, bn, ops.EPI_SWIGLU, row_index=rt,
-                      extra=[w["sh_gate"], w["sh_up"]])
+    C, ws = gemm_call(dev(to_fmt(X, fmt)), [w["gate"], w["up"]], E, N, m, bn, ops.EPI_SWIGLU,
+                      fmt, row_index=rt, extra=[w["sh_gate"], w["sh_up"]])
     assert ops.device_status(ws) == 0
-    got = bf16_np(C).astype(np.float64)
-    X = synth.bf16_to_f32(x).astype(np.float64)
+    got = c_np(C, fmt)
     ref = np.zeros_like(got)
     for g in range(E + 1):
         if g < E:
             rows = np.arange(m["offsets"][g], m["offsets"][g + 1])
-            Wg, Wu = deq_bf16(orc, w["gate"], g), deq_bf16(orc, w["up"], g)
+            Wg, Wu = deq(orc, w["gate"], g, fmt), deq(orc, w["up"], g, fmt)
         else:
             rows = np.arange(T * k, T * k + T)
-            Wg, Wu = deq_bf16(orc, w["sh_gate"], 0), deq_bf16(orc, w["sh_up"], 0)
+            Wg, Wu = deq(orc, w["sh_gate"], 0, fmt), deq(orc, w["sh_up"], 0, fmt)
         xr = X[m["row_token"][rows]]
         gg, uu = xr @ Wg.T, xr @ Wu.T
         ref[rows] = gg / (1 + np.exp(-gg)) * uu
     err = got - ref
-    assert np.linalg.norm(err) / np.linalg.norm(ref) < 4e-3
-    assert np.max(np.abs(err) / (np.abs(ref) + 1e-2 * np.sqrt(np.mean(ref ** 2)))) < 2e-2
+    tol = 1e-3 if fmt == "f16" else 4e-3  # rounding of h to the operand format dominates
+    assert np.linalg.norm(err) / np.linalg.norm(ref) < tol
+    assert np.max(np.abs(err) / (np.abs(ref) + 1e-2 * np.sqrt(np.mean(ref ** 2)))) < 5 * tol
 
 
-@pytest.mark.parametrize("bn", [32, 64])
-def test_combine_epilogue(orc, bn):
+@pytest.mark.parametrize("fmt,bn", [("f16", 32), ("bf16", 64)])
+def test_combine_epilogue(orc, bn, fmt):
     from bit_moe_expert_route_gb300 import ops
     shape = LayerShape(d_model=512, n_experts=8, top_k=3, d_ff=256, d_ff_shared=256)
     T, E, k, d, f = 200, 8, 3, 512, 256
     w = synth.layer_weights(shape, seed=13)
     ids, m = routing(orc, T, E, k, bn, seed=13 + bn)
     rows = T * k + T
-    h = synth.normal_bf16(synth.key(13, 0, 400), rows * f, 1.0).reshape(rows, f)
+    H = round_fmt(synth.normal_f32(synth.key(13, 0, 400), rows * f, 1.0).reshape(rows, f), fmt)
     scale = synth.normal_f32(synth.key(13, 0, 401), rows, 0.5)
     out = torch.zeros(T, d, dtype=torch.float32, device="cuda")
-    C, ws = gemm_call(dev(h), [w["down"]], E, d, m, bn, ops.EPI_COMBINE, extra=[w["sh_down"]],
-                      row_scale=torch.from_numpy(scale).cuda(),
+    C, ws = gemm_call(dev(to_fmt(H, fmt)), [w["down"]], E, d, m, bn, ops.EPI_COMBINE, fmt,
+                      extra=[w["sh_down"]], row_scale=torch.from_numpy(scale).cuda(),
                       out_row=torch.from_numpy(m["row_token"]).cuda(), C=out)
     assert ops.device_status(ws) == 0
-    H = synth.bf16_to_f32(h).astype(np.float64)
     ref = np.zeros((T, d))
     for g in range(E + 1):
         r = (np.arange(m["offsets"][g], m["offsets"][g + 1]) if g < E
              else np.arange(T * k, rows))
-        Wd = deq_bf16(orc, w["down"], g) if g < E else deq_bf16(orc, w["sh_down"], 0)
+        Wd = deq(orc, w["down"], g, fmt) if g < E else deq(orc, w["sh_down"], 0, fmt)
         np.add.at(ref, m["row_token"][r], scale[r, None] * (H[r] @ Wd.T))
     got = to_np(out).astype(np.float64)
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < 1e-5
@@ -161,7 +183,7 @@ def test_empty_work_leaves_output_untouched(orc):
     m = dict(block_map=np.zeros((0, 4), np.int32), num_tiles=0)
     A = dev(synth.tokens(LayerShape(d_model=K), 4, seed=4))
     C = torch.full((4, N), 7.0, device="cuda")
-    C, ws = gemm_call(A, [(q, s, b)], 2, N, m, 16, ops.EPI_NONE, C=C)
+    C, ws = gemm_call(A, [(q, s, b)], 2, N, m, 16, ops.EPI_NONE, "bf16", C=C)
     assert ops.device_status(ws) == 0 and bool((C == 7.0).all())
 
 
@@ -172,13 +194,14 @@ def test_bad_block_map_and_rows_are_rejected_on_device(orc):
     q, s, b = synth.w4_projection(LayerShape(d_model=K, d_ff=N, n_experts=2), 4, 0, 0)
     A = dev(synth.tokens(LayerShape(d_model=K), 8, seed=4))
     bad_group = dict(block_map=np.array([[5, 0, 4, 0]], np.int32), num_tiles=1)
-    C, ws = gemm_call(A, [(q, s, b)], 2, N, bad_group, 16, ops.EPI_NONE, n_rows=8)
+    C, ws = gemm_call(A, [(q, s, b)], 2, N, bad_group, 16, ops.EPI_NONE, "bf16", n_rows=8)
     assert ops.device_status(ws) == ops.DEV_BAD_TILE
     bad_rows = dict(block_map=np.array([[0, 6, 4, 0]], np.int32), num_tiles=1)  # 6+4 > 8
-    C, ws = gemm_call(A, [(q, s, b)], 2, N, bad_rows, 16, ops.EPI_NONE, n_rows=8)
+    C, ws = gemm_call(A, [(q, s, b)], 2, N, bad_rows, 16, ops.EPI_NONE, "bf16", n_rows=8)
     assert ops.device_status(ws) == ops.DEV_BAD_TILE
     ri = torch.tensor([0, 1, 99, 3], dtype=torch.int32, device="cuda")  # row 99 of 8
     ok_map = dict(block_map=np.array([[1, 0, 4, 0]], np.int32), num_tiles=1)
-    C, ws = gemm_call(A, [(q, s, b)], 2, N, ok_map, 16, ops.EPI_NONE, row_index=ri)
+    C = torch.full((4, N), 7.0, device="cuda")
+    C, ws = gemm_call(A, [(q, s, b)], 2, N, ok_map, 16, ops.EPI_NONE, "bf16", row_index=ri, C=C)
     assert ops.device_status(ws) == ops.DEV_BAD_ROW
-    assert bool((C[2] == 0).all())  # the refused row reads as zeros
+    assert bool((C[2] == 0).all()) and bool((C[0] != 7.0).any())  # refused row reads as zeros
