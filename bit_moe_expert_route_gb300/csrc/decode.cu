@@ -10,12 +10,18 @@
 // (weights, and x), then waits (griddepcontrol.wait), so its weight traffic
 // overlaps the previous kernel's tail:
 //   1. decode_router_shared_kernel  router logits (8 complete logits per
-//        block) and the shared expert's gate/up rows (h of the shared slot);
-//        the last block to finish selects the top k and writes the weights.
-//   2. decode_gateup_kernel   the routed experts' gate/up rows, h = silu(g)*u.
-//   3. decode_down_kernel     one warp per output column: down rows of every
-//        slot, weighted and summed in slot order, rounded once to bf16. Its
-//        down-row loads are issued before it waits for h.
+//        block), the shared gate logit, and the shared expert's gate/up rows
+//        (h of the shared slot).
+//   2. decode_gateup_kernel   every block selects the top k from the logits
+//        (warp argmax, ties to the lower id; block 0 also stores ids, weights
+//        and the gate), then the routed experts' gate/up rows, h = silu(g)*u.
+//   3. decode_down_kernel     selects the top k the same way before its wait
+//        (kernel 1 has completed by then) and issues its down-row loads, then
+//        waits for h; one warp per output column sums every slot's down row,
+//        weighted, in slot order, rounded once to bf16.
+// The selection is recomputed per block instead of being published by a
+// last-block-done step: it costs one L2 read of E logits per block and
+// removes a fence, an atomic and a dependent round trip from the path.
 //
 // Dot products per 16-byte chunk (32 codes, half a group): a code q becomes the
 // float f = 1 + q/16 exactly (bit pattern 0x3F800000 | q << 19), so
@@ -167,15 +173,73 @@ MOE_DEVINL float rowpair_h(const RowPairLoads<XC>& L, const XChunks<XC>& xc, int
   return ag / (1.f + expf(-ag)) * au;
 }
 
+// Top-k of the E logits (+ router bias) by warp 0 of the block, read from
+// global memory (L2): ids, softmax-over-selected weights and the shared gate
+// go to shared memory. Descending, ties to the lower id.
+template <int NPL>
+MOE_DEVINL void block_topk(const DecodeParams& p, int* s_ids, float* s_w) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float z[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = i * 32 + lane;
+      z[i] = 0.f;
+      if (e < p.E) {
+        z[i] = __ldcg(p.logits + e);
+        if (p.w.router_bias) z[i] = z[i] + p.w.router_bias[e];
+      }
+    }
+    uint32_t taken = 0;
+    float my_z = 0.f;
+    int my_e = 0;
+    for (int j = 0; j < p.k; ++j) {
+      float bv = 0.f;
+      int be = INT_MAX;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int e = i * 32 + lane;
+        if (e < p.E && !((taken >> i) & 1u) && (be == INT_MAX || z[i] > bv)) {
+          bv = z[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(kFull, bv, off);
+        const int oe = __shfl_xor_sync(kFull, be, off);
+        if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (lane == j) {
+        my_z = bv;
+        my_e = be;
+      }
+    }
+    const float zmax = __shfl_sync(kFull, my_z, 0);
+    const float ex = lane < p.k ? expf(my_z - zmax) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+    if (lane < p.k) {
+      s_ids[lane] = my_e;
+      s_w[lane] = ex / sum;
+    }
+    if (lane == 0) s_w[p.k] = p.shared ? 1.f / (1.f + expf(-__ldcg(p.gate_logit))) : 0.f;
+  }
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------- kernel 1
 // blocks [0, E/8): router logits 8b..8b+7 (thread t takes rows t + 256 j);
 // blocks [E/8, E/8 + f/8): shared expert gate/up, one row pair per warp.
-template <int NPL, int XC>
+template <int XC>
 __global__ void __launch_bounds__(256) decode_router_shared_kernel(DecodeParams p) {
   constexpr int kPre = 8;  // router rows per thread loaded before the wait
   __shared__ float s_red[8][8];
-  __shared__ float s_logit[1025];
-  __shared__ int s_last;
   const int E = p.E, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_router = E / 8;
   const bool is_router = (int)blockIdx.x < n_router;
@@ -251,87 +315,35 @@ __global__ void __launch_bounds__(256) decode_router_shared_kernel(DecodeParams 
       if (lane == 0) p.gate_logit[0] = a;
     }
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(p.counter, 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_logit[e] = __ldcg(p.logits + e);
-  if (threadIdx.x == 0) s_logit[E] = p.shared ? __ldcg(p.gate_logit) : 0.f;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    float z[NPL];
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      const int e = i * 32 + lane;
-      z[i] = e < E ? (p.w.router_bias ? s_logit[e] + p.w.router_bias[e] : s_logit[e]) : 0.f;
-    }
-    uint32_t taken = 0;
-    float my_z = 0.f;
-    int my_e = 0;
-    for (int j = 0; j < p.k; ++j) {
-      float bv = 0.f;
-      int be = INT_MAX;
-#pragma unroll
-      for (int i = 0; i < NPL; ++i) {
-        const int e = i * 32 + lane;
-        if (e < E && !((taken >> i) & 1u) && (be == INT_MAX || z[i] > bv)) {
-          bv = z[i];
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(kFull, bv, off);
-        const int oe = __shfl_xor_sync(kFull, be, off);
-        if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (lane == j) {
-        my_z = bv;
-        my_e = be;
-      }
-    }
-    const float zmax = __shfl_sync(kFull, my_z, 0);
-    const float ex = lane < p.k ? expf(my_z - zmax) : 0.f;
-    float sum = ex;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
-    if (lane < p.k) {
-      p.ids[lane] = my_e;
-      p.wts[lane] = ex / sum;
-    }
-    if (lane == 0) {
-      p.wts[p.k] = p.shared ? 1.f / (1.f + expf(-s_logit[E])) : 0.f;
-      *p.counter = 0u;  // ready for the next call
-    }
-  }
 }
 
 // ---------------------------------------------------------------- kernel 2
 // Routed gate/up rows: row pair rp = slot * f + row, two per warp at a time.
-template <int XC>
+template <int NPL, int XC>
 __global__ void __launch_bounds__(256, XC <= 2 ? 2 : 1) decode_gateup_kernel(DecodeParams p) {
+  __shared__ int s_ids[32];
+  __shared__ float s_w[33];
   XChunks<XC> xc;
   load_x_chunks<XC>(p.x, p.d / 32, xc);  // x does not depend on the router
   pdl_wait();
   pdl_launch_dependents();
+  block_topk<NPL>(p, s_ids, s_w);
+  if (blockIdx.x == 0 && threadIdx.x <= p.k) {
+    if (threadIdx.x < p.k) p.ids[threadIdx.x] = s_ids[threadIdx.x];
+    p.wts[threadIdx.x] = s_w[threadIdx.x];
+  }
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * 8;
   const int total = p.k * p.f;
   for (int rp0 = blockIdx.x * 8 + (threadIdx.x >> 5); rp0 < total; rp0 += 2 * nwarps) {
     const int rp1 = rp0 + nwarps;
     RowPairLoads<XC> L0, L1;
-    int e0 = p.ids[rp0 / p.f], e1 = 0;
+    int e0 = s_ids[rp0 / p.f], e1 = 0;
     const bool ok0 = e0 >= 0 && e0 < p.E;
     if (ok0) load_rowpair<XC>(p.w.gate, p.w.up, (int64_t)e0 * p.f + rp0 % p.f, p.d, L0);
     bool ok1 = false;
     if (rp1 < total) {
-      e1 = p.ids[rp1 / p.f];
+      e1 = s_ids[rp1 / p.f];
       ok1 = e1 >= 0 && e1 < p.E;
       if (ok1) load_rowpair<XC>(p.w.gate, p.w.up, (int64_t)e1 * p.f + rp1 % p.f, p.d, L1);
     }
@@ -350,17 +362,21 @@ __global__ void __launch_bounds__(256, XC <= 2 ? 2 : 1) decode_gateup_kernel(Dec
 // ---------------------------------------------------------------- kernel 3
 // One warp per output column j: chunk idx = slot * (f/32) + c of the down rows
 // (slot < k: routed expert ids[slot], slot k: shared), weighted by wts[slot].
-template <int NI>
+template <int NPL, int NI>
 __global__ void __launch_bounds__(256) decode_down_kernel(DecodeParams p) {
   extern __shared__ float4 smem4[];
+  __shared__ int s_ids[32];
+  __shared__ float s_w[33];
   const int nslots = p.k + (p.shared ? 1 : 0);
   const int fch = p.f / 32;
   const int total = nslots * fch;
   const int lane = threadIdx.x & 31;
   const int j = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int64_t qrow = p.f / 8, grow = p.f / 64;
-  // 1. this warp's down-row chunks (the expert ids come from kernel 1, which
-  //    has completed: kernel 2 waited for it before letting this grid start)
+  // 1. the selection (from kernel 1's logits: kernel 1 has completed, since
+  //    every block of kernel 2 waited for it before letting this grid start)
+  //    and this warp's down-row chunks
+  block_topk<NPL>(p, s_ids, s_w);
   uint4 w[NI];
   uint16_t sc[NI], bi[NI];
   float coef[NI];
@@ -373,7 +389,7 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeParams p) {
       int64_t e = 0;
       const moe_w4_t* D = &p.w.sh_down;
       if (slot < p.k) {
-        e = p.ids[slot];
+        e = s_ids[slot];
         D = &p.w.down;
       }
       if (e >= 0 && e < p.E) {
@@ -412,7 +428,7 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeParams p) {
     if (idx < total && coef[i] != 0.f) {
       const float2 a = affine_f(sc[i], bi[i]);
       const float part = fmaf(a.x, chunk_fdot_smem(w[i], hv, idx), a.y * hsum[idx]);
-      acc = fmaf(__ldcg(p.wts + idx / fch), part, acc);
+      acc = fmaf(s_w[idx / fch], part, acc);
     }
   }
   // chunks beyond NI * 32 (large k * d_ff): loaded after the wait
@@ -421,7 +437,7 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeParams p) {
     int64_t e = 0;
     const moe_w4_t* D = &p.w.sh_down;
     if (slot < p.k) {
-      e = p.ids[slot];
+      e = s_ids[slot];
       D = &p.w.down;
     }
     if (e < 0 || e >= p.E) continue;
@@ -429,7 +445,7 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeParams p) {
     const uint4 wq = __ldcs(reinterpret_cast<const uint4*>(D->q + r * qrow) + c);
     const float2 a = affine_f(__ldcs(D->scale + r * grow + (c >> 1)), __ldcs(D->bias + r * grow + (c >> 1)));
     const float part = fmaf(a.x, chunk_fdot_smem(wq, hv, idx), a.y * hsum[idx]);
-    acc = fmaf(__ldcg(p.wts + slot), part, acc);
+    acc = fmaf(s_w[slot], part, acc);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
@@ -455,36 +471,25 @@ cudaError_t launch_pdl(K kernel, dim3 grid, size_t smem, cudaStream_t s, Args...
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-template <int XC>
-cudaError_t launch_k1(const DecodeParams& p, int nblk, cudaStream_t s) {
-  const int npl = (p.E + 31) / 32;
-  if (npl <= 1) return launch_pdl(decode_router_shared_kernel<1, XC>, dim3(nblk), 0, s, p);
-  if (npl <= 2) return launch_pdl(decode_router_shared_kernel<2, XC>, dim3(nblk), 0, s, p);
-  if (npl <= 4) return launch_pdl(decode_router_shared_kernel<4, XC>, dim3(nblk), 0, s, p);
-  if (npl <= 8) return launch_pdl(decode_router_shared_kernel<8, XC>, dim3(nblk), 0, s, p);
-  if (npl <= 16) return launch_pdl(decode_router_shared_kernel<16, XC>, dim3(nblk), 0, s, p);
-  return launch_pdl(decode_router_shared_kernel<32, XC>, dim3(nblk), 0, s, p);
-}
-
-template <int XC>
+template <int NPL, int XC>
 cudaError_t launch_xc(const DecodeParams& p, cudaStream_t s) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int n1 = p.E / 8 + (p.shared ? (p.f + 7) / 8 : 0);
-  cudaError_t err = launch_k1<XC>(p, n1, s);
+  cudaError_t err = launch_pdl(decode_router_shared_kernel<XC>, dim3(n1), 0, s, p);
   if (err != cudaSuccess) return err;
   const int rowpairs = p.k * p.f;
   const int n2 = std::max(1, std::min((rowpairs + 15) / 16, 2 * sms));
-  err = launch_pdl(decode_gateup_kernel<XC>, dim3(n2), 0, s, p);
+  err = launch_pdl(decode_gateup_kernel<NPL, XC>, dim3(n2), 0, s, p);
   if (err != cudaSuccess) return err;
   const int nslots = p.k + (p.shared ? 1 : 0);
   const int total = nslots * (p.f / 32);
   const size_t smem = (size_t)total * 8 * 16 + (size_t)total * 4;
   const dim3 g3((p.d + 7) / 8);
-  auto k3 = total <= 32 * 2 ? decode_down_kernel<2>
-            : total <= 32 * 4 ? decode_down_kernel<4>
-            : total <= 32 * 6 ? decode_down_kernel<6> : decode_down_kernel<8>;
+  auto k3 = total <= 32 * 2 ? decode_down_kernel<NPL, 2>
+            : total <= 32 * 4 ? decode_down_kernel<NPL, 4>
+            : total <= 32 * 6 ? decode_down_kernel<NPL, 6> : decode_down_kernel<NPL, 8>;
   if (smem > 48 * 1024) {
     err = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
@@ -492,16 +497,24 @@ cudaError_t launch_xc(const DecodeParams& p, cudaStream_t s) {
   return launch_pdl(k3, g3, smem, s, p);
 }
 
+template <int NPL>
+cudaError_t launch_npl(const DecodeParams& p, cudaStream_t s) {
+  switch (p.d / 1024) {
+    case 0:
+    case 1: return launch_xc<NPL, 1>(p, s);
+    case 2: return launch_xc<NPL, 2>(p, s);
+    case 3: return launch_xc<NPL, 3>(p, s);
+    default: return launch_xc<NPL, 4>(p, s);
+  }
+}
+
 }  // namespace
 
 cudaError_t decode_launch(const DecodeParams& p, cudaStream_t s) {
-  switch (p.d / 1024) {
-    case 0:
-    case 1: return launch_xc<1>(p, s);
-    case 2: return launch_xc<2>(p, s);
-    case 3: return launch_xc<3>(p, s);
-    default: return launch_xc<4>(p, s);
-  }
+  const int npl = (p.E + 31) / 32;
+  if (npl <= 2) return launch_npl<2>(p, s);
+  if (npl <= 8) return launch_npl<8>(p, s);
+  return launch_npl<32>(p, s);
 }
 
 }  // namespace moe

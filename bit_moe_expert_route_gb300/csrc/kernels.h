@@ -96,7 +96,6 @@ struct DecodeParams {
   int32_t* ids;             // [k]
   float* wts;               // [k]
   float* h;                 // [k+1][f]
-  uint32_t* counter;        // [1] last-block-done counter (self-resetting)
   int32_t* status;
 };
 cudaError_t decode_launch(const DecodeParams& p, cudaStream_t s);

@@ -113,7 +113,6 @@ FwdWs forward_ws(void* ws, const moe_shape_t* s, int bn) {
 
 struct DecWs {
   moe_decode_views_t v;
-  uint32_t* counter;
   size_t bytes;
 };
 
@@ -123,7 +122,6 @@ DecWs decode_ws(void* ws, const moe_shape_t* s) {
   DecWs r;
   memset(&r.v, 0, sizeof r.v);
   r.v.status = c.take<int32_t>(kStatusWords);
-  r.counter = reinterpret_cast<uint32_t*>(r.v.status + 16);
   r.v.logits = c.take<float>(E);
   r.v.gate_logit = c.take<float>(1);
   r.v.topk_ids = c.take<int32_t>(k);
@@ -456,7 +454,8 @@ int moe_decode_gemv_w4(const uint16_t* x, const moe_weights_t* w, const moe_shap
   if (!ws || !aligned(ws, kAlign) || ws_bytes < dw.bytes) return MOE_ERR_WORKSPACE;
   if ((rc = check_device()) != MOE_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((rc = cuda_status(cudaMemsetAsync(dw.v.status, 0, kStatusWords * 4, s))) != MOE_OK) return rc;
+  // the first decode kernel clears the status word itself (after its
+  // dependency wait), so consecutive calls stay one chain of PDL launches
   moe::DecodeParams p;
   memset(&p, 0, sizeof p);
   p.x = x;
@@ -472,7 +471,6 @@ int moe_decode_gemv_w4(const uint16_t* x, const moe_weights_t* w, const moe_shap
   p.ids = dw.v.topk_ids;
   p.wts = dw.v.topk_w;
   p.h = dw.v.h;
-  p.counter = dw.counter;
   p.status = dw.v.status;
   return cuda_status(moe::decode_launch(p, s));
 }
