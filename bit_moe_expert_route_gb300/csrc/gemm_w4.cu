@@ -16,13 +16,14 @@
 //                  4 KB per projection) into a ring of shared-memory stages.
 //   * warp 1       allocates TMEM and issues tcgen05.mma (one thread).
 //   * warps 4-7    dequantise: thread m owns weight row m; it turns 64 codes
-//                  into bf16 RNE(scale*q + bias) and writes them into the
-//                  128-byte-swizzled K-major A operand.
+//                  into RNE(scale*q + bias) (f16 or bf16) and writes them into
+//                  the 128-byte-swizzled K-major A operand, then frees the
+//                  packed-code stage (only after its codes are consumed).
 //   * warps 8-11   gather: token rows (through row_index) are copied with
 //                  16-byte cp.async into the swizzled K-major B operand;
 //                  rows past the tile's end are zero-filled.
 //   * warps 12-15  epilogue: tcgen05.ld of the accumulators, then
-//                  NONE (fp32 store), SWIGLU (bf16 silu(g)*u) or COMBINE
+//                  NONE (fp32 store), SWIGLU (silu(g)*u in the operand type) or COMBINE
 //                  (row_scale * y added into the output row).
 //   Accumulators are double buffered so the epilogue of one tile overlaps the
 //   MMAs of the next. Every wait is bounded; a CTA that gives up records
@@ -333,7 +334,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
           qw[j][0] = src[0];
           qw[j][1] = src[1];
         }
-        mbar_arrive(&q_empty[sq]);
         const int sa = it % C::kSA;
         if (!mbar_wait(&a_empty[sa], ((it / C::kSA) & 1) ^ 1, abort_flag, g.status, 7)) {
           alive = false;
@@ -358,6 +358,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
         }
         fence_proxy_async_smem();
         mbar_arrive(&a_full[sa]);
+        // Release the packed-code stage only now that its codes have been
+        // consumed: releasing it right after the shared-memory loads let the
+        // next TMA refill land before those loads had returned their data.
+        mbar_arrive(&q_empty[sq]);
       }
     }
   } else if (warp >= 8 && warp < 12) {

@@ -144,3 +144,21 @@ def test_forward_graph_replay_matches_eager(host_layer, dev_layers):
     torch.cuda.synchronize()
     diff = (out.float() - eager.float()).abs().max().item()
     assert diff <= 1e-2 * eager.float().abs().max().item()  # combine adds are unordered
+
+
+@pytest.mark.parametrize("T,bn", [(4096, 128), (4096, 64)])
+def test_forward_repeatable(dev_layers, T, bn):
+    """The gate/up GEMM has no atomics, so h must be bit-identical run to run;
+    a pipeline race between stages shows up here first."""
+    from bit_moe_expert_route_gb300 import ops
+    fwd = ops.Forward(dev_layers[False], T, bn)
+    x = torch.from_numpy(synth.tokens(FULL, T, seed=3).view(np.int16)).cuda()
+    rows = T * (FULL.top_k + 1)
+    hs = []
+    for _ in range(6):
+        fwd(x)
+        torch.cuda.synchronize()
+        hs.append(fwd.view("h", (rows, FULL.d_ff), torch.int16).clone())
+    assert ops.device_status(fwd.ws) == 0
+    for h in hs[1:]:
+        assert torch.equal(h, hs[0])
