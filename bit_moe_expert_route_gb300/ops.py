@@ -92,6 +92,7 @@ def lib():
         L.moe_decode_workspace_bytes.argtypes = [vp]
         L.moe_decode_views.argtypes = [vp, sz, vp, vp]
         L.moe_decode_gemv_w4.argtypes = [vp, vp, vp, vp, vp, sz, vp]
+        L.moe_decode_gemv_w4_noalloc.argtypes = [vp, vp, vp, vp, vp]
         L.moe_get_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
         _lib = L
     return _lib

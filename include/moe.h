@@ -256,6 +256,30 @@ int moe_decode_views(void* ws, size_t ws_bytes, const moe_shape_t* shape,
                      moe_decode_views_t* views);
 
 /*
+ * moe_decode_gemv_w4_noalloc: moe_decode_gemv_w4 without a caller workspace.
+ * The pages have no counterpart to this call; it exists for callers that may
+ * not allocate device memory, such as plug-ins running inside a framework
+ * whose memory pool owns the GPU, or serving loops that cannot afford an
+ * allocation's synchronisation. Its scratch is a 256 KB array compiled into
+ * the library (each GPU that loads the library holds one until the process
+ * exits); the call itself allocates nothing.
+ *   x, w, shape, out, stream: as for moe_decode_gemv_w4 (shape->T == 1).
+ *   Returns MOE_ERR_WORKSPACE when moe_decode_workspace_bytes(shape) exceeds
+ *   256 KB (the top-8-of-256 layer with d_ff 512 needs about 20 KB), and
+ *   MOE_ERR_CUDA if the scratch's device address cannot be obtained.
+ * The first call on each device looks the scratch up (cudaGetSymbolAddress,
+ * which may load the library's device code onto that device); make that
+ * first call before any stream capture. All calls share the one array, which
+ * keeps the previous call's contents; nothing in it needs to start at zero
+ * (the first kernel clears the status words, every other value is written
+ * before it is read). Calls that overlap on the GPU, e.g. on two streams,
+ * race on the array; device-side fault records stay in the array and are not
+ * readable through moe_get_device_status.
+ */
+int moe_decode_gemv_w4_noalloc(const uint16_t* x, const moe_weights_t* w,
+                               const moe_shape_t* shape, uint16_t* out, void* stream);
+
+/*
  * Reads the device status word of a workspace (synchronises `stream`).
  * *device_status receives a moe_device_status value.
  */
