@@ -91,6 +91,17 @@ MOE_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, i
   }
 }
 
+// One arrival on behalf of the calling warp's active lanes: they sync first
+// (which orders each lane's earlier shared-memory writes and proxy fences
+// before the arrive), then the lowest of them arrives. Arrivals on one
+// barrier word serialise in shared memory, so a barrier that hundreds of
+// threads would each arrive on is counted in warps instead.
+MOE_DEVINL void mbar_arrive_warp(uint64_t* bar) {
+  const unsigned mask = __activemask();
+  __syncwarp(mask);
+  if ((threadIdx.x & 31) == __ffs(mask) - 1) mbar_arrive(bar);
+}
+
 MOE_DEVINL void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -133,6 +144,34 @@ MOE_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "m
 template <int N>
 MOE_DEVINL void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------------------------- bulk copies (TMA, untiled)
+// Shared -> global copy of `bytes` (16-byte aligned addresses, multiple of 16).
+MOE_DEVINL void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_u32(ssrc)), "r"(bytes)
+               : "memory");
+}
+// Shared -> global element-wise fp32 add (the reduction happens at L2).
+MOE_DEVINL void bulk_reduce_add_f32(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                   gdst),
+               "r"(smem_u32(ssrc)), "r"(bytes)
+               : "memory");
+}
+MOE_DEVINL void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+MOE_DEVINL void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until all of this thread's bulk groups have completed.
+MOE_DEVINL void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Barrier `id` (1..15) over `count` threads (whole warps).
+MOE_DEVINL void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05 / TMEM

@@ -15,16 +15,20 @@
 //   * warp 0       TMA producer: packed-code tiles (128 rows x 64 codes =
 //                  4 KB per projection) into a ring of shared-memory stages.
 //   * warp 1       allocates TMEM and issues tcgen05.mma (one thread).
-//   * warps 4-7    dequantise: thread m owns weight row m; it turns 64 codes
-//                  into RNE(scale*q + bias) (f16 or bf16) and writes them into
-//                  the 128-byte-swizzled K-major A operand, then frees the
-//                  packed-code stage (only after its codes are consumed).
-//   * warps 8-11   gather: token rows (through row_index) are copied with
+//   * warps 4-11   dequantise: two threads per weight row, 32 codes each;
+//                  RNE(scale*q + bias) (f16 or bf16) goes into the
+//                  128-byte-swizzled K-major A operand, then the packed-code
+//                  stage is freed (only after its codes are consumed).
+//   * warps 2-3    gather: token rows (through row_index) are copied with
 //                  16-byte cp.async into the swizzled K-major B operand;
-//                  rows past the tile's end are zero-filled.
+//                  rows past the tile's end are zero-filled. Without a
+//                  row_index the rows are contiguous and warp 0 loads each
+//                  B tile with one 128-byte-swizzled TMA copy instead.
 //   * warps 12-15  epilogue: tcgen05.ld of the accumulators, then
-//                  NONE (fp32 store), SWIGLU (silu(g)*u in the operand type) or COMBINE
-//                  (row_scale * y added into the output row).
+//                  NONE (fp32 store), SWIGLU (silu(g)*u in the operand type) or
+//                  COMBINE (row_scale * y added into the output row), the last
+//                  two staged in shared memory and written one token row per
+//                  TMA bulk copy (COMBINE: bulk fp32 add, done at L2).
 //   Accumulators are double buffered so the epilogue of one tile overlaps the
 //   MMAs of the next. Every wait is bounded; a CTA that gives up records
 //   MOE_DEV_TIMEOUT, drains what it issued, frees TMEM and returns.
@@ -42,33 +46,52 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kTileM = 128;      // weight rows per tile (MMA M)
 constexpr int kKB = 64;          // codes per k-block (= quantisation group)
-constexpr int kQBytes = kTileM * kKB / 2;   // packed tile: 4 KB
+constexpr int kQBytes = kTileM * kKB / 2;   // packed codes of one k-block: 4 KB
 constexpr int kABytes = kTileM * kKB * 2;   // dequantised tile: 16 KB
-constexpr int kSQ = 4;           // packed-code stages
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kSmemBudget = 220 * 1024;
 
-template <int BN, int NMAT>
+// QK = k-blocks of packed codes per TMA box (and per ring stage). 4: one box
+// of 128 rows x 128 bytes (128-byte swizzle) per matrix; 1: 128 rows x 32
+// bytes. The wide box moves the same bytes with a quarter of the row
+// requests, which is what bounds a stream of narrow strided boxes.
+template <int BN, int NMAT, int EPI, int QK>
 struct Cfg {
+  static constexpr int kSQ = QK == 1 ? 4 : 2;      // packed-code stages
+  static constexpr int kQStage = kQBytes * QK;     // bytes per matrix per stage
+  static constexpr int kCH = BN < 32 ? BN : 32;  // epilogue chunk: token columns per pass
+  // Epilogue staging: two buffers of kCH token rows x 128 outputs
+  // (fp32 for COMBINE, 16-bit for SWIGLU), plus per-row scale and output row.
+  static constexpr int kStageElem = EPI == MOE_EPI_COMBINE ? 4 : EPI == MOE_EPI_SWIGLU ? 2 : 0;
+  static constexpr int kEpiBytes = 2 * kCH * kTileM * kStageElem;
+  static constexpr int kRowInfoBytes = EPI == MOE_EPI_COMBINE ? 2 * BN * 4 : 0;
+  // Rings: packed codes (TMA), dequantised A tiles (dequant warps), token
+  // tiles B (gather warps or TMA). B tiles are small, so B runs deepest: it
+  // has the longest latency to cover (row gathers from L2/HBM).
+  static constexpr int kAStage = NMAT * kABytes;
   static constexpr int kBBytes = BN * kKB * 2;
-  static constexpr int kStage = NMAT * kABytes + kBBytes;
-  static constexpr int kQRing = kSQ * NMAT * kQBytes;
-  static constexpr int kSA0 = (kSmemBudget - kQRing) / kStage;
-  static constexpr int kSA = kSA0 > 6 ? 6 : kSA0;
+  static constexpr int kQRing = kSQ * NMAT * kQStage;
+  static constexpr int kSA = NMAT == 2 ? 2 : 3;
+  static constexpr int kSB0 =
+      (kSmemBudget - kQRing - kEpiBytes - kRowInfoBytes - kSA * kAStage) / kBBytes;
+  static constexpr int kSB = kSB0 > 8 ? 8 : kSB0;
   static constexpr int kOffA = 0;
-  static constexpr int kOffB = kOffA + kSA * NMAT * kABytes;
-  static constexpr int kOffQ = kOffB + kSA * kBBytes;
-  static constexpr int kOffBar = kOffQ + kQRing;
-  static constexpr int kBarBytes = 8 * (2 * kSQ + 2 * kSA + 5) + 16;
+  static constexpr int kOffB = kOffA + kSA * kAStage;
+  static constexpr int kOffQ = kOffB + kSB * kBBytes;
+  static constexpr int kOffEpi = kOffQ + kQRing;
+  static constexpr int kOffRowInfo = kOffEpi + kEpiBytes;
+  static constexpr int kOffBar = kOffRowInfo + kRowInfoBytes;
+  static constexpr int kBarBytes = 8 * (2 * kSQ + 2 * kSA + 2 * kSB + 5) + 16;
   static constexpr int kSmem = kOffBar + kBarBytes + 1024;  // + alignment slack
   static constexpr int kTmemCols0 = 2 * NMAT * BN;
   static constexpr int kTmemCols = kTmemCols0 <= 32 ? 32 : kTmemCols0 <= 64 ? 64
                                    : kTmemCols0 <= 128 ? 128 : kTmemCols0 <= 256 ? 256 : 512;
-  static_assert(kSA >= 2, "not enough shared memory for two stages");
+  static_assert(kSB >= 3, "not enough shared memory for three token-tile stages");
   static_assert(kTmemCols0 <= 512, "accumulators exceed TMEM");
+  static_assert(kSmem <= 232448, "shared memory per CTA exceeded");
 };
 
 struct KParams {
-  CUtensorMap tm[4];  // packed codes: W[0], W[1], X[0], X[1]
+  CUtensorMap tm[5];  // packed codes W[0], W[1], X[0], X[1]; [4] activations A (row_index == null)
   GemmParams g;
 };
 
@@ -168,9 +191,10 @@ MOE_DEVINL uint16_t to_operand(float v) {
   }
 }
 
-template <int BN, int NMAT, int EPI, bool F16>
+template <int BN, int NMAT, int EPI, bool F16, int QK>
 __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_constant__ KParams kp) {
-  using C = Cfg<BN, NMAT>;
+  using C = Cfg<BN, NMAT, EPI, QK>;
+  constexpr int kSQ = C::kSQ;
   const GemmParams& g = kp.g;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -180,7 +204,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
   uint64_t* q_empty = q_full + kSQ;
   uint64_t* a_full = q_empty + kSQ;
   uint64_t* a_empty = a_full + C::kSA;
-  uint64_t* acc_full = a_empty + C::kSA;   // [2]
+  uint64_t* b_full = a_empty + C::kSA;
+  uint64_t* b_empty = b_full + C::kSB;
+  uint64_t* acc_full = b_empty + C::kSB;   // [2]
   uint64_t* acc_empty = acc_full + 2;      // [2]
   uint64_t* drain = acc_empty + 2;         // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -189,19 +215,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int MT = g.N / kTileM;
   const int KB = g.K / kKB;
+  const bool b_by_tma = g.row_index == nullptr;  // contiguous rows: one TMA tile per k-block
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSQ; ++i) {
       mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], 128);
+      mbar_init(&q_empty[i], 8);    // dequant warps
     }
     for (int i = 0; i < C::kSA; ++i) {
-      mbar_init(&a_full[i], 256);
+      mbar_init(&a_full[i], 8);     // dequant warps
       mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < C::kSB; ++i) {
+      mbar_init(&b_full[i], b_by_tma ? 1 : 2);  // TMA, or the gather warps
+      mbar_init(&b_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 128);
+      mbar_init(&acc_empty[i], 4);  // epilogue warps
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -218,6 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
       tma_prefetch_desc(&kp.tm[2]);
       if (NMAT == 2) tma_prefetch_desc(&kp.tm[3]);
     }
+    if (b_by_tma) tma_prefetch_desc(&kp.tm[4]);
   }
   tc_fence_before();
   __syncthreads();
@@ -229,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t policy = l2_policy_evict_last();
-      uint32_t it = 0;
+      uint32_t it = 0, qit = 0;
       bool alive = true;
       for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
         const TileInfo t = load_tile(g, u, MT);
@@ -240,22 +272,39 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
         const bool ext = t.group == g.n_groups;
         const int row = (ext ? 0 : t.group * g.N) + t.mt * kTileM;
         for (int kb = 0; kb < KB; ++kb, ++it) {
-          const int s = it % kSQ;
-          if (!mbar_wait(&q_empty[s], ((it / kSQ) & 1) ^ 1, abort_flag, g.status, 1)) {
-            alive = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&q_full[s], NMAT * kQBytes);
+          if (kb % QK == 0) {
+            const int s = qit % kSQ;
+            if (!mbar_wait(&q_empty[s], ((qit / kSQ) & 1) ^ 1, abort_flag, g.status, 1)) {
+              alive = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&q_full[s], NMAT * C::kQStage);
 #pragma unroll
-          for (int j = 0; j < NMAT; ++j)
-            tma_load_2d(smem + C::kOffQ + (s * NMAT + j) * kQBytes, &kp.tm[(ext ? 2 : 0) + j],
-                        kb * (kKB / 8), row, &q_full[s], policy);
+            for (int j = 0; j < NMAT; ++j)
+              tma_load_2d(smem + C::kOffQ + (s * NMAT + j) * C::kQStage, &kp.tm[(ext ? 2 : 0) + j],
+                          kb * (kKB / 8), row, &q_full[s], policy);
+            ++qit;
+          }
+          if (b_by_tma) {
+            const int sb = it % C::kSB;
+            if (!mbar_wait(&b_empty[sb], ((it / C::kSB) & 1) ^ 1, abort_flag, g.status, 10)) {
+              alive = false;
+              ++it;
+              break;
+            }
+            mbar_arrive_expect_tx(&b_full[sb], C::kBBytes);
+            tma_load_2d(smem + C::kOffB + sb * C::kBBytes, &kp.tm[4], kb * kKB, t.row0, &b_full[sb],
+                        policy);
+          }
         }
       }
       // drain: every issued load must land before the CTA exits
-      const uint32_t n_issued = it;
-      for (uint32_t j = n_issued > (uint32_t)kSQ ? n_issued - kSQ : 0; j < n_issued; ++j)
+      for (uint32_t j = qit > (uint32_t)kSQ ? qit - kSQ : 0; j < qit; ++j)
         mbar_wait(&q_full[j % kSQ], (j / kSQ) & 1, abort_flag, g.status, 2);
+      const uint32_t n_issued = it;
+      if (b_by_tma)
+        for (uint32_t j = n_issued > (uint32_t)C::kSB ? n_issued - C::kSB : 0; j < n_issued; ++j)
+          mbar_wait(&b_full[j % C::kSB], (j / C::kSB) & 1, abort_flag, g.status, 2);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -271,13 +320,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * (NMAT * BN);
         for (int kb = 0; kb < KB; ++kb, ++it) {
-          const int s = it % C::kSA;
-          if (!mbar_wait(&a_full[s], (it / C::kSA) & 1, abort_flag, g.status, 4)) {
+          const int s = it % C::kSA, sb = it % C::kSB;
+          if (!mbar_wait(&a_full[s], (it / C::kSA) & 1, abort_flag, g.status, 4) ||
+              !mbar_wait(&b_full[sb], (it / C::kSB) & 1, abort_flag, g.status, 4)) {
             alive = false;
             break;
           }
           tc_fence_after();
-          const uint32_t b_addr = smem_u32(smem + C::kOffB + s * C::kBBytes);
+          const uint32_t b_addr = smem_u32(smem + C::kOffB + sb * C::kBBytes);
 #pragma unroll
           for (int j = 0; j < NMAT; ++j) {
             const uint32_t a_addr = smem_u32(smem + C::kOffA + (s * NMAT + j) * kABytes);
@@ -287,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
                           smem_desc_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0);
           }
           tc_commit(&a_empty[s]);
+          tc_commit(&b_empty[sb]);
         }
         if (!alive) break;
         tc_commit(&acc_full[buf]);
@@ -296,11 +347,58 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
       tc_commit(drain);
       mbar_wait(drain, 0, abort_flag, g.status, 5);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ dequantise
-    const int m = threadIdx.x - 128;  // weight row inside the tile
-    uint32_t it = 0;
+    const int dt = threadIdx.x - 128;
+    const int m = dt & (kTileM - 1);  // weight row inside the tile
+    const int half = dt >> 7;         // codes half*32 .. half*32+31 of each k-block
+    uint32_t it = 0, qit = 0;
     bool alive = true;
+    // One k-block: wait for its packed codes and a free A stage, write the
+    // operand tile, signal the MMA; release the code stage after its last
+    // k-block (only once its codes are consumed: releasing right after the
+    // shared-memory loads let the next TMA refill land before those loads
+    // had returned their data).
+    auto step = [&](int kb, const uint32_t (&s2)[NMAT], const uint32_t (&b2)[NMAT]) -> bool {
+      const int sq = qit % kSQ;
+      if (kb % QK == 0 && !mbar_wait(&q_full[sq], (qit / kSQ) & 1, abort_flag, g.status, 6))
+        return false;
+      // this thread's 16 bytes of codes: row m, k-block kb % QK, half `half`
+      // (QK = 4: 128-byte rows, 16-byte chunk index XOR (m % 8) as TMA wrote them)
+      const int qoff = QK == 1 ? m * 32 + half * 16
+                               : m * 128 + ((((kb % QK) * 2 + half) ^ (m & 7)) << 4);
+      uint4 qw[NMAT];
+#pragma unroll
+      for (int j = 0; j < NMAT; ++j)
+        qw[j] = *reinterpret_cast<const uint4*>(smem + C::kOffQ + (sq * NMAT + j) * C::kQStage + qoff);
+      const int sa = it % C::kSA;
+      if (!mbar_wait(&a_empty[sa], ((it / C::kSA) & 1) ^ 1, abort_flag, g.status, 7)) return false;
+#pragma unroll
+      for (int j = 0; j < NMAT; ++j) {
+        uint8_t* a_tile = smem + C::kOffA + (sa * NMAT + j) * kABytes;
+        const uint32_t words[4] = {qw[j].x, qw[j].y, qw[j].z, qw[j].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 o;
+          if constexpr (F16)
+            o = dequant_word_f16(words[c], *reinterpret_cast<const __half2*>(&s2[j]),
+                                 *reinterpret_cast<const __half2*>(&b2[j]));
+          else
+            o = dequant_word(words[c], *reinterpret_cast<const __nv_bfloat162*>(&s2[j]),
+                             *reinterpret_cast<const __nv_bfloat162*>(&b2[j]));
+          *reinterpret_cast<uint4*>(a_tile + sw128_offset(m, half * 4 + c)) = o;
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive_warp(&a_full[sa]);
+      if (kb % QK == QK - 1) {
+        mbar_arrive_warp(&q_empty[sq]);
+        ++qit;
+      }
+      ++it;
+      return true;
+    };
+    const bool vec = (KB & 7) == 0;  // scale/bias rows load 8 groups (16 bytes) at a time
     for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
       const TileInfo t = load_tile(g, u, MT);
       if (!t.ok) continue;
@@ -314,66 +412,76 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
         sc[j] = w.scale + row * KB;
         bi[j] = w.bias + row * KB;
       }
-      for (int kb = 0; kb < KB; ++kb, ++it) {
-        uint32_t s2[NMAT], b2[NMAT];
+      if (vec) {
+        // 8 k-blocks per scale/bias load, unrolled so every word index is
+        // static (a runtime index would put the words in local memory); the
+        // next batch is loaded one batch ahead of use
+        uint4 s_nxt[NMAT], b_nxt[NMAT];
 #pragma unroll
         for (int j = 0; j < NMAT; ++j) {
-          s2[j] = splat_operand<F16>(__ldg(sc[j] + kb));
-          b2[j] = splat_operand<F16>(__ldg(bi[j] + kb));
+          s_nxt[j] = __ldg(reinterpret_cast<const uint4*>(sc[j]));
+          b_nxt[j] = __ldg(reinterpret_cast<const uint4*>(bi[j]));
         }
-        const int sq = it % kSQ;
-        if (!mbar_wait(&q_full[sq], (it / kSQ) & 1, abort_flag, g.status, 6)) {
-          alive = false;
-          break;
-        }
-        uint4 qw[NMAT][2];
+        for (int kb0 = 0; kb0 < KB && alive; kb0 += 8) {
+          uint4 s_cur[NMAT], b_cur[NMAT];
 #pragma unroll
-        for (int j = 0; j < NMAT; ++j) {
-          const uint4* src =
-              reinterpret_cast<const uint4*>(smem + C::kOffQ + (sq * NMAT + j) * kQBytes + m * 32);
-          qw[j][0] = src[0];
-          qw[j][1] = src[1];
-        }
-        const int sa = it % C::kSA;
-        if (!mbar_wait(&a_empty[sa], ((it / C::kSA) & 1) ^ 1, abort_flag, g.status, 7)) {
-          alive = false;
-          break;
-        }
+          for (int j = 0; j < NMAT; ++j) {
+            s_cur[j] = s_nxt[j];
+            b_cur[j] = b_nxt[j];
+            if (kb0 + 8 < KB) {
+              s_nxt[j] = __ldg(reinterpret_cast<const uint4*>(sc[j]) + (kb0 >> 3) + 1);
+              b_nxt[j] = __ldg(reinterpret_cast<const uint4*>(bi[j]) + (kb0 >> 3) + 1);
+            }
+          }
 #pragma unroll
-        for (int j = 0; j < NMAT; ++j) {
-          uint8_t* a_tile = smem + C::kOffA + (sa * NMAT + j) * kABytes;
-          const uint32_t words[8] = {qw[j][0].x, qw[j][0].y, qw[j][0].z, qw[j][0].w,
-                                     qw[j][1].x, qw[j][1].y, qw[j][1].z, qw[j][1].w};
+          for (int i = 0; i < 8; ++i) {
+            uint32_t s2[NMAT], b2[NMAT];
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint4 o;
-            if constexpr (F16)
-              o = dequant_word_f16(words[c], *reinterpret_cast<const __half2*>(&s2[j]),
-                                   *reinterpret_cast<const __half2*>(&b2[j]));
-            else
-              o = dequant_word(words[c], *reinterpret_cast<const __nv_bfloat162*>(&s2[j]),
-                               *reinterpret_cast<const __nv_bfloat162*>(&b2[j]));
-            *reinterpret_cast<uint4*>(a_tile + sw128_offset(m, c)) = o;
+            for (int j = 0; j < NMAT; ++j) {
+              const uint32_t sw = i < 2 ? s_cur[j].x : i < 4 ? s_cur[j].y : i < 6 ? s_cur[j].z : s_cur[j].w;
+              const uint32_t bw = i < 2 ? b_cur[j].x : i < 4 ? b_cur[j].y : i < 6 ? b_cur[j].z : b_cur[j].w;
+              s2[j] = splat_operand<F16>((uint16_t)(sw >> ((i & 1) * 16)));
+              b2[j] = splat_operand<F16>((uint16_t)(bw >> ((i & 1) * 16)));
+            }
+            if (!step(kb0 + i, s2, b2)) {
+              alive = false;
+              break;
+            }
           }
         }
-        fence_proxy_async_smem();
-        mbar_arrive(&a_full[sa]);
-        // Release the packed-code stage only now that its codes have been
-        // consumed: releasing it right after the shared-memory loads let the
-        // next TMA refill land before those loads had returned their data.
-        mbar_arrive(&q_empty[sq]);
+      } else {
+        for (int kb = 0; kb < KB; ++kb) {
+          uint32_t s2[NMAT], b2[NMAT];
+#pragma unroll
+          for (int j = 0; j < NMAT; ++j) {
+            s2[j] = splat_operand<F16>(__ldg(sc[j] + kb));
+            b2[j] = splat_operand<F16>(__ldg(bi[j] + kb));
+          }
+          if (!step(kb, s2, b2)) {
+            alive = false;
+            break;
+          }
+        }
       }
     }
-  } else if (warp >= 8 && warp < 12) {
+  } else if ((warp == 2 || warp == 3) && !b_by_tma) {
     // ------------------------------------------------------------ gather B
-    constexpr int kRowsPerThread = (BN * 8 + 127) / 128;  // 16-byte chunks per thread
-    const int gt = threadIdx.x - 256;
+    // 16-byte cp.async per (row, chunk) into the swizzled tile. A thread
+    // signals a step only once its copies have landed (wait_group, then the
+    // proxy fence, then the arrive), deferred by kD steps so that kD + 1
+    // steps of gathers are in flight at once. The arrival of step i comes
+    // after the issue of step i + kD, which waits for the MMA of step
+    // i + kD - kSB to release its stage: with kD = kSB - 2 that is the MMA of
+    // step i - 2, so the MMA of step i - 1 still runs while step i is being
+    // signalled (kD = kSB - 1 would make every MMA wait for the previous
+    // one to finish and the copies to be signalled: MMAs one at a time).
+    constexpr int kD = C::kSB - 2;
+    constexpr int kRowsPerThread = (BN * 8 + 63) / 64;  // 16-byte chunks per thread
+    const int gt = threadIdx.x - 64;
     const int c = gt & 7;           // chunk of the 128-byte row slice
-    const int n_first = gt >> 3;    // first row handled; rows n_first + 16*i
-    uint32_t it = 0;
+    const int n_first = gt >> 3;    // first row handled; rows n_first + 8*i
+    uint32_t it = 0, arrived = 0;
     bool alive = true;
-    bool pending = false;
-    int pending_sa = 0;
     for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
       const TileInfo t = load_tile(g, u, MT);
       if (!t.ok) continue;
@@ -381,12 +489,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
       bool valid[kRowsPerThread];
 #pragma unroll
       for (int i = 0; i < kRowsPerThread; ++i) {
-        const int n = n_first + 16 * i;
+        const int n = n_first + 8 * i;
         valid[i] = n < BN && n < t.rows;
         src_row[i] = 0;
         if (valid[i]) {
           const int64_t r = t.row0 + n;
-          const int64_t a = g.row_index ? (int64_t)g.row_index[r] : r;
+          const int64_t a = (int64_t)g.row_index[r];
           if (a < 0 || a >= g.A_rows) {
             report(g.status, MOE_DEV_BAD_ROW, 32, (int)r);
             valid[i] = false;
@@ -396,51 +504,72 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
         }
       }
       for (int kb = 0; kb < KB; ++kb, ++it) {
-        const int sa = it % C::kSA;
-        if (!mbar_wait(&a_empty[sa], ((it / C::kSA) & 1) ^ 1, abort_flag, g.status, 8)) {
+        const int sb = it % C::kSB;
+        if (!mbar_wait(&b_empty[sb], ((it / C::kSB) & 1) ^ 1, abort_flag, g.status, 8)) {
           alive = false;
           break;
         }
-        const uint32_t b_tile = smem_u32(smem + C::kOffB + sa * C::kBBytes);
+        const uint32_t b_tile = smem_u32(smem + C::kOffB + sb * C::kBBytes);
 #pragma unroll
         for (int i = 0; i < kRowsPerThread; ++i) {
-          const int n = n_first + 16 * i;
+          const int n = n_first + 8 * i;
           if (n < BN) {
             const uint16_t* src = g.A + src_row[i] * g.K + kb * kKB + c * 8;
             cp_async_16(b_tile + sw128_offset(n, c), src, valid[i] ? 16u : 0u);
           }
         }
         cp_async_commit();
-        if (pending) {
-          cp_async_wait<1>();
+        if (it + 1 - arrived > (uint32_t)kD) {  // step `arrived` is kD steps old: complete it
+          cp_async_wait<kD>();
           fence_proxy_async_smem();
-          mbar_arrive(&a_full[pending_sa]);
+          mbar_arrive_warp(&b_full[arrived % C::kSB]);
+          ++arrived;
         }
-        pending = true;
-        pending_sa = sa;
       }
     }
     cp_async_wait<0>();
-    if (pending) {
-      fence_proxy_async_smem();
-      mbar_arrive(&a_full[pending_sa]);
-    }
+    fence_proxy_async_smem();
+    for (; arrived < it; ++arrived) mbar_arrive_warp(&b_full[arrived % C::kSB]);
   } else if (warp >= 12) {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp & 3;             // TMEM lane quarter
-    const int m = ew * 32 + lane;        // weight row inside the tile
-    constexpr int CH = BN < 32 ? BN : 32;
-    uint32_t acc_it = 0;
+    // TMEM -> registers -> (NONE) direct fp32 stores, or (SWIGLU, COMBINE) a
+    // per-warp shared-memory staging tile of CH token rows x the warp's 32
+    // outputs, double buffered, written back one token-row segment per lane
+    // with a TMA bulk copy: a plain store (SWIGLU) or an fp32 add into the
+    // token's output row at L2 (COMBINE, the weighted combine of the routed
+    // experts and the shared one). Only warp-level syncs per chunk.
+    const int ew = warp & 3;             // TMEM lane quarter = the warp's 32 outputs
+    const int et = threadIdx.x - 384;    // 0..127 inside the epilogue group
+    constexpr int CH = C::kCH;
+    constexpr int kWarpStage = CH * 32;  // elements per staging buffer of one warp
+    float* s_rscale = reinterpret_cast<float*>(smem + C::kOffRowInfo);
+    int* s_orow = reinterpret_cast<int*>(s_rscale + BN);
+    uint8_t* stage_w = smem + C::kOffEpi + ew * 2 * kWarpStage * C::kStageElem;
+    uint32_t acc_it = 0, chunk = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const TileInfo t = load_tile(g, u, MT);
       if (!t.ok) continue;
       const uint32_t buf = acc_it & 1;
       if (!mbar_wait(&acc_full[buf], (acc_it >> 1) & 1, abort_flag, g.status, 9)) break;
       tc_fence_after();
+      if constexpr (EPI == MOE_EPI_COMBINE) {
+        named_bar_sync(1, 128);  // every epilogue warp is done with the previous tile's rows
+        for (int n = et; n < t.rows; n += 128) {
+          const int64_t r = (int64_t)t.row0 + n;
+          int orow = __ldg(g.out_row + r);
+          if (orow < 0 || orow >= g.C_rows) {
+            report(g.status, MOE_DEV_BAD_ROW, 33, (int)r);
+            orow = -1;
+          }
+          s_orow[n] = orow;
+          s_rscale[n] = __ldg(g.row_scale + r);
+        }
+        named_bar_sync(1, 128);
+      }
       const uint32_t taddr = tmem_base + ((uint32_t)(ew * 32) << 16) + buf * (NMAT * BN);
-      const int64_t col = (int64_t)t.mt * kTileM + m;
+      const int64_t col0 = (int64_t)t.mt * kTileM + ew * 32;  // this warp's first output
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += CH) {
+      for (int c0 = 0; c0 < BN; c0 += CH, ++chunk) {
         uint32_t v0[32], v1[32];
         if constexpr (CH == 32) {
           tmem_ld_32x32b_x32(taddr + c0, v0);
@@ -456,33 +585,55 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
           }
         }
         tc_wait_ld();
+        if constexpr (EPI == MOE_EPI_NONE) {
 #pragma unroll
-        for (int i = 0; i < CH; ++i) {
-          const int n = c0 + i;
-          if (n >= t.rows) break;
-          const int64_t r = (int64_t)t.row0 + n;
-          const float a = __uint_as_float(v0[i]);
-          if constexpr (EPI == MOE_EPI_NONE) {
-            static_cast<float*>(g.C)[r * g.ldc + col] = a;
-          } else if constexpr (EPI == MOE_EPI_SWIGLU) {
-            const float uval = __uint_as_float(v1[i]);
-            const float hval = a / (1.f + __expf(-a)) * uval;
-            static_cast<uint16_t*>(g.C)[r * g.ldc + col] = to_operand<F16>(hval);
+          for (int i = 0; i < CH; ++i) {
+            const int n = c0 + i;
+            if (n >= t.rows) break;
+            static_cast<float*>(g.C)[((int64_t)t.row0 + n) * g.ldc + col0 + lane] =
+                __uint_as_float(v0[i]);
+          }
+        } else {
+          const int sb = chunk & 1;
+          if (lane < CH) bulk_wait_read<1>();  // copies from two chunks ago read this buffer
+          __syncwarp();
+          if constexpr (EPI == MOE_EPI_COMBINE) {
+            float* S = reinterpret_cast<float*>(stage_w) + sb * kWarpStage;
+#pragma unroll
+            for (int i = 0; i < CH; ++i) S[i * 32 + lane] = __uint_as_float(v0[i]) * s_rscale[c0 + i];
           } else {
-            const int orow = __ldg(g.out_row + r);
-            if (orow < 0 || orow >= g.C_rows) {
-              report(g.status, MOE_DEV_BAD_ROW, 33, (int)r);
-            } else {
-              atomicAdd(static_cast<float*>(g.C) + (int64_t)orow * g.ldc + col,
-                        __ldg(g.row_scale + r) * a);
+            uint16_t* S = reinterpret_cast<uint16_t*>(stage_w) + sb * kWarpStage;
+#pragma unroll
+            for (int i = 0; i < CH; ++i) {
+              const float a = __uint_as_float(v0[i]);
+              S[i * 32 + lane] = to_operand<F16>(a / (1.f + __expf(-a)) * __uint_as_float(v1[i]));
             }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane < CH) {
+            const int n = c0 + lane;
+            if (n < t.rows) {
+              if constexpr (EPI == MOE_EPI_COMBINE) {
+                const int orow = s_orow[n];
+                const float* src = reinterpret_cast<const float*>(stage_w) + sb * kWarpStage + lane * 32;
+                if (orow >= 0)
+                  bulk_reduce_add_f32(static_cast<float*>(g.C) + (int64_t)orow * g.ldc + col0, src, 128);
+              } else {
+                const uint16_t* src =
+                    reinterpret_cast<const uint16_t*>(stage_w) + sb * kWarpStage + lane * 32;
+                bulk_store(static_cast<uint16_t*>(g.C) + ((int64_t)t.row0 + n) * g.ldc + col0, src, 64);
+              }
+            }
+            bulk_commit();
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(&acc_empty[buf]);
+      mbar_arrive_warp(&acc_empty[buf]);
       ++acc_it;
     }
+    if (lane < CH) bulk_wait_all();  // every bulk copy has landed before the CTA exits
   }
 
   tc_fence_before();
@@ -507,22 +658,37 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 }
 
 // Packed codes viewed as a 2-D uint32 tensor [rows][K/8]; box 8 words x 128 rows.
-bool make_q_map(CUtensorMap* tm, const uint32_t* q, int64_t rows, int K) {
+bool make_q_map(CUtensorMap* tm, const uint32_t* q, int64_t rows, int K, int qk) {
   auto fn = get_encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)(K / 8) * 4};
-  const cuuint32_t box[2] = {kKB / 8, kTileM};
+  const cuuint32_t box[2] = {(cuuint32_t)(kKB / 8 * qk), kTileM};
   const cuuint32_t estr[2] = {1, 1};
   return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(q), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            qk == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int NMAT, int EPI, bool F16>
+// Activations viewed as a 2-D 16-bit tensor [rows][K]; box 64 x box_rows,
+// 128-byte swizzle: exactly the K-major B operand tile the MMA reads.
+bool make_act_map(CUtensorMap* tm, const uint16_t* A, int64_t rows, int K, int box_rows) {
+  auto fn = get_encode_fn();
+  if (!fn || rows < 1) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {kKB, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(A), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int NMAT, int EPI, bool F16, int QK>
 cudaError_t launch_t(const KParams& kp, cudaStream_t s) {
-  using C = Cfg<BN, NMAT>;
-  auto kern = gemm_w4_kernel<BN, NMAT, EPI, F16>;
+  using C = Cfg<BN, NMAT, EPI, QK>;
+  auto kern = gemm_w4_kernel<BN, NMAT, EPI, F16, QK>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (err != cudaSuccess) return err;
@@ -535,23 +701,25 @@ cudaError_t launch_t(const KParams& kp, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int NMAT, int EPI, bool F16>
+template <int NMAT, int EPI, bool F16, int QK>
 cudaError_t launch_bn(const KParams& kp, cudaStream_t s) {
   switch (kp.g.block_n) {
-    case 16: return launch_t<16, NMAT, EPI, F16>(kp, s);
-    case 32: return launch_t<32, NMAT, EPI, F16>(kp, s);
-    case 64: return launch_t<64, NMAT, EPI, F16>(kp, s);
-    case 128: return launch_t<128, NMAT, EPI, F16>(kp, s);
+    case 16: return launch_t<16, NMAT, EPI, F16, QK>(kp, s);
+    case 32: return launch_t<32, NMAT, EPI, F16, QK>(kp, s);
+    case 64: return launch_t<64, NMAT, EPI, F16, QK>(kp, s);
+    case 128: return launch_t<128, NMAT, EPI, F16, QK>(kp, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <bool F16>
+int q_kblocks_per_stage(int K) { return (K / kKB) % 4 == 0 ? 4 : 1; }
+
+template <bool F16, int QK>
 cudaError_t launch_epi(const KParams& kp, cudaStream_t s) {
   switch (kp.g.epilogue) {
-    case MOE_EPI_NONE: return launch_bn<1, MOE_EPI_NONE, F16>(kp, s);
-    case MOE_EPI_SWIGLU: return launch_bn<2, MOE_EPI_SWIGLU, F16>(kp, s);
-    case MOE_EPI_COMBINE: return launch_bn<1, MOE_EPI_COMBINE, F16>(kp, s);
+    case MOE_EPI_NONE: return launch_bn<1, MOE_EPI_NONE, F16, QK>(kp, s);
+    case MOE_EPI_SWIGLU: return launch_bn<2, MOE_EPI_SWIGLU, F16, QK>(kp, s);
+    case MOE_EPI_COMBINE: return launch_bn<1, MOE_EPI_COMBINE, F16, QK>(kp, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -563,12 +731,16 @@ cudaError_t gemm_w4_launch(const GemmParams& p, cudaStream_t s) {
   memset(&kp, 0, sizeof kp);
   kp.g = p;
   const int nmat = p.epilogue == MOE_EPI_SWIGLU ? 2 : 1;
+  const int qk = q_kblocks_per_stage(p.K);
   for (int j = 0; j < nmat; ++j) {
-    if (!make_q_map(&kp.tm[j], p.W[j].q, (int64_t)p.n_groups * p.N, p.K))
+    if (!make_q_map(&kp.tm[j], p.W[j].q, (int64_t)p.n_groups * p.N, p.K, qk))
       return cudaErrorInvalidValue;
-    if (p.X[0].q && !make_q_map(&kp.tm[2 + j], p.X[j].q, p.N, p.K)) return cudaErrorInvalidValue;
+    if (p.X[0].q && !make_q_map(&kp.tm[2 + j], p.X[j].q, p.N, p.K, qk)) return cudaErrorInvalidValue;
   }
-  return p.operand_f16 ? launch_epi<true>(kp, s) : launch_epi<false>(kp, s);
+  if (!p.row_index && !make_act_map(&kp.tm[4], p.A, p.A_rows, p.K, p.block_n))
+    return cudaErrorInvalidValue;
+  if (qk == 4) return p.operand_f16 ? launch_epi<true, 4>(kp, s) : launch_epi<false, 4>(kp, s);
+  return p.operand_f16 ? launch_epi<true, 1>(kp, s) : launch_epi<false, 1>(kp, s);
 }
 
 }  // namespace moe

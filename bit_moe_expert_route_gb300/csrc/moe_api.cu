@@ -132,7 +132,8 @@ DecWs decode_ws(void* ws, const moe_shape_t* s) {
 }
 
 bool w4_ok(const moe_w4_t& w) {
-  return w.q && w.scale && w.bias && aligned(w.q, 16) && aligned(w.scale, 4) && aligned(w.bias, 4);
+  return w.q && w.scale && w.bias && aligned(w.q, 16) && aligned(w.scale, 16) &&
+         aligned(w.bias, 16);
 }
 
 int check_weights(const moe_weights_t* w, const moe_shape_t* s) {
@@ -259,6 +260,9 @@ int moe_grouped_gemm_w4a16(const uint16_t* A, int64_t A_rows, int K, const int32
       max_tiles < 0 || !valid_block_n(block_n, false) || ldc < N || C_rows < 0)
     return MOE_ERR_SHAPE;
   if (epilogue != MOE_EPI_COMBINE && C_rows < n_rows) return MOE_ERR_SHAPE;
+  // SWIGLU and COMBINE write 16-byte token-row segments (bulk copies)
+  if (epilogue == MOE_EPI_SWIGLU && ldc % 8) return MOE_ERR_SHAPE;
+  if (epilogue == MOE_EPI_COMBINE && ldc % 4) return MOE_ERR_SHAPE;
   if (!A || !W || !block_map || !num_tiles || !C) return MOE_ERR_NULL;
   if (epilogue == MOE_EPI_COMBINE && (!row_scale || !out_row)) return MOE_ERR_NULL;
   const int nmat = epilogue == MOE_EPI_SWIGLU ? 2 : 1;

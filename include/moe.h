@@ -29,8 +29,8 @@
  *       scale bf16   [G][N][K/group]
  *       bias  bf16   [G][N][K/group]
  *     element value w[g][n][k] = scale * q + bias (one scale/bias per group
- *     of `group` consecutive codes along K). q must be 16-byte aligned,
- *     scale and bias 4-byte aligned.
+ *     of `group` consecutive codes along K). q, scale and bias must be
+ *     16-byte aligned.
  *   - Supported sizes: group == 64; d_model and d_ff multiples of 128;
  *     1 <= top_k <= 32, top_k <= n_experts <= 1024; d_ff_shared == d_ff
  *     when a shared expert is present.
@@ -177,7 +177,8 @@ int moe_route(const float* logits, const float* logit_bias, int T, int n_experts
  *   out_row     COMBINE: int32 [n_rows] destination row of each GEMM row.
  *   C           NONE: fp32 [n_rows][ldc]; SWIGLU: [n_rows][ldc] of the operand type;
  *               COMBINE: fp32 [C_rows][ldc], accumulated with atomic adds
- *               (order of the adds is not fixed). ldc >= N, in elements.
+ *               (order of the adds is not fixed). ldc >= N, in elements;
+ *               SWIGLU needs ldc % 8 == 0, COMBINE ldc % 4 == 0.
  *   N           output columns (multiple of 128); K multiple of 64.
  *   ws          256-byte aligned, >= moe_gemm_workspace_bytes() bytes.
  * block_n in {16, 32, 64, 128}.
