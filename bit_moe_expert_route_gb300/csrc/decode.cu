@@ -1,34 +1,51 @@
-// Batch-1 decode: one token through the MoE layer with matrix-vector kernels
-// that stream only the router, the shared expert and the top-k selected
+// Batch-1 decode: one token through the MoE layer with matrix-vector work
+// that streams only the router, the shared expert and the top-k selected
 // experts' packed 4-bit weights. ("Perplexity's Lily Beats MLX-LM by 1.35x
 // Running Qwen3.6 on Apple Silicon", section "Why prefill and decode get
 // different treatment": batch-1 decode is bound by reading the weights, and
-// uses matrix-vector kernels on the vector ALUs.)
+// uses matrix-vector work on the vector ALUs.)
 //
-// Three launches chained with programmatic dependent launch (PDL). Each
-// kernel first issues the loads that do not depend on the previous kernel
-// (weights, and x), then waits (griddepcontrol.wait), so its weight traffic
-// overlaps the previous kernel's tail:
-//   1. decode_router_shared_kernel  router logits (8 complete logits per
-//        block), the shared gate logit, and the shared expert's gate/up rows
-//        (h of the shared slot).
-//   2. decode_gateup_kernel   every block selects the top k from the logits
-//        (warp argmax, ties to the lower id; block 0 also stores ids, weights
-//        and the gate), then the routed experts' gate/up rows, h = silu(g)*u.
-//   3. decode_down_kernel     selects the top k the same way before its wait
-//        (kernel 1 has completed by then) and issues its down-row loads, then
-//        waits for h; one warp per output column sums every slot's down row,
-//        weighted, in slot order, rounded once to bf16.
-// The selection is recomputed per block instead of being published by a
-// last-block-done step: it costs one L2 read of E logits per block and
-// removes a fence, an atomic and a dependent round trip from the path.
+// One persistent launch per layer: G blocks (one per SM), 256 threads each.
+//   before the dependency wait (griddepcontrol.wait; nothing here depends on
+//     the previous kernel): TMA bulk copies of this block's shared-expert
+//     gate/up rows and shared-expert down rows into shared memory, and
+//     register loads of its slice of the router.
+//   phase A  x into shared memory (one round trip); router partial logits
+//     over this block's (8 experts x d/KS rows) slice and the matching partial
+//     of the shared gate logit x . w_sg; h of its shared-expert rows.
+//   phase B  every block polls the KS partials of each logit (summed in a
+//     fixed order), selects the top k itself (two-level rank count,
+//     descending, ties to the lower id) and issues its bulk copies: the
+//     routed gate/up rows of its share of the k * d_ff row pairs and the
+//     routed down rows of its share of the d_model outputs; then h of its
+//     row pairs.
+//   phase C  every block polls h of every slot into shared memory and
+//     computes its outputs: every slot's down row, weighted, in slot order,
+//     rounded once to bf16.
+// Cross-block values are published as 64-bit {value, call epoch} words, so a
+// reader's poll is both the synchronisation and the load: one L2 round trip
+// per dependency. Block 0 stores the epoch for the next call at its end; no
+// counter needs resetting, so consecutive calls on one workspace stay one
+// chain of programmatic dependent launches, and the next layer's blocks
+// (two blocks fit per SM) fetch their weights while this layer runs.
 //
-// Dot products per 16-byte chunk (32 codes, half a group): a code q becomes the
-// float f = 1 + q/16 exactly (bit pattern 0x3F800000 | q << 19), so
-// sum_k (s*q_k + b) v_k = 16 s * sum_k f_k v_k + (b - 16 s) * sum_k v_k,
-// with the activation chunk sums taken once per chunk. f stays in [1, 2), so
-// the fp32 sums cancel no more than a factor of a few.
+// Every block runs each phase once per launch, so the kernel's instruction
+// footprint, fetched cold from L2 on every SM, matters as much as its
+// arithmetic: each computation has one copy of its code (two rows, or two
+// output columns, per pass; an odd one out runs as a duplicate).
+//
+// Dot products per packed word (8 codes; 4 words = 32 codes = half a group):
+// a code q becomes the 16-bit float f = 1 + q/16 exactly (bf16 bits
+// 0x3F80 | q << 3, f16 bits 0x3C00 | q << 6), two codes per shift-and-mask,
+// and is multiplied with the activation by a mixed-precision FMA (16-bit
+// inputs, fp32 accumulate; the product is exact). With the activation chunk
+// sums taken once,
+//   sum_k (s*q_k + b) v_k = 16 s * sum_k f_k v_k + (b - 16 s) * sum_k v_k.
+// f stays in [1, 2), so the fp32 sums cancel no more than a factor of a few.
+// x enters as its own bf16 values; h (the SwiGLU output) enters the down
+// projection rounded to f16, as in the prefill path.
 #include <climits>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -37,52 +54,76 @@ namespace moe {
 namespace {
 
 constexpr uint32_t kFull = 0xFFFFFFFFu;
-// XC = chunks of a d_model-long row per lane = d_model / 1024 (d_model <= 4096).
+constexpr int kDecThreads = 256;
+constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kRouterPre = 2;  // router rows per thread loaded before the dependency wait
 
 MOE_DEVINL void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 MOE_DEVINL void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
-// f = 1 + q/16 for code n (0..7) of a packed word.
-MOE_DEVINL float code_f(uint32_t w, int n) {
-  const int sh = 19 - 4 * n;
-  const uint32_t v = sh >= 0 ? (w << sh) : (w >> (-sh));
-  return __uint_as_float((v & 0x00780000u) | 0x3F800000u);
+// 1-D TMA bulk copy global -> this CTA's shared memory, completing on `bar`.
+MOE_DEVINL void bulk_load(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
-// sum over the 32 codes of a chunk of f_k * v_k, v in registers.
-MOE_DEVINL float chunk_fdot(const uint4 q, const float (&v)[32]) {
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-  float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-#pragma unroll
-    for (int n = 0; n < 8; n += 2) {
-      a0 = fmaf(code_f(w[i], n), v[8 * i + n], a0);
-      a1 = fmaf(code_f(w[i], n + 1), v[8 * i + n + 1], a1);
+// Bounded wait on a shared-memory barrier phase (every thread).
+MOE_DEVINL void bar_wait(uint64_t* bar, uint32_t parity, int32_t* status, int where) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+      report(status, MOE_DEV_TIMEOUT, where, (int)threadIdx.x);
+      return;
     }
   }
-  return a0 + a1;
 }
 
-// Same with v in swizzled shared memory (float4 j of chunk c at c*8 + (j ^ (c & 7))).
-MOE_DEVINL int chunk_slot(int c, int j) { return c * 8 + (j ^ (c & 7)); }
-MOE_DEVINL float chunk_fdot_smem(const uint4 q, const float4* __restrict__ v, int c) {
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-  float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float4 v0 = v[chunk_slot(c, 2 * i)];
-    const float4 v1 = v[chunk_slot(c, 2 * i + 1)];
-    a0 = fmaf(code_f(w[i], 0), v0.x, a0);
-    a1 = fmaf(code_f(w[i], 1), v0.y, a1);
-    a0 = fmaf(code_f(w[i], 2), v0.z, a0);
-    a1 = fmaf(code_f(w[i], 3), v0.w, a1);
-    a0 = fmaf(code_f(w[i], 4), v1.x, a0);
-    a1 = fmaf(code_f(w[i], 5), v1.y, a1);
-    a0 = fmaf(code_f(w[i], 6), v1.z, a0);
-    a1 = fmaf(code_f(w[i], 7), v1.w, a1);
+// ---------------------------------------------------------------- dot products
+// a0 += f_lo * v_lo, a1 += f_hi * v_hi for one pair of 16-bit values.
+template <bool BF16>
+MOE_DEVINL void fma_pair(float& a0, float& a1, uint32_t f, uint32_t v) {
+  if constexpr (BF16)
+    asm("{ .reg .b16 fl, fh, vl, vh;\n\t mov.b32 {fl, fh}, %2;\n\t mov.b32 {vl, vh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, fl, vl, %0;\n\t fma.rn.f32.bf16 %1, fh, vh, %1; }"
+        : "+f"(a0), "+f"(a1)
+        : "r"(f), "r"(v));
+  else
+    asm("{ .reg .b16 fl, fh, vl, vh;\n\t mov.b32 {fl, fh}, %2;\n\t mov.b32 {vl, vh}, %3;\n\t"
+        "fma.rn.f32.f16 %0, fl, vl, %0;\n\t fma.rn.f32.f16 %1, fh, vh, %1; }"
+        : "+f"(a0), "+f"(a1)
+        : "r"(f), "r"(v));
+}
+
+// a0/a1 += sum over the 8 codes of word w of f_k * v_k, v given as the four
+// pairs (v_i, v_{i+4}), i = 0..3 (vp.x .. vp.w): shifting w puts codes i
+// and i+4 (bits 4i and 16 + 4i) at the two halves' mantissa tops together.
+template <bool BF16>
+MOE_DEVINL void word_fdot(uint32_t w, const uint4& vp, float& a0, float& a1) {
+  if constexpr (BF16) {
+    constexpr uint32_t m = 0x00780078u, one = 0x3F803F80u;
+    fma_pair<true>(a0, a1, ((w << 3) & m) | one, vp.x);
+    fma_pair<true>(a0, a1, ((w >> 1) & m) | one, vp.y);
+    fma_pair<true>(a0, a1, ((w >> 5) & m) | one, vp.z);
+    fma_pair<true>(a0, a1, ((w >> 9) & m) | one, vp.w);
+  } else {
+    constexpr uint32_t m = 0x03C003C0u, one = 0x3C003C00u;
+    fma_pair<false>(a0, a1, ((w << 6) & m) | one, vp.x);
+    fma_pair<false>(a0, a1, ((w << 2) & m) | one, vp.y);
+    fma_pair<false>(a0, a1, ((w >> 2) & m) | one, vp.z);
+    fma_pair<false>(a0, a1, ((w >> 6) & m) | one, vp.w);
   }
-  return a0 + a1;
+}
+
+// The four pairs (v_i, v_{i+4}) of 8 consecutive 16-bit values held as 4
+// words (v0 v1), (v2 v3), (v4 v5), (v6 v7).
+MOE_DEVINL uint4 pair_up(uint4 v) {
+  return make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
+                    __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
 }
 
 // 16 s and (b - 16 s) of a group, from bf16 scale/bias bits.
@@ -91,376 +132,770 @@ MOE_DEVINL float2 affine_f(uint16_t sbits, uint16_t bbits) {
   return make_float2(s16, bf16_bits_to_f32(bbits) - s16);
 }
 
-// x chunks of this lane (c = lane + 32 i) as fp32 registers, and their sums.
-template <int XC>
-struct XChunks {
-  float v[XC][32];
-  float sum[XC];
+// ---------------------------------------------------------------- publishing
+// Values other blocks read (router partials, h) are published as 64-bit words
+// {value bits, call epoch}: a reader polls a word until its epoch is this
+// call's, so one L2 round trip both synchronises and delivers the value. The
+// epoch is one more than the last call's (kept in the workspace by block 0).
+MOE_DEVINL void publish(unsigned long long* w, float v, uint32_t epoch) {
+  const unsigned long long x = ((unsigned long long)epoch << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(w), "l"(x) : "memory");
+}
+MOE_DEVINL unsigned long long ld_word(const unsigned long long* w) {
+  unsigned long long x;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(x) : "l"(w) : "memory");
+  return x;
+}
+MOE_DEVINL void ld_word2(const unsigned long long* w, unsigned long long& a, unsigned long long& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(w) : "memory");
+}
+MOE_DEVINL bool word_ready(unsigned long long x, uint32_t epoch) { return (uint32_t)(x >> 32) == epoch; }
+MOE_DEVINL float word_value(unsigned long long x) { return __uint_as_float((uint32_t)x); }
+
+// Bounded poll helper: true while the caller should keep polling.
+struct Poll {
+  uint64_t t0 = 0;
+  uint32_t i = 0;
+  MOE_DEVINL bool again(int32_t* status, int where) {
+    if (++i == 32) t0 = globaltimer_ns();
+    if (i > 32) {
+      __nanosleep(32);
+      if ((i & 63) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+        report(status, MOE_DEV_TIMEOUT, where, (int)blockIdx.x);
+        return false;
+      }
+    }
+    return true;
+  }
 };
 
-template <int XC>
-MOE_DEVINL void load_x_chunks(const uint16_t* __restrict__ x, int nch, XChunks<XC>& xc) {
-  const int lane = threadIdx.x & 31;
+// ---------------------------------------------------------------- layout
+// Shared memory of one block (byte offsets from a 128-byte aligned base):
+//   Y   row pairs: gate codes [capY][d/2], up codes [capY][d/2], gate scale,
+//       gate bias, up scale, up bias [capY][d/64] each (bf16). Phase C reuses
+//       it for h as f16 pairs (see pair_slot), then the h chunk sums (fp32).
+//   X   down rows per slot s (S = k routed + shared): codes [capX][f/2],
+//       scale, bias [capX][f/64] each.
+//   Z   the shared expert's row pairs, laid out as in Y with capS rows.
+//   XP  x as bf16 pairs (see pair_slot) [d/32 chunks][4 words], then the x
+//       chunk sums (fp32 [d/32]).
+//   K   the keys [E] and the top-k candidates.
+//   then the selection and reduction scratch and the two bulk-copy barriers.
+struct DecSmem {
+  uint8_t* Y;
+  uint8_t* X;
+  uint8_t* Z;
+  uint4* xp;        // [d/32 * 4]
+  float* xsum;      // [d/32]
+  float* keys;      // [E]
+  float* cand_key;  // [8 * kc]
+  int* cand_id;     // [8 * kc]
+  int* s_ids;       // [32]
+  float* s_z;       // [32]
+  float* s_w;       // [33]: routing weights, then the shared gate
+  float* red;       // [8][9]
+  float* s_gp;      // [kDecodeMaxSplits] gate-logit partials
+  uint32_t* s_epoch;
+  uint64_t* barY;
+  uint64_t* barX;
+  uint64_t* barZ;
+};
+
+MOE_DEVINL DecSmem carve_dec_smem(uint8_t* base, const DecodeParams& p) {
+  DecSmem m;
+  m.Y = base;
+  m.X = base + p.y_bytes;
+  m.Z = m.X + p.x_bytes;
+  uint8_t* u = m.Z + p.z_bytes;
+  m.xp = reinterpret_cast<uint4*>(u);
+  m.xsum = reinterpret_cast<float*>(u + (size_t)p.d * 2);
+  m.keys = m.xsum + ((p.d / 32 + 3) & ~3);
+  const int kc = min(p.k, p.E / 8);
+  m.cand_key = m.keys + p.E;
+  m.cand_id = reinterpret_cast<int*>(m.cand_key + 8 * kc);
+  float* f = reinterpret_cast<float*>(u + p.u_bytes);
+  m.s_ids = reinterpret_cast<int*>(f);
+  f += 32;
+  m.s_z = f;
+  f += 32;
+  m.s_w = f;
+  f += 40;
+  m.red = f;
+  f += 8 * 9;
+  m.s_gp = f;
+  f += kDecodeMaxSplits;
+  m.s_epoch = reinterpret_cast<uint32_t*>(f);
+  f += 2;
+  m.barY = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(f) + 7) & ~uintptr_t(7));
+  m.barX = m.barY + 1;
+  m.barZ = m.barY + 2;
+  return m;
+}
+
+// Activations (x, and h in phase C) are held as 16-byte words of four pairs
+// (v_i, v_{i+4}), one word per 8 values, 4 words per 32-value chunk. Word j
+// of chunk c is slot c*4 + (j ^ ((c >> 1) & 3)): the 8 lanes of a wavefront
+// reading word j of chunks c..c+7 then hit 8 different bank groups.
+MOE_DEVINL int pair_slot(int c, int j) { return c * 4 + (j ^ ((c >> 1) & 3)); }
+// 16-bit element index of value i inside that layout.
+MOE_DEVINL int pair_elem(int i) { return pair_slot(i >> 5, (i >> 3) & 3) * 8 + (i & 3) * 2 + ((i >> 2) & 1); }
+
+// Row-pair views inside Y.
+struct RowPairSmem {
+  const uint4* gq;
+  const uint4* uq;
+  const uint16_t *gs, *gb, *us, *ub;
+};
+
+MOE_DEVINL RowPairSmem rowpair_smem(const uint8_t* Y, int capY, int i, int d) {
+  RowPairSmem r;
+  const size_t half_row = (size_t)d / 2, groups = (size_t)d / 64;
+  r.gq = reinterpret_cast<const uint4*>(Y + i * half_row);
+  r.uq = reinterpret_cast<const uint4*>(Y + ((size_t)capY + i) * half_row);
+  const uint16_t* s0 = reinterpret_cast<const uint16_t*>(Y + (size_t)capY * d);
+  r.gs = s0 + i * groups;
+  r.gb = s0 + (capY + i) * groups;
+  r.us = s0 + (2 * capY + i) * groups;
+  r.ub = s0 + (3 * capY + i) * groups;
+  return r;
+}
+
+MOE_DEVINL uint32_t word_of(const uint4& q, int j) { return j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w; }
+
+// v * 1/(1 + e^-v) with a correctly rounded reciprocal (no division slow path)
+MOE_DEVINL float silu(float v) { return v * __frcp_rn(1.f + expf(-v)); }
+
+// h of rows [0, n) of Y (row i = flattened row pair r0 + i), four rows per
+// warp per pass (rows i, i+8, i+16, i+24; those past n run as duplicates of
+// row i): h = silu(x . g) * (x . u), published and stored plainly for the
+// workspace view. Lanes take the 32-code chunks c = lane, lane + 32, ...;
+// 16 independent FMA chains each.
+constexpr int kRowsPerPass = 4;
+__device__ __noinline__ void rows_h(const DecodeParams& p, const uint8_t* Y, int cap, const uint4* xp,
+                                    const float* xsum, int n, int r0, uint32_t epoch) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, d = p.d, nch = d / 32;
+#pragma unroll 1
+  for (int i = warp; i < n; i += kRowsPerPass * kDecWarps) {
+    RowPairSmem r[kRowsPerPass];
 #pragma unroll
-  for (int i = 0; i < XC; ++i) {
-    const int c = lane + 32 * i;
-    float s = 0.f;
-    if (c < nch) {
-      const uint4* src = reinterpret_cast<const uint4*>(x + 32 * c);
+    for (int t = 0; t < kRowsPerPass; ++t) {
+      const int it = i + t * kDecWarps;
+      r[t] = rowpair_smem(Y, cap, it < n ? it : i, d);
+    }
+    float acc[2 * kRowsPerPass];  // gate, up of each row
+#pragma unroll
+    for (int m = 0; m < 2 * kRowsPerPass; ++m) acc[m] = 0.f;
+#pragma unroll 1
+    for (int c = lane; c < nch; c += 32) {
+      uint4 q[2 * kRowsPerPass];
+#pragma unroll
+      for (int t = 0; t < kRowsPerPass; ++t) {
+        q[2 * t] = r[t].gq[c];
+        q[2 * t + 1] = r[t].uq[c];
+      }
+      float lo[2 * kRowsPerPass], hi[2 * kRowsPerPass];
+#pragma unroll
+      for (int m = 0; m < 2 * kRowsPerPass; ++m) lo[m] = hi[m] = 0.f;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint4 b = src[j];
-        const uint32_t u[4] = {b.x, b.y, b.z, b.w};
+        const uint4 vp = xp[pair_slot(c, j)];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          xc.v[i][8 * j + 2 * t] = __uint_as_float(u[t] << 16);
-          xc.v[i][8 * j + 2 * t + 1] = __uint_as_float(u[t] & 0xFFFF0000u);
-          s += xc.v[i][8 * j + 2 * t] + xc.v[i][8 * j + 2 * t + 1];
-        }
+        for (int m = 0; m < 2 * kRowsPerPass; ++m) word_fdot<true>(word_of(q[m], j), vp, lo[m], hi[m]);
+      }
+      const int g = c >> 1;
+      const float xs = xsum[c];
+#pragma unroll
+      for (int t = 0; t < kRowsPerPass; ++t) {
+        const float2 ag = affine_f(r[t].gs[g], r[t].gb[g]), au = affine_f(r[t].us[g], r[t].ub[g]);
+        acc[2 * t] = fmaf(ag.x, lo[2 * t] + hi[2 * t], fmaf(ag.y, xs, acc[2 * t]));
+        acc[2 * t + 1] = fmaf(au.x, lo[2 * t + 1] + hi[2 * t + 1], fmaf(au.y, xs, acc[2 * t + 1]));
       }
     }
-    xc.sum[i] = s;
-  }
-}
-
-// One gate row and one up row (K = d codes, group 64): this lane's chunks.
-template <int XC>
-struct RowPairLoads {
-  uint4 g[XC], u[XC];
-  uint16_t gs[XC], gb[XC], us[XC], ub[XC];
-};
-
-template <int XC>
-MOE_DEVINL void load_rowpair(const moe_w4_t& G, const moe_w4_t& U, int64_t r, int d,
-                             RowPairLoads<XC>& L) {
-  const int lane = threadIdx.x & 31, nch = d / 32;
-  const uint4* gq = reinterpret_cast<const uint4*>(G.q + r * (d / 8));
-  const uint4* uq = reinterpret_cast<const uint4*>(U.q + r * (d / 8));
-  const int64_t gr = r * (d / 64);
 #pragma unroll
-  for (int i = 0; i < XC; ++i) {
-    const int c = lane + 32 * i;
-    if (c < nch) {
-      L.g[i] = __ldcs(gq + c);
-      L.u[i] = __ldcs(uq + c);
-      L.gs[i] = __ldcs(G.scale + gr + (c >> 1));
-      L.gb[i] = __ldcs(G.bias + gr + (c >> 1));
-      L.us[i] = __ldcs(U.scale + gr + (c >> 1));
-      L.ub[i] = __ldcs(U.bias + gr + (c >> 1));
+    for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+      for (int m = 0; m < 2 * kRowsPerPass; ++m) acc[m] += __shfl_xor_sync(kFull, acc[m], off);
+    if (lane < kRowsPerPass && i + lane * kDecWarps < n) {
+      float g = acc[0], u = acc[1];
+#pragma unroll
+      for (int t = 1; t < kRowsPerPass; ++t)
+        if (lane == t) {
+          g = acc[2 * t];
+          u = acc[2 * t + 1];
+        }
+      const int row = r0 + i + lane * kDecWarps;
+      const float v = silu(g) * u;
+      p.h[row] = v;
+      publish(p.pub_h + row, v, epoch);
     }
   }
 }
 
-// h = silu(x . g_row) * (x . u_row), warp-reduced, valid on every lane.
-template <int XC>
-MOE_DEVINL float rowpair_h(const RowPairLoads<XC>& L, const XChunks<XC>& xc, int d) {
-  const int lane = threadIdx.x & 31, nch = d / 32;
-  float ag = 0.f, au = 0.f;
+// Output columns [j0, j0 + nj) from the down rows in X and h (f16 pairs in
+// hp, chunk sums in hsum), two columns per warp per pass (the same h words
+// serve both): over the flattened (slot, chunk) index idx = lane + 32 i,
+// each slot's part weighted by its routing weight; rounded once to bf16.
+__device__ __noinline__ void down_cols(const DecodeParams& p, const uint8_t* X, const uint4* hp,
+                                       const float* hsum, const float* s_w, int total, int j0, int nj) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, f = p.f, fch = f / 32;
+  const size_t half_row = f / 2, groups = f / 64;
+  const size_t slot_bytes = (size_t)p.capX * (half_row + 4 * groups);
+#pragma unroll 1
+  for (int j = warp; j < nj; j += 2 * kDecWarps) {
+    const int j1 = j + kDecWarps < nj ? j + kDecWarps : j;
+    float acc0 = 0.f, acc1 = 0.f;
+    // two chunks per step (idx and idx + 32; the second masked past total)
+#pragma unroll 1
+    for (int idx0 = lane; idx0 < total; idx0 += 64) {
 #pragma unroll
-  for (int i = 0; i < XC; ++i) {
-    if (lane + 32 * i < nch) {
-      const float2 fg = affine_f(L.gs[i], L.gb[i]);
-      const float2 fu = affine_f(L.us[i], L.ub[i]);
-      ag = fmaf(fg.x, chunk_fdot(L.g[i], xc.v[i]), fmaf(fg.y, xc.sum[i], ag));
-      au = fmaf(fu.x, chunk_fdot(L.u[i], xc.v[i]), fmaf(fu.y, xc.sum[i], au));
+      for (int u = 0; u < 2; ++u) {
+        const int idx = idx0 + 32 * u;
+        if (u == 1 && idx >= total) break;
+        const int s = idx / fch, c = idx % fch;
+        const uint8_t* base = X + s * slot_bytes;
+        const uint16_t* sc = reinterpret_cast<const uint16_t*>(base + (size_t)p.capX * half_row);
+        const uint16_t* bi = sc + (size_t)p.capX * groups;
+        const uint4 q0 = reinterpret_cast<const uint4*>(base + j * half_row)[c];
+        const uint4 q1 = reinterpret_cast<const uint4*>(base + j1 * half_row)[c];
+        const float2 a0 = affine_f(sc[j * groups + (c >> 1)], bi[j * groups + (c >> 1)]);
+        const float2 a1 = affine_f(sc[j1 * groups + (c >> 1)], bi[j1 * groups + (c >> 1)]);
+        float lo0 = 0.f, hi0 = 0.f, lo1 = 0.f, hi1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint4 vp = hp[pair_slot(idx, w)];
+          word_fdot<false>(word_of(q0, w), vp, lo0, hi0);
+          word_fdot<false>(word_of(q1, w), vp, lo1, hi1);
+        }
+        const float ws = s_w[s], hs = hsum[idx];
+        acc0 = fmaf(ws, fmaf(a0.x, lo0 + hi0, a0.y * hs), acc0);
+        acc1 = fmaf(ws, fmaf(a1.x, lo1 + hi1, a1.y * hs), acc1);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      acc0 += __shfl_xor_sync(kFull, acc0, off);
+      acc1 += __shfl_xor_sync(kFull, acc1, off);
+    }
+    if (lane < 2 && (lane == 0 || j1 != j)) {
+      const __nv_bfloat16 o = __float2bfloat16_rn(lane == 0 ? acc0 : acc1);
+      p.out[j0 + (lane == 0 ? j : j1)] = *reinterpret_cast<const uint16_t*>(&o);
     }
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    ag += __shfl_xor_sync(kFull, ag, off);
-    au += __shfl_xor_sync(kFull, au, off);
-  }
-  return ag / (1.f + expf(-ag)) * au;
 }
 
-// Top-k of the E logits (+ router bias) by warp 0 of the block, read from
-// global memory (L2): ids, softmax-over-selected weights and the shared gate
-// go to shared memory. Descending, ties to the lower id.
-template <int NPL>
-MOE_DEVINL void block_topk(const DecodeParams& p, int* s_ids, float* s_w) {
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    float z[NPL];
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      const int e = i * 32 + lane;
-      z[i] = 0.f;
-      if (e < p.E) {
-        z[i] = __ldcg(p.logits + e);
-        if (p.w.router_bias) z[i] = z[i] + p.w.router_bias[e];
+// Bulk copies of row pairs [r0, r0 + n) of one expert's gate/up into Y slots
+// [i0, i0 + n).
+__device__ __noinline__ void issue_rowpairs(uint8_t* Y, int capY, int i0, const moe_w4_t& G,
+                                            const moe_w4_t& U, int64_t r0, int n, int d, uint64_t* bar) {
+  const uint32_t half_row = d / 2, sbytes = d / 32;  // codes and scale bytes per row
+  const uint32_t qb = n * half_row, sb = n * sbytes;
+  const int64_t qoff = r0 * half_row, soff = r0 * sbytes;
+  uint8_t* s0 = Y + (size_t)capY * d + (size_t)i0 * sbytes;
+  const size_t sstride = (size_t)capY * sbytes;
+  bulk_load(Y + (size_t)i0 * half_row, reinterpret_cast<const uint8_t*>(G.q) + qoff, qb, bar);
+  bulk_load(Y + ((size_t)capY + i0) * half_row, reinterpret_cast<const uint8_t*>(U.q) + qoff, qb, bar);
+  bulk_load(s0, reinterpret_cast<const uint8_t*>(G.scale) + soff, sb, bar);
+  bulk_load(s0 + sstride, reinterpret_cast<const uint8_t*>(G.bias) + soff, sb, bar);
+  bulk_load(s0 + 2 * sstride, reinterpret_cast<const uint8_t*>(U.scale) + soff, sb, bar);
+  bulk_load(s0 + 3 * sstride, reinterpret_cast<const uint8_t*>(U.bias) + soff, sb, bar);
+}
+
+// Bulk copies of down rows [j0, j0 + n) of expert e (matrix D) into slot s of X.
+__device__ __noinline__ void issue_down(uint8_t* X, int capX, int s, const moe_w4_t& D, int64_t e,
+                                        int j0, int n, int d, int f, uint64_t* bar) {
+  const uint32_t half_row = f / 2, sbytes = f / 32;
+  uint8_t* base = X + (size_t)s * capX * (half_row + 2 * sbytes);
+  const int64_t r0 = e * d + j0;
+  bulk_load(base, reinterpret_cast<const uint8_t*>(D.q) + r0 * half_row, n * half_row, bar);
+  bulk_load(base + (size_t)capX * half_row, reinterpret_cast<const uint8_t*>(D.scale) + r0 * sbytes,
+            n * sbytes, bar);
+  bulk_load(base + (size_t)capX * (half_row + sbytes),
+            reinterpret_cast<const uint8_t*>(D.bias) + r0 * sbytes, n * sbytes, bar);
+}
+
+// Routed row pairs [r0, r0 + n) of the flattened (slot, row) order into Y
+// slots [0, n), split where a slot (expert) ends.
+__device__ __noinline__ void issue_routed(const DecodeParams& p, uint8_t* Y, const int* ids, int r0,
+                                          int n, uint64_t* bar) {
+  for (int i = 0; i < n;) {
+    const int r = r0 + i, slot = r / p.f, row = r % p.f;
+    const int seg = min(n - i, p.f - row);
+    issue_rowpairs(Y, p.capY, i, p.w.gate, p.w.up, (int64_t)ids[slot] * p.f + row, seg, p.d, bar);
+    i += seg;
+  }
+}
+
+// Down rows [j0, j0 + n) of every slot (routed ones, then the shared one if
+// `with_shared`) into X.
+__device__ __noinline__ void issue_down_all(const DecodeParams& p, uint8_t* X, const int* ids, int j0,
+                                            int n, bool with_shared, uint64_t* bar) {
+  for (int s = 0; s < p.k; ++s) issue_down(X, p.capX, s, p.w.down, ids[s], j0, n, p.d, p.f, bar);
+  if (with_shared) issue_down(X, p.capX, p.k, p.w.sh_down, 0, j0, n, p.d, p.f, bar);
+}
+
+// The selected experts' first chunks, one bulk copy per lane (so a batch
+// goes out in a few warp instructions): routed gate/up rows [r0, r0 + n)
+// into Y (6 copies per segment of one expert: codes of gate and up, then
+// gate scale, gate bias, up scale, up bias), then down rows [j0, j0 + nj)
+// of each routed slot into X (codes, scale, bias). Called by a whole warp.
+__device__ __noinline__ void issue_selected(const DecodeParams& p, uint8_t* Y, uint8_t* X, const int* ids,
+                                            int r0, int n, int j0, int nj, uint64_t* barY, uint64_t* barX) {
+  const int lane = threadIdx.x & 31, d = p.d, f = p.f;
+  const uint32_t hq = d / 2, hs = d / 32;  // gate/up row: code bytes, scale bytes
+  const uint32_t dq = f / 2, ds = f / 32;  // down row
+  const int nseg = n > 0 ? (r0 + n - 1) / f - r0 / f + 1 : 0;
+  const int nq = 6 * nseg + (nj > 0 ? 3 * p.k : 0);
+  for (int q = lane; q < nq; q += 32) {
+    uint8_t* dst;
+    const uint8_t* src;
+    uint32_t bytes;
+    uint64_t* bar;
+    if (q < 6 * nseg) {
+      const int si = q / 6, kind = q % 6, slot = r0 / f + si;
+      const int lo = max(r0, slot * f), hi = min(r0 + n, (slot + 1) * f);
+      const int i0 = lo - r0, len = hi - lo;
+      const int64_t grow = (int64_t)ids[slot] * f + (lo - slot * f);
+      const moe_w4_t& W = (kind == 1 || kind >= 4) ? p.w.up : p.w.gate;
+      if (kind < 2) {
+        dst = Y + ((size_t)(kind ? p.capY : 0) + i0) * hq;
+        src = reinterpret_cast<const uint8_t*>(W.q) + grow * hq;
+        bytes = len * hq;
+      } else {
+        const int m = kind - 2;  // gate scale, gate bias, up scale, up bias
+        dst = Y + (size_t)p.capY * d + ((size_t)m * p.capY + i0) * hs;
+        src = reinterpret_cast<const uint8_t*>((m & 1) ? W.bias : W.scale) + grow * hs;
+        bytes = len * hs;
       }
+      bar = barY;
+    } else {
+      const int qq = q - 6 * nseg, s = qq / 3, kind = qq % 3;
+      const int64_t r = (int64_t)ids[s] * d + j0;
+      uint8_t* base = X + (size_t)s * p.capX * (dq + 2 * ds);
+      if (kind == 0) {
+        dst = base;
+        src = reinterpret_cast<const uint8_t*>(p.w.down.q) + r * dq;
+        bytes = nj * dq;
+      } else {
+        dst = base + (size_t)p.capX * dq + (size_t)(kind - 1) * p.capX * ds;
+        src = reinterpret_cast<const uint8_t*>(kind == 1 ? p.w.down.scale : p.w.down.bias) + r * ds;
+        bytes = nj * ds;
+      }
+      bar = barX;
     }
-    uint32_t taken = 0;
-    float my_z = 0.f;
-    int my_e = 0;
-    for (int j = 0; j < p.k; ++j) {
-      float bv = 0.f;
-      int be = INT_MAX;
-#pragma unroll
-      for (int i = 0; i < NPL; ++i) {
-        const int e = i * 32 + lane;
-        if (e < p.E && !((taken >> i) & 1u) && (be == INT_MAX || z[i] > bv)) {
-          bv = z[i];
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(kFull, bv, off);
-        const int oe = __shfl_xor_sync(kFull, be, off);
-        if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (lane == j) {
-        my_z = bv;
-        my_e = be;
-      }
-    }
-    const float zmax = __shfl_sync(kFull, my_z, 0);
-    const float ex = lane < p.k ? expf(my_z - zmax) : 0.f;
-    float sum = ex;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
-    if (lane < p.k) {
-      s_ids[lane] = my_e;
-      s_w[lane] = ex / sum;
-    }
-    if (lane == 0) s_w[p.k] = p.shared ? 1.f / (1.f + expf(-__ldcg(p.gate_logit))) : 0.f;
+    bulk_load(dst, src, bytes, bar);
+  }
+}
+
+// [lo, hi) of `units` work units for block b of G, scaled by `gran`.
+MOE_DEVINL int2 block_range(int units, int b, int G, int gran) {
+  const int lo = (int)((int64_t)units * b / G), hi = (int)((int64_t)units * (b + 1) / G);
+  return make_int2(lo * gran, hi * gran);
+}
+
+// ---------------------------------------------------------------- kernel
+__global__ void __launch_bounds__(kDecThreads, 2) decode_layer_kernel(const __grid_constant__ DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t dsmem[];
+  const DecSmem sm = carve_dec_smem(dsmem, p);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, b = blockIdx.x;
+  const int d = p.d, E = p.E, k = p.k, f = p.f;
+  const int S = k + (p.shared ? 1 : 0);
+  const int ncg = E / 8, n_items = ncg * p.KS, rs = (d + p.KS - 1) / p.KS;
+  const uint32_t rp_bytes = d + d / 8;          // one row pair in Y
+  const uint32_t dn_bytes = f / 2 + f / 16;     // one down row (codes, scale, bias) in X
+  const int2 rr = block_range(k * f / p.qrow, b, G, p.qrow);                       // routed row pairs
+  const int2 sr = p.shared ? block_range(f / p.qrow, b, G, p.qrow) : make_int2(0, 0);  // shared row pairs
+  const int2 orng = block_range(d / p.qout, b, G, p.qout);                          // outputs
+  const int nj0 = min(orng.y - orng.x, p.capX);
+
+  if (tid == 0) {
+    mbar_init(sm.barY, 1);
+    mbar_init(sm.barZ, 1);
+    mbar_init(sm.barX, 2);  // each X chunk: shared-slot arrival + routed-slot arrival
+    fence_mbar_init();
   }
   __syncthreads();
-}
 
-// ---------------------------------------------------------------- kernel 1
-// blocks [0, E/8): router logits 8b..8b+7 (thread t takes rows t + 256 j);
-// blocks [E/8, E/8 + f/8): shared expert gate/up, one row pair per warp.
-template <int XC>
-__global__ void __launch_bounds__(256) decode_router_shared_kernel(DecodeParams p) {
-  constexpr int kPre = 8;  // router rows per thread loaded before the wait
-  __shared__ float s_red[8][8];
-  const int E = p.E, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_router = E / 8;
-  const bool is_router = (int)blockIdx.x < n_router;
-  float4 wa[kPre], wb[kPre];
-  RowPairLoads<XC> L;
-  int64_t sh_row = -1;
-  if (is_router) {
-    const int e0 = blockIdx.x * 8;
+  // ---- before the dependency wait: weights only (nothing the previous kernel writes)
+  if (warp == 0) {
+    const int ns0 = min(sr.y - sr.x, p.capS), njs = p.shared ? nj0 : 0;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(sm.barZ, ns0 * rp_bytes);
+      mbar_arrive_expect_tx(sm.barX, njs * dn_bytes);
+    }
+    __syncwarp();
+    if (lane == 0 && ns0 > 0) issue_rowpairs(sm.Z, p.capS, 0, p.w.sh_gate, p.w.sh_up, sr.x, ns0, d, sm.barZ);
+    if (lane == 1 && njs > 0) issue_down(sm.X, p.capX, k, p.w.sh_down, 0, orng.x, njs, d, f, sm.barX);
+  }
+  uint32_t y_phase = 0, z_phase = 1;
+  // this block's first router item (8 experts x d/KS rows): kRouterPre rows per thread
+  float4 wa[kRouterPre], wb[kRouterPre];
+  float wg[kRouterPre];
+  {
+    const int cg = b % ncg, ks = b / ncg, row1 = min(d, (ks + 1) * rs);
 #pragma unroll
-    for (int j = 0; j < kPre; ++j) {
-      const int k = threadIdx.x + 256 * j;
-      if (k < p.d) {
-        const float4* w = reinterpret_cast<const float4*>(p.w.router + (size_t)k * E + e0);
+    for (int j = 0; j < kRouterPre; ++j) {
+      const int row = ks * rs + tid + kDecThreads * j;
+      wa[j] = wb[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      wg[j] = 0.f;
+      if (b < n_items && row < row1) {
+        const float4* w = reinterpret_cast<const float4*>(p.w.router + (size_t)row * E + cg * 8);
         wa[j] = __ldcs(w);
         wb[j] = __ldcs(w + 1);
+        if (cg == 0 && p.shared) wg[j] = __ldcs(p.w.shared_gate + row);
       }
     }
-  } else {
-    sh_row = (int64_t)(blockIdx.x - n_router) * 8 + warp;
-    if (sh_row < p.f) load_rowpair<XC>(p.w.sh_gate, p.w.sh_up, sh_row, p.d, L);
   }
-  pdl_wait();
-  if (blockIdx.x == 0 && threadIdx.x < 4) p.status[threadIdx.x] = 0;
+
+  // One thread waits for the previous kernel (its completion and memory are
+  // then visible to the whole grid); the others wait at the block barrier.
+  if (tid == 0) pdl_wait();
+  __syncthreads();
   pdl_launch_dependents();
-  if (is_router) {
-    const int e0 = blockIdx.x * 8;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+
+  // ---- x (one round trip): paired words and chunk sums; this call's epoch
+  if (b == 0 && tid < 4) p.status[tid] = 0;
+  if (tid == 0) {
+    const uint32_t e = *reinterpret_cast<volatile uint32_t*>(p.sync) + 1;
+    *sm.s_epoch = e == 0 ? 1 : e;
+  }
+  for (int i = tid; i < d / 8; i += kDecThreads) {  // word j = i % 4 of chunk c = i / 4
+    const uint4 v = reinterpret_cast<const uint4*>(p.x)[i];
+    sm.xp[pair_slot(i >> 2, i & 3)] = pair_up(v);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    float s = 0.f;
 #pragma unroll
-    for (int j = 0; j < kPre; ++j) {
-      const int k = threadIdx.x + 256 * j;
-      if (k < p.d) {
-        const float xv = bf16_bits_to_f32(p.x[k]);
+    for (int t = 0; t < 4; ++t) s += __uint_as_float(u[t] << 16) + __uint_as_float(u[t] & 0xFFFF0000u);
+    // the 4 words of a chunk are 4 adjacent lanes, active together (d / 8 is a
+    // multiple of 16)
+    s += __shfl_xor_sync(__activemask(), s, 1);
+    s += __shfl_xor_sync(__activemask(), s, 2);
+    if ((i & 3) == 0) sm.xsum[i >> 2] = s;
+  }
+  __syncthreads();
+  const uint32_t epoch = *sm.s_epoch;
+  const uint16_t* xh = reinterpret_cast<const uint16_t*>(sm.xp);
+
+  // ---- phase A: router partials (and the shared gate-logit partial)
+#pragma unroll 1
+  for (int it = b; it < n_items; it += G) {
+    const int cg = it % ncg, ks = it / ncg, row1 = min(d, (ks + 1) * rs);
+    float acc[9] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int row = ks * rs + tid;
+    if (it == b) {  // the rows loaded before the wait
+#pragma unroll
+      for (int j = 0; j < kRouterPre; ++j, row += kDecThreads) {
+        if (row >= row1) continue;
+        const float xv = bf16_bits_to_f32(xh[pair_elem(row)]);
         acc[0] = fmaf(xv, wa[j].x, acc[0]); acc[1] = fmaf(xv, wa[j].y, acc[1]);
         acc[2] = fmaf(xv, wa[j].z, acc[2]); acc[3] = fmaf(xv, wa[j].w, acc[3]);
         acc[4] = fmaf(xv, wb[j].x, acc[4]); acc[5] = fmaf(xv, wb[j].y, acc[5]);
         acc[6] = fmaf(xv, wb[j].z, acc[6]); acc[7] = fmaf(xv, wb[j].w, acc[7]);
+        acc[8] = fmaf(xv, wg[j], acc[8]);
       }
     }
-    for (int k = threadIdx.x + 256 * kPre; k < p.d; k += 256) {
-      const float xv = bf16_bits_to_f32(p.x[k]);
-      const float4* w = reinterpret_cast<const float4*>(p.w.router + (size_t)k * E + e0);
-      const float4 a = __ldcs(w), b = __ldcs(w + 1);
+#pragma unroll 1
+    for (; row < row1; row += kDecThreads) {
+      const float4* w = reinterpret_cast<const float4*>(p.w.router + (size_t)row * E + cg * 8);
+      const float4 a = __ldcs(w), c = __ldcs(w + 1);
+      const float g = (cg == 0 && p.shared) ? __ldcs(p.w.shared_gate + row) : 0.f;
+      const float xv = bf16_bits_to_f32(xh[pair_elem(row)]);
       acc[0] = fmaf(xv, a.x, acc[0]); acc[1] = fmaf(xv, a.y, acc[1]);
       acc[2] = fmaf(xv, a.z, acc[2]); acc[3] = fmaf(xv, a.w, acc[3]);
-      acc[4] = fmaf(xv, b.x, acc[4]); acc[5] = fmaf(xv, b.y, acc[5]);
-      acc[6] = fmaf(xv, b.z, acc[6]); acc[7] = fmaf(xv, b.w, acc[7]);
+      acc[4] = fmaf(xv, c.x, acc[4]); acc[5] = fmaf(xv, c.y, acc[5]);
+      acc[6] = fmaf(xv, c.z, acc[6]); acc[7] = fmaf(xv, c.w, acc[7]);
+      acc[8] = fmaf(xv, g, acc[8]);
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 9; ++i)
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) acc[i] += __shfl_xor_sync(kFull, acc[i], off);
     if (lane == 0)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) s_red[warp][i] = acc[i];
+      for (int i = 0; i < 9; ++i) sm.red[warp * 9 + i] = acc[i];
     __syncthreads();
-    if (threadIdx.x < 8) {
+    if (tid < 9) {
       float v = 0.f;
-      for (int w = 0; w < 8; ++w) v += s_red[w][threadIdx.x];
-      p.logits[e0 + threadIdx.x] = v;
+      for (int w = 0; w < kDecWarps; ++w) v += sm.red[w * 9 + tid];
+      if (tid < 8) publish(p.pub + (size_t)ks * E + cg * 8 + tid, v, epoch);
+      else if (cg == 0) publish(p.pub + (size_t)kDecodeMaxSplits * E + ks, v, epoch);
+    }
+    __syncthreads();
+  }
+
+  // ---- phase B: logits (polled from the published partials), top k
+#pragma unroll 1
+  for (int e = tid; e < E; e += kDecThreads) {
+    unsigned long long w[kDecodeMaxSplits];
+    bool ready = false;
+    Poll poll;
+    do {
+      ready = true;
+#pragma unroll
+      for (int s = 0; s < kDecodeMaxSplits; ++s)
+        if (s < p.KS) {
+          w[s] = ld_word(p.pub + (size_t)s * E + e);
+          ready = ready && word_ready(w[s], epoch);
+        }
+    } while (!ready && poll.again(p.status, 41));
+    float z = 0.f;
+#pragma unroll
+    for (int s = 0; s < kDecodeMaxSplits; ++s)
+      if (s < p.KS) z += word_value(w[s]);
+    if (b == 0) p.logits[e] = z;
+    sm.keys[e] = p.w.router_bias ? z + p.w.router_bias[e] : z;
+  }
+  if (tid >= kDecThreads - 32 && tid - (kDecThreads - 32) < p.KS) {  // gate-logit partials
+    const int s = tid - (kDecThreads - 32);
+    unsigned long long w;
+    Poll poll;
+    do w = ld_word(p.pub + (size_t)kDecodeMaxSplits * E + s);
+    while (!word_ready(w, epoch) && poll.again(p.status, 42));
+    sm.s_gp[s] = word_value(w);
+  }
+  __syncthreads();
+  // top k in two levels: each warp keeps the best kc of its E/8 keys (rank by
+  // counting), then the 8 * kc candidates are ranked among themselves. An
+  // expert in the overall top k is in its warp's top kc, and everything that
+  // outranks it is too, so its rank among the candidates is its overall rank.
+  // (Rank counts are branch-free so the compares and loads pipeline.)
+  const int EW = E / 8, kc = min(k, EW), n_cand = kDecWarps * kc;
+  if (EW <= 32) {  // one key per lane: the warp's keys come by register shuffles
+    const int base = warp * EW;
+    const float ke = lane < EW ? sm.keys[base + lane] : 0.f;
+    int rank = 0;
+#pragma unroll
+    for (int o = 1; o < 32; ++o) {
+      const int src = (lane + o) & 31;
+      const float kj = __shfl_sync(kFull, ke, src);
+      rank += (int)(src < EW) & ((int)(kj > ke) | ((int)(kj == ke) & (int)(src < lane)));
+    }
+    if (lane < EW && rank < kc) {
+      sm.cand_key[warp * kc + rank] = ke;
+      sm.cand_id[warp * kc + rank] = base + lane;
     }
   } else {
-    if (sh_row < p.f) {
-      XChunks<XC> xc;
-      load_x_chunks<XC>(p.x, p.d / 32, xc);
-      const float h = rowpair_h<XC>(L, xc, p.d);
-      if (lane == 0) p.h[(size_t)p.k * p.f + sh_row] = h;
-    }
-    if (blockIdx.x == (unsigned)n_router && threadIdx.x < 32) {  // shared gate logit x . w_sg
-      float a = 0.f;
-      for (int k = lane; k < p.d; k += 32) a = fmaf(bf16_bits_to_f32(p.x[k]), p.w.shared_gate[k], a);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(kFull, a, off);
-      if (lane == 0) p.gate_logit[0] = a;
-    }
-  }
-}
-
-// ---------------------------------------------------------------- kernel 2
-// Routed gate/up rows: row pair rp = slot * f + row, two per warp at a time.
-template <int NPL, int XC>
-__global__ void __launch_bounds__(256, XC <= 2 ? 2 : 1) decode_gateup_kernel(DecodeParams p) {
-  __shared__ int s_ids[32];
-  __shared__ float s_w[33];
-  XChunks<XC> xc;
-  load_x_chunks<XC>(p.x, p.d / 32, xc);  // x does not depend on the router
-  pdl_wait();
-  pdl_launch_dependents();
-  block_topk<NPL>(p, s_ids, s_w);
-  if (blockIdx.x == 0 && threadIdx.x <= p.k) {
-    if (threadIdx.x < p.k) p.ids[threadIdx.x] = s_ids[threadIdx.x];
-    p.wts[threadIdx.x] = s_w[threadIdx.x];
-  }
-  const int lane = threadIdx.x & 31;
-  const int nwarps = gridDim.x * 8;
-  const int total = p.k * p.f;
-  for (int rp0 = blockIdx.x * 8 + (threadIdx.x >> 5); rp0 < total; rp0 += 2 * nwarps) {
-    const int rp1 = rp0 + nwarps;
-    RowPairLoads<XC> L0, L1;
-    int e0 = s_ids[rp0 / p.f], e1 = 0;
-    const bool ok0 = e0 >= 0 && e0 < p.E;
-    if (ok0) load_rowpair<XC>(p.w.gate, p.w.up, (int64_t)e0 * p.f + rp0 % p.f, p.d, L0);
-    bool ok1 = false;
-    if (rp1 < total) {
-      e1 = s_ids[rp1 / p.f];
-      ok1 = e1 >= 0 && e1 < p.E;
-      if (ok1) load_rowpair<XC>(p.w.gate, p.w.up, (int64_t)e1 * p.f + rp1 % p.f, p.d, L1);
-    }
-    if (!ok0 || (rp1 < total && !ok1)) report(p.status, MOE_DEV_BAD_EXPERT, 21, ok0 ? e1 : e0);
-    if (ok0) {
-      const float h = rowpair_h<XC>(L0, xc, p.d);
-      if (lane == 0) p.h[rp0] = h;
-    }
-    if (ok1) {
-      const float h = rowpair_h<XC>(L1, xc, p.d);
-      if (lane == 0) p.h[rp1] = h;
-    }
-  }
-}
-
-// ---------------------------------------------------------------- kernel 3
-// One warp per output column j: chunk idx = slot * (f/32) + c of the down rows
-// (slot < k: routed expert ids[slot], slot k: shared), weighted by wts[slot].
-template <int NPL, int NI>
-__global__ void __launch_bounds__(256) decode_down_kernel(DecodeParams p) {
-  extern __shared__ float4 smem4[];
-  __shared__ int s_ids[32];
-  __shared__ float s_w[33];
-  const int nslots = p.k + (p.shared ? 1 : 0);
-  const int fch = p.f / 32;
-  const int total = nslots * fch;
-  const int lane = threadIdx.x & 31;
-  const int j = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int64_t qrow = p.f / 8, grow = p.f / 64;
-  // 1. the selection (from kernel 1's logits: kernel 1 has completed, since
-  //    every block of kernel 2 waited for it before letting this grid start)
-  //    and this warp's down-row chunks
-  block_topk<NPL>(p, s_ids, s_w);
-  uint4 w[NI];
-  uint16_t sc[NI], bi[NI];
-  float coef[NI];
-#pragma unroll
-  for (int i = 0; i < NI; ++i) {
-    const int idx = lane + 32 * i;
-    coef[i] = 0.f;
-    if (idx < total && j < p.d) {
-      const int slot = idx / fch, c = idx % fch;
-      int64_t e = 0;
-      const moe_w4_t* D = &p.w.sh_down;
-      if (slot < p.k) {
-        e = s_ids[slot];
-        D = &p.w.down;
+#pragma unroll 1
+    for (int m = lane; m < EW; m += 32) {
+      const int base = warp * EW;
+      const float ke = sm.keys[base + m];
+      int rank = 0;
+#pragma unroll 8
+      for (int j = 0; j < EW; ++j) {
+        const float kj = sm.keys[base + j];
+        rank += (int)(kj > ke) | ((int)(kj == ke) & (int)(j < m));
       }
-      if (e >= 0 && e < p.E) {
-        const int64_t r = e * p.d + j;
-        w[i] = __ldcs(reinterpret_cast<const uint4*>(D->q + r * qrow) + c);
-        sc[i] = __ldcs(D->scale + r * grow + (c >> 1));
-        bi[i] = __ldcs(D->bias + r * grow + (c >> 1));
-        coef[i] = 1.f;
-      } else {
-        report(p.status, MOE_DEV_BAD_EXPERT, 22, (int)e);
+      if (rank < kc) {
+        sm.cand_key[warp * kc + rank] = ke;
+        sm.cand_id[warp * kc + rank] = base + m;
       }
     }
   }
-  pdl_wait();
-  pdl_launch_dependents();
-  // 2. h of every slot, staged as swizzled fp32 chunks, with chunk sums
-  float4* hv = smem4;
-  float* hsum = reinterpret_cast<float*>(smem4 + total * 8);
-  for (int i = threadIdx.x; i < total * 8; i += blockDim.x)
-    hv[chunk_slot(i >> 3, i & 7)] = __ldcg(reinterpret_cast<const float4*>(p.h) + i);
   __syncthreads();
-  for (int c = threadIdx.x; c < total; c += blockDim.x) {
+#pragma unroll 1
+  for (int t = tid; t < n_cand; t += kDecThreads) {
+    const float kt = sm.cand_key[t];
+    const int et = sm.cand_id[t];
+    int rank = 0;
+#pragma unroll 8
+    for (int j = 0; j < n_cand; ++j) {
+      const float kj = sm.cand_key[j];
+      rank += (int)(kj > kt) | ((int)(kj == kt) & (int)(sm.cand_id[j] < et));
+    }
+    if (rank < k) {
+      sm.s_ids[rank] = et;
+      sm.s_z[rank] = kt;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {  // the selected experts' rows, as early as possible
+    const int nr0 = min(rr.y - rr.x, p.capY);
+    if (lane == 0) {
+      mbar_arrive_expect_tx(sm.barY, nr0 * rp_bytes);
+      mbar_arrive_expect_tx(sm.barX, k * nj0 * dn_bytes);
+    }
+    __syncwarp();
+    issue_selected(p, sm.Y, sm.X, sm.s_ids, rr.x, nr0, orng.x, nj0, sm.barY, sm.barX);
+  }
+  ++y_phase;
+  if (warp == 0) {  // softmax over the selected biased logits; the shared gate
+    const float zmax = sm.s_z[0];
+    const float ex = lane < k ? expf(sm.s_z[lane] - zmax) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+    const float wt = ex * __frcp_rn(sum);
+    if (lane < k) sm.s_w[lane] = wt;
+    float gl = 0.f;
+    for (int s = 0; s < p.KS; ++s) gl += sm.s_gp[s];
+    const float gate = p.shared ? __frcp_rn(1.f + expf(-gl)) : 0.f;
+    if (lane == 0) sm.s_w[k] = gate;
+    if (b == 0) {
+      if (lane < k) {
+        p.ids[lane] = sm.s_ids[lane];
+        p.wts[lane] = wt;
+      }
+      if (lane == 0) {
+        p.gate_logit[0] = gl;
+        p.wts[k] = gate;
+      }
+    }
+  }
+
+  // ---- h of the shared expert's rows: off the critical path here, while
+  // the routed rows are in flight (their copies went out above)
+#pragma unroll 1
+  for (int c0 = sr.x; c0 < sr.y; c0 += p.capS) {
+    const int n = min(p.capS, sr.y - c0);
+    if (c0 != sr.x) {
+      __syncthreads();  // the previous chunk's rows are consumed
+      if (tid == 0) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(sm.barZ, n * rp_bytes);
+        issue_rowpairs(sm.Z, p.capS, 0, p.w.sh_gate, p.w.sh_up, c0, n, d, sm.barZ);
+      }
+      ++z_phase;
+    }
+    bar_wait(sm.barZ, (z_phase - 1) & 1, p.status, 40);
+    rows_h(p, sm.Z, p.capS, sm.xp, sm.xsum, n, k * f + c0, epoch);
+  }
+
+  // ---- phase B: h of the routed row pairs
+#pragma unroll 1
+  for (int c0 = rr.x; c0 < rr.y; c0 += p.capY) {
+    const int n = min(p.capY, rr.y - c0);
+    if (c0 != rr.x) {
+      __syncthreads();
+      if (tid == 0) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(sm.barY, n * rp_bytes);
+        issue_routed(p, sm.Y, sm.s_ids, c0, n, sm.barY);
+      }
+      ++y_phase;
+    }
+    bar_wait(sm.barY, (y_phase - 1) & 1, p.status, 43);
+    rows_h(p, sm.Y, p.capY, sm.xp, sm.xsum, n, c0, epoch);  // flattened (slot, row) = slot * f + row
+  }
+  __syncthreads();  // Y is consumed: it holds h from here on
+
+  // ---- phase C: h of every slot (polled; as f16 pairs), then the block's outputs
+  const int total = S * (f / 32);
+  uint4* hp = reinterpret_cast<uint4*>(sm.Y);
+  float* hsum = reinterpret_cast<float*>(hp + (size_t)total * 4);
+  uint16_t* hph = reinterpret_cast<uint16_t*>(hp);
+  constexpr int kHB = 12;  // 16-byte words per thread per polling batch (one batch: (k+1) f <= 6144)
+  const int n_pairs = total * 16;
+#pragma unroll 1
+  for (int base = 0; base < n_pairs; base += kHB * kDecThreads) {
+    unsigned long long w0[kHB], w1[kHB];
+    uint32_t pending = 0;
+#pragma unroll
+    for (int m = 0; m < kHB; ++m)
+      if (base + m * kDecThreads + tid < n_pairs) pending |= 1u << m;
+    Poll poll;
+    do {
+#pragma unroll
+      for (int m = 0; m < kHB; ++m)
+        if (pending & (1u << m)) ld_word2(p.pub_h + 2 * (base + m * kDecThreads + tid), w0[m], w1[m]);
+#pragma unroll
+      for (int m = 0; m < kHB; ++m)
+        if ((pending & (1u << m)) && word_ready(w0[m], epoch) && word_ready(w1[m], epoch)) {
+          const int i = 2 * (base + m * kDecThreads + tid);
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const float v = word_value(t == 0 ? w0[m] : w1[m]);
+            const __half hv = __float2half_rn(fminf(fmaxf(v, -65504.f), 65504.f));
+            hph[pair_elem(i + t)] = *reinterpret_cast<const uint16_t*>(&hv);
+          }
+          pending &= ~(1u << m);
+        }
+    } while (pending && poll.again(p.status, 44));
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int c = tid; c < total; c += kDecThreads) {  // chunk sums of the f16 values used
     float s = 0.f;
-    for (int t = 0; t < 8; ++t) {
-      const float4 f = hv[chunk_slot(c, t)];
-      s += (f.x + f.y) + (f.z + f.w);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 v = hp[pair_slot(c, j)];
+      const float2 h0 = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+      const float2 h1 = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+      const float2 h2 = __half22float2(*reinterpret_cast<const __half2*>(&v.z));
+      const float2 h3 = __half22float2(*reinterpret_cast<const __half2*>(&v.w));
+      s += ((h0.x + h0.y) + (h1.x + h1.y)) + ((h2.x + h2.y) + (h3.x + h3.y));
     }
     hsum[c] = s;
   }
   __syncthreads();
-  if (j >= p.d) return;
-  float acc = 0.f;
-#pragma unroll
-  for (int i = 0; i < NI; ++i) {
-    const int idx = lane + 32 * i;
-    if (idx < total && coef[i] != 0.f) {
-      const float2 a = affine_f(sc[i], bi[i]);
-      const float part = fmaf(a.x, chunk_fdot_smem(w[i], hv, idx), a.y * hsum[idx]);
-      acc = fmaf(s_w[idx / fch], part, acc);
+  uint32_t x_phase = 0;
+#pragma unroll 1
+  for (int j0 = orng.x; j0 < orng.y; j0 += p.capX) {
+    const int nj = min(p.capX, orng.y - j0);
+    if (j0 != orng.x) {
+      __syncthreads();
+      if (tid == 0) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(sm.barX, S * nj * dn_bytes);
+        issue_down_all(p, sm.X, sm.s_ids, j0, nj, p.shared, sm.barX);
+        mbar_arrive(sm.barX);
+      }
     }
+    bar_wait(sm.barX, x_phase & 1, p.status, 45);
+    ++x_phase;
+    down_cols(p, sm.X, hp, hsum, sm.s_w, total, j0, nj);
   }
-  // chunks beyond NI * 32 (large k * d_ff): loaded after the wait
-  for (int idx = lane + 32 * NI; idx < total; idx += 32) {
-    const int slot = idx / fch, c = idx % fch;
-    int64_t e = 0;
-    const moe_w4_t* D = &p.w.sh_down;
-    if (slot < p.k) {
-      e = s_ids[slot];
-      D = &p.w.down;
-    }
-    if (e < 0 || e >= p.E) continue;
-    const int64_t r = e * p.d + j;
-    const uint4 wq = __ldcs(reinterpret_cast<const uint4*>(D->q + r * qrow) + c);
-    const float2 a = affine_f(__ldcs(D->scale + r * grow + (c >> 1)), __ldcs(D->bias + r * grow + (c >> 1)));
-    const float part = fmaf(a.x, chunk_fdot_smem(wq, hv, idx), a.y * hsum[idx]);
-    acc = fmaf(s_w[slot], part, acc);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
-  if (lane == 0) {
-    const __nv_bfloat16 o = __float2bfloat16_rn(acc);
-    p.out[j] = *reinterpret_cast<const uint16_t*>(&o);
-  }
+
+  // ---- block 0 records this call's epoch for the next call (every block
+  // read the old value before it published the h block 0 has waited for)
+  if (b == 0 && tid == 0) *reinterpret_cast<volatile uint32_t*>(p.sync) = epoch;
 }
 
 // ---------------------------------------------------------------- launch
+// Two blocks per SM (this layer's and the next layer's, which prefetches):
+// 228 KB of shared memory per SM, less 1 KB reserved per block, halved.
+constexpr size_t kDecSmemLimit = (228 * 1024 - 2 * 1024) / 2;
+
+int gcd_int(int a, int b) { return b == 0 ? a : gcd_int(b, a % b); }
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+size_t round_up(size_t v, size_t m) { return (v + m - 1) / m * m; }
+
+int sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+uint32_t u_bytes(const DecodeParams& p) {  // x pairs, x chunk sums, keys and candidates
+  const int kc = std::min(p.k, p.E / 8);
+  return (uint32_t)round_up((size_t)p.d * 2 + (size_t)((p.d / 32 + 3) & ~3) * 4 + (size_t)(p.E + 16 * kc) * 4, 16);
+}
+
+size_t scratch_bytes(const DecodeParams& p) {
+  return u_bytes(p) + (size_t)(32 + 32 + 40 + 72 + kDecodeMaxSplits + 2) * 4 + 8 + 24;
+}
+
+void size_buffers(DecodeParams& p) {
+  const int S = p.k + (p.shared ? 1 : 0);
+  const size_t rp = (size_t)p.d + p.d / 8, dn = (size_t)p.f / 2 + p.f / 16;
+  const size_t h_bytes = (size_t)S * p.f * 2 + (size_t)S * (p.f / 32) * 4;  // f16 h, chunk sums
+  p.y_bytes = (uint32_t)round_up(std::max((size_t)p.capY * rp, h_bytes), 128);
+  p.x_bytes = (uint32_t)round_up((size_t)p.capX * S * dn, 128);
+  p.z_bytes = (uint32_t)round_up((size_t)p.capS * rp, 128);
+  p.u_bytes = u_bytes(p);
+}
+
 template <class K, class... Args>
 cudaError_t launch_pdl(K kernel, dim3 grid, size_t smem, cudaStream_t s, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(kDecThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -471,50 +906,71 @@ cudaError_t launch_pdl(K kernel, dim3 grid, size_t smem, cudaStream_t s, Args...
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-template <int NPL, int XC>
-cudaError_t launch_xc(const DecodeParams& p, cudaStream_t s) {
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int n1 = p.E / 8 + (p.shared ? (p.f + 7) / 8 : 0);
-  cudaError_t err = launch_pdl(decode_router_shared_kernel<XC>, dim3(n1), 0, s, p);
-  if (err != cudaSuccess) return err;
-  const int rowpairs = p.k * p.f;
-  const int n2 = std::max(1, std::min((rowpairs + 15) / 16, 2 * sms));
-  err = launch_pdl(decode_gateup_kernel<NPL, XC>, dim3(n2), 0, s, p);
-  if (err != cudaSuccess) return err;
-  const int nslots = p.k + (p.shared ? 1 : 0);
-  const int total = nslots * (p.f / 32);
-  const size_t smem = (size_t)total * 8 * 16 + (size_t)total * 4;
-  const dim3 g3((p.d + 7) / 8);
-  auto k3 = total <= 32 * 2 ? decode_down_kernel<NPL, 2>
-            : total <= 32 * 4 ? decode_down_kernel<NPL, 4>
-            : total <= 32 * 6 ? decode_down_kernel<NPL, 6> : decode_down_kernel<NPL, 8>;
-  if (smem > 48 * 1024) {
-    err = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
+cudaError_t launch_decode(const DecodeParams& p, int G, size_t smem, cudaStream_t s) {
+  static std::mutex mu;
+  static bool attr_set = false;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr_set) {
+      const cudaError_t err = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)kDecSmemLimit);
+      if (err != cudaSuccess) return err;
+      attr_set = true;
+    }
   }
-  return launch_pdl(k3, g3, smem, s, p);
-}
-
-template <int NPL>
-cudaError_t launch_npl(const DecodeParams& p, cudaStream_t s) {
-  switch (p.d / 1024) {
-    case 0:
-    case 1: return launch_xc<NPL, 1>(p, s);
-    case 2: return launch_xc<NPL, 2>(p, s);
-    case 3: return launch_xc<NPL, 3>(p, s);
-    default: return launch_xc<NPL, 4>(p, s);
-  }
+  return launch_pdl(decode_layer_kernel, dim3(G), smem, s, p);
 }
 
 }  // namespace
 
-cudaError_t decode_launch(const DecodeParams& p, cudaStream_t s) {
-  const int npl = (p.E + 31) / 32;
-  if (npl <= 2) return launch_npl<2>(p, s);
-  if (npl <= 8) return launch_npl<8>(p, s);
-  return launch_npl<32>(p, s);
+size_t decode_pub_words(int E) { return (size_t)kDecodeMaxSplits * E + kDecodeMaxSplits; }
+
+bool decode_shape_supported(int d, int E, int k, int f, bool shared) {
+  if (d > 4096 || E % 8) return false;
+  DecodeParams p = {};
+  p.d = d;
+  p.E = E;
+  p.k = k;
+  p.f = f;
+  p.shared = shared;
+  p.capY = 16 / gcd_int(16, d / 32);  // smallest chunks the kernel can loop over
+  p.capX = 16 / gcd_int(16, f / 32);
+  p.capS = shared ? p.capY : 0;
+  size_buffers(p);
+  return (size_t)p.y_bytes + p.x_bytes + p.z_bytes + scratch_bytes(p) <= kDecSmemLimit;
+}
+
+cudaError_t decode_launch(const DecodeParams& p0, cudaStream_t s) {
+  DecodeParams p = p0;
+  // Bulk copies move whole 16-byte units: row ranges start and end on
+  // multiples of qrow (gate/up, d/32 scale bytes per row) and qout (down).
+  p.qrow = 16 / gcd_int(16, p.d / 32);
+  p.qout = 16 / gcd_int(16, p.f / 32);
+  // One block per SM, but no more blocks than routed row-pair units: every
+  // block then publishes some h, which block 0 waits for before it moves the
+  // epoch on (so no block can read the epoch after it changed).
+  const int G = std::min(sm_count(), p.k * p.f / p.qrow);
+  if (G <= 0) return cudaErrorInvalidDevice;
+  const int ncg = p.E / 8;
+  p.KS = std::max(1, std::min(kDecodeMaxSplits, G / ncg));
+  p.capY = ceil_div(p.k * p.f / p.qrow, G) * p.qrow;
+  p.capX = ceil_div(p.d / p.qout, G) * p.qout;
+  p.capS = p.shared ? ceil_div(p.f / p.qrow, G) * p.qrow : 0;
+  size_buffers(p);
+  // too large for two blocks per SM: smaller chunks (the kernel loops over them)
+  while ((size_t)p.y_bytes + p.x_bytes + p.z_bytes + scratch_bytes(p) > kDecSmemLimit &&
+         (p.capY > p.qrow || p.capX > p.qout || p.capS > p.qrow)) {
+    if (p.capS > p.qrow && p.capS >= p.capY)
+      p.capS = std::max(p.qrow, (p.capS / 2) / p.qrow * p.qrow);
+    else if (p.capY > p.qrow && (p.y_bytes >= p.x_bytes || p.capX <= p.qout))
+      p.capY = std::max(p.qrow, (p.capY / 2) / p.qrow * p.qrow);
+    else
+      p.capX = std::max(p.qout, (p.capX / 2) / p.qout * p.qout);
+    size_buffers(p);
+  }
+  const size_t smem = (size_t)p.y_bytes + p.x_bytes + p.z_bytes + scratch_bytes(p);
+  if (smem > kDecSmemLimit) return cudaErrorInvalidValue;
+  return launch_decode(p, G, smem, s);
 }
 
 }  // namespace moe

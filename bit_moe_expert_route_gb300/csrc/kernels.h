@@ -97,7 +97,19 @@ struct DecodeParams {
   float* wts;               // [k]
   float* h;                 // [k+1][f]
   int32_t* status;
+  // published {value, epoch} words: [kDecodeMaxSplits][E] router partials,
+  // then [kDecodeMaxSplits] gate-logit partials; and h [k+1][f]
+  unsigned long long* pub;
+  unsigned long long* pub_h;
+  uint32_t* sync;           // [0]: epoch of the last call (zero before the first call)
+  // set by decode_launch
+  int KS, qrow, qout, capY, capX, capS;
+  uint32_t y_bytes, x_bytes, z_bytes, u_bytes;
 };
+constexpr int kDecodeMaxSplits = 8;  // router K splits
+size_t decode_pub_words(int E);
+// Sizes the decode kernel can run: d <= 4096 and h of every slot fits in shared memory.
+bool decode_shape_supported(int d, int E, int k, int f, bool shared);
 cudaError_t decode_launch(const DecodeParams& p, cudaStream_t s);
 
 }  // namespace moe

@@ -113,6 +113,9 @@ FwdWs forward_ws(void* ws, const moe_shape_t* s, int bn) {
 
 struct DecWs {
   moe_decode_views_t v;
+  uint32_t* sync;                // the decode kernel's call epoch (zero before the first call)
+  unsigned long long* pub;       // published router and gate-logit partial sums
+  unsigned long long* pub_h;     // published h
   size_t bytes;
 };
 
@@ -122,11 +125,14 @@ DecWs decode_ws(void* ws, const moe_shape_t* s) {
   DecWs r;
   memset(&r.v, 0, sizeof r.v);
   r.v.status = c.take<int32_t>(kStatusWords);
+  r.sync = c.take<uint32_t>(4);
   r.v.logits = c.take<float>(E);
   r.v.gate_logit = c.take<float>(1);
   r.v.topk_ids = c.take<int32_t>(k);
   r.v.topk_w = c.take<float>(k + 1);
   r.v.h = c.take<float>((size_t)(k + 1) * s->d_ff);
+  r.pub = c.take<unsigned long long>(moe::decode_pub_words(E));
+  r.pub_h = c.take<unsigned long long>((size_t)(k + 1) * s->d_ff);
   r.bytes = c.off;
   return r;
 }
@@ -450,6 +456,9 @@ int moe_decode_views(void* ws, size_t ws_bytes, const moe_shape_t* shape,
 int moe_decode_gemv_w4(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* shape,
                        uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
   if (!shape_ok(shape, true) || shape->T != 1) return MOE_ERR_SHAPE;
+  if (!moe::decode_shape_supported(shape->d_model, shape->n_experts, shape->top_k, shape->d_ff,
+                                   w && w->shared_gate))
+    return MOE_ERR_SHAPE;
   int rc = check_weights(w, shape);
   if (rc != MOE_OK) return rc;
   if (!x || !out) return MOE_ERR_NULL;
@@ -458,8 +467,9 @@ int moe_decode_gemv_w4(const uint16_t* x, const moe_weights_t* w, const moe_shap
   if (!ws || !aligned(ws, kAlign) || ws_bytes < dw.bytes) return MOE_ERR_WORKSPACE;
   if ((rc = check_device()) != MOE_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the first decode kernel clears the status word itself (after its
-  // dependency wait), so consecutive calls stay one chain of PDL launches
+  // the decode kernel clears the status word itself (after its dependency
+  // wait) and keeps its epoch in the workspace, so consecutive calls stay one
+  // chain of PDL launches with no memset between them
   moe::DecodeParams p;
   memset(&p, 0, sizeof p);
   p.x = x;
@@ -476,6 +486,9 @@ int moe_decode_gemv_w4(const uint16_t* x, const moe_weights_t* w, const moe_shap
   p.wts = dw.v.topk_w;
   p.h = dw.v.h;
   p.status = dw.v.status;
+  p.pub = dw.pub;
+  p.pub_h = dw.pub_h;
+  p.sync = dw.sync;
   return cuda_status(moe::decode_launch(p, s));
 }
 

@@ -117,7 +117,8 @@ def _stream(stream=None):
 
 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:
-    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    """Zero-filled device workspace (the decode call requires a zeroed one)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
 def device_status(ws: torch.Tensor, stream=None) -> int:

@@ -235,11 +235,20 @@ int moe_forward_views(void* ws, size_t ws_bytes, const moe_shape_t* shape, int b
 
 /*
  * moe_decode_gemv_w4: one token (shape->T == 1) through the layer with
- * matrix-vector kernels that read only the router, the shared expert and the
+ * matrix-vector work that reads only the router, the shared expert and the
  * top_k selected experts' packed weights ("Why prefill and decode get
- * different treatment").
- *   x bf16 [d_model] device; out bf16 [d_model] device.
- *   ws 256-byte aligned, >= moe_decode_workspace_bytes(shape) bytes.
+ * different treatment"). One kernel launch per call, one block per SM; the
+ * blocks synchronise through counters in the workspace, so the call needs
+ * the whole GPU to itself while it runs (other work on the GPU only delays
+ * it; a wait that exceeds 2 s records MOE_DEV_TIMEOUT).
+ *   x bf16 [d_model] device; out bf16 [d_model] device; d_model <= 4096 and
+ *   (top_k + 1) * d_ff <= about 24000 (h of every slot is staged on chip);
+ *   other sizes return MOE_ERR_SHAPE.
+ *   ws 256-byte aligned, >= moe_decode_workspace_bytes(shape) bytes, and
+ *   zero-filled before its first use (cudaMemset); every call leaves its
+ *   counters at zero for the next one. Zero it again after a call whose
+ *   device status reports MOE_DEV_TIMEOUT. Calls on one workspace must not
+ *   overlap on the GPU.
  */
 size_t moe_decode_workspace_bytes(const moe_shape_t* shape);
 int moe_decode_gemv_w4(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* shape,
@@ -266,16 +275,16 @@ int moe_decode_views(void* ws, size_t ws_bytes, const moe_shape_t* shape,
  * exits); the call itself allocates nothing.
  *   x, w, shape, out, stream: as for moe_decode_gemv_w4 (shape->T == 1).
  *   Returns MOE_ERR_WORKSPACE when moe_decode_workspace_bytes(shape) exceeds
- *   256 KB (the top-8-of-256 layer with d_ff 512 needs about 20 KB), and
+ *   256 KB (the top-8-of-256 layer with d_ff 512 needs about 40 KB), and
  *   MOE_ERR_CUDA if the scratch's device address cannot be obtained.
  * The first call on each device looks the scratch up (cudaGetSymbolAddress,
  * which may load the library's device code onto that device); make that
  * first call before any stream capture. All calls share the one array, which
- * keeps the previous call's contents; nothing in it needs to start at zero
- * (the first kernel clears the status words, every other value is written
- * before it is read). Calls that overlap on the GPU, e.g. on two streams,
- * race on the array; device-side fault records stay in the array and are not
- * readable through moe_get_device_status.
+ * keeps the previous call's contents (a static device array starts at zero,
+ * and every call leaves the kernel's counters at zero). Calls that overlap
+ * on the GPU, e.g. on two streams, race on the array; device-side fault
+ * records stay in the array and are not readable through
+ * moe_get_device_status.
  */
 int moe_decode_gemv_w4_noalloc(const uint16_t* x, const moe_weights_t* w,
                                const moe_shape_t* shape, uint16_t* out, void* stream);
