@@ -30,7 +30,8 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer tokens/s (batch-1 decode, 40 layers) at 1 GB300 + % roofline"
 N_LAYERS = 40
 SELECTED_BYTES_PER_LAYER = 9 * 1_769_472      # 8 routed + shared expert: q + scale + bias
-ROUTER_BYTES_PER_LAYER = 2048 * 256 * 4 + 2048 * 4
+ROUTER_BYTES_PER_LAYER = 2048 * 256 * 4 + 2048 * 4  # fp32 router and shared-gate weights
+DECODE_BYTES_PER_LAYER = SELECTED_BYTES_PER_LAYER + ROUTER_BYTES_PER_LAYER
 FLOP_PER_TOKEN = 9 * 3 * 2 * 2048 * 512        # 56,623,104
 
 
@@ -43,6 +44,10 @@ def parse():
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill configurations")
     ap.add_argument("--prefill-iters", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["decode", "prefill"],
+                    help="no measurement: run one layer repeatedly (decode: 20 + 200 calls; prefill: "
+                         "3 forwards at --profile-T tokens) for a profiler to attach to")
+    ap.add_argument("--profile-T", type=int, default=4096)
     return ap.parse_args()
 
 
@@ -263,19 +268,18 @@ def run_decode(args, world, peaks):
 
     K = args.steps
     step_s = t_dev / K
-    achieved = L * SELECTED_BYTES_PER_LAYER / step_s / 1e9
+    achieved = L * DECODE_BYTES_PER_LAYER / step_s / 1e9
     res = dict(
         value=world * K / t_dev, ms_per_step=step_s * 1e3,
         e2e=dict(value=world * K / t_e2e, unit="tokens/s", h2d_bytes_per_step=L * d * 2,
                  d2h_bytes_per_step=L * d * 2),
-        gpu_launches=3 * L * K,
+        gpu_launches=L * K,  # one decode kernel per layer
         roofline=dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"],
                       unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4),
                       traffic=TRAFFIC.get("decode_layer"),
-                      kernel="decode layer: router GEMV+top-8, gate/up GEMV+SwiGLU, "
-                             "down GEMV+combine (3 launches)",
-                      bytes_per_layer=SELECTED_BYTES_PER_LAYER,
-                      router_bytes_per_layer_not_counted=ROUTER_BYTES_PER_LAYER,
+                      kernel="decode_layer_kernel: router GEMV + top-8 + gate/up GEMV + SwiGLU + "
+                             "down GEMV + weighted combine, one launch per layer",
+                      bytes_per_layer=DECODE_BYTES_PER_LAYER,
                       peak_source=peaks["source"]),
         clocks=clk,
     )
@@ -332,12 +336,14 @@ def run_prefill(T, zipf, host0, args, peaks):
     bm = fwd.view("block_map", (mt, 4), torch.int32)
     nt = fwd.view("num_tiles", (1,), torch.int32)
     rt = fwd.view("row_token", (rows,), torch.int32)
-    h = fwd.view("h", (rows, f), torch.bfloat16)
+    # the layer's own operands: x as f16 (written by the router kernel) and f16 h
+    x16 = fwd.view("x16", (T, d), torch.float16)
+    h = fwd.view("h", (rows, f), torch.float16)
     rw = fwd.view("row_weight", (rows,), torch.float32)
     acc = fwd.view("out_acc", (T, d), torch.float32)
     t = dl.t
     g1 = gpu_graph(lambda: ops.grouped_gemm_w4a16(
-        x, [t["gate"], t["up"]], E, f, bm, nt, mt, bn, ops.EPI_SWIGLU, row_index=rt, n_rows=rows,
+        x16, [t["gate"], t["up"]], E, f, bm, nt, mt, bn, ops.EPI_SWIGLU, row_index=rt, n_rows=rows,
         W_extra=[t["sh_gate"], t["sh_up"]], C=h), stream)
     g2 = gpu_graph(lambda: ops.grouped_gemm_w4a16(
         h, [t["down"]], E, d, bm, nt, mt, bn, ops.EPI_COMBINE, n_rows=rows,
@@ -423,7 +429,38 @@ CONFIG = {
 
 # DRAM bytes per launch unit from the committed ncu summaries (profiles/); None
 # until counters for the current kernels are taken.
-TRAFFIC: dict = {}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch from ncu --set full captures
+# (profiles/): the decode kernel on one layer (cold cache: all of its weights come from
+# HBM), and both grouped GEMMs of one T = 4096 forward. None where no capture of the
+# current kernel exists.
+TRAFFIC: dict = {
+    "decode_layer": 18_132_992,
+    "gemm_T4096": 345_815_040 + 27_454_208 + 231_386_368 + 16_433_664,
+}
+
+
+def profile_run(args):
+    """One layer of the seeded workload, run repeatedly with no timing: the target of the
+    ncu commands recorded under profiles/."""
+    import numpy as np
+    import torch
+    from bit_moe_expert_route_gb300 import ops, synth
+    shape = synth.LayerShape()
+    dl = ops.DeviceLayer(synth.layer_weights(shape, seed=0, layer=0), shape)
+    if args.profile == "decode":
+        dec = ops.Decode(dl)
+        x = torch.from_numpy(synth.tokens(shape, 1, seed=1).view(np.int16)).cuda().view(-1)
+        out = torch.empty(shape.d_model, dtype=torch.bfloat16, device="cuda")
+        for _ in range(220):
+            dec(x, out)
+    else:
+        T = args.profile_T
+        fwd = ops.Forward(dl, T)
+        x = torch.from_numpy(synth.tokens(shape, T, seed=0).view(np.int16)).cuda()
+        for _ in range(3):
+            fwd(x)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": args.profile, "ok": True}), flush=True)
 
 
 def main():
@@ -440,6 +477,9 @@ def main():
     if rank == 0 and not B.up_to_date():
         B.build()
     barrier(world)
+    if args.profile:
+        profile_run(args)
+        return 0
     peaks = measured_peaks()
     res = run_decode(args, world, peaks)
     prefill = []
