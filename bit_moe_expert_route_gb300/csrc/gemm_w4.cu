@@ -67,10 +67,15 @@ struct Cfg {
   // Rings: packed codes (TMA), dequantised A tiles (dequant warps), token
   // tiles B (gather warps or TMA). B tiles are small, so B runs deepest: it
   // has the longest latency to cover (row gathers from L2/HBM).
-  static constexpr int kAStage = NMAT * kABytes;
+  // One weight matrix (down projection): the dequantised A operand goes to
+  // tensor memory instead of shared memory, so the MMA reads only B from
+  // shared memory (the shared-memory traffic per k-block roughly halves).
+  static constexpr bool kATmem = NMAT == 1;
+  static constexpr int kAStage = kATmem ? 0 : NMAT * kABytes;
   static constexpr int kBBytes = BN * kKB * 2;
   static constexpr int kQRing = kSQ * NMAT * kQStage;
-  static constexpr int kSA = NMAT == 2 ? 2 : 3;
+  static constexpr int kSA = NMAT == 2 ? 2 : 4;
+  static constexpr int kACol = 2 * NMAT * BN;  // first TMEM column of the A stages (kATmem)
   static constexpr int kSB0 =
       (kSmemBudget - kQRing - kEpiBytes - kRowInfoBytes - kSA * kAStage) / kBBytes;
   static constexpr int kSB = kSB0 > 8 ? 8 : kSB0;
@@ -82,11 +87,11 @@ struct Cfg {
   static constexpr int kOffBar = kOffRowInfo + kRowInfoBytes;
   static constexpr int kBarBytes = 8 * (2 * kSQ + 2 * kSA + 2 * kSB + 5) + 16;
   static constexpr int kSmem = kOffBar + kBarBytes + 1024;  // + alignment slack
-  static constexpr int kTmemCols0 = 2 * NMAT * BN;
+  static constexpr int kTmemCols0 = 2 * NMAT * BN + (kATmem ? kSA * (kKB / 2) : 0);
   static constexpr int kTmemCols = kTmemCols0 <= 32 ? 32 : kTmemCols0 <= 64 ? 64
                                    : kTmemCols0 <= 128 ? 128 : kTmemCols0 <= 256 ? 256 : 512;
   static_assert(kSB >= 3, "not enough shared memory for three token-tile stages");
-  static_assert(kTmemCols0 <= 512, "accumulators exceed TMEM");
+  static_assert(kTmemCols0 <= 512, "accumulators and A stages exceed TMEM");
   static_assert(kSmem <= 232448, "shared memory per CTA exceeded");
 };
 
@@ -328,13 +333,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
           }
           tc_fence_after();
           const uint32_t b_addr = smem_u32(smem + C::kOffB + sb * C::kBBytes);
-#pragma unroll
-          for (int j = 0; j < NMAT; ++j) {
-            const uint32_t a_addr = smem_u32(smem + C::kOffA + (s * NMAT + j) * kABytes);
+          if constexpr (C::kATmem) {
+            const uint32_t a_tmem = tmem_base + C::kACol + s * (kKB / 2);
 #pragma unroll
             for (int kk = 0; kk < kKB / 16; ++kk)
-              tc_mma_bf16(d_tmem + j * BN, smem_desc_sw128(a_addr + kk * 32),
-                          smem_desc_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0);
+              tc_mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0);
+          } else {
+#pragma unroll
+            for (int j = 0; j < NMAT; ++j) {
+              const uint32_t a_addr = smem_u32(smem + C::kOffA + (s * NMAT + j) * kABytes);
+#pragma unroll
+              for (int kk = 0; kk < kKB / 16; ++kk)
+                tc_mma_bf16(d_tmem + j * BN, smem_desc_sw128(a_addr + kk * 32),
+                            smem_desc_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0);
+            }
           }
           tc_commit(&a_empty[s]);
           tc_commit(&b_empty[sb]);
@@ -375,8 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
       if (!mbar_wait(&a_empty[sa], ((it / C::kSA) & 1) ^ 1, abort_flag, g.status, 7)) return false;
 #pragma unroll
       for (int j = 0; j < NMAT; ++j) {
-        uint8_t* a_tile = smem + C::kOffA + (sa * NMAT + j) * kABytes;
         const uint32_t words[4] = {qw[j].x, qw[j].y, qw[j].z, qw[j].w};
+        uint32_t r[16];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint4 o;
@@ -386,10 +398,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
           else
             o = dequant_word(words[c], *reinterpret_cast<const __nv_bfloat162*>(&s2[j]),
                              *reinterpret_cast<const __nv_bfloat162*>(&b2[j]));
-          *reinterpret_cast<uint4*>(a_tile + sw128_offset(m, half * 4 + c)) = o;
+          if constexpr (C::kATmem) {
+            r[4 * c] = o.x;
+            r[4 * c + 1] = o.y;
+            r[4 * c + 2] = o.z;
+            r[4 * c + 3] = o.w;
+          } else {
+            uint8_t* a_tile = smem + C::kOffA + (sa * NMAT + j) * kABytes;
+            *reinterpret_cast<uint4*>(a_tile + sw128_offset(m, half * 4 + c)) = o;
+          }
         }
+        if constexpr (C::kATmem)  // row m = lane (quarter warp % 4), columns half*16 .. +15 of the stage
+          tmem_st_32x32b_x16(tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + C::kACol +
+                                 sa * (kKB / 2) + half * 16, r);
       }
-      fence_proxy_async_smem();
+      if constexpr (C::kATmem) {
+        tc_wait_st();
+        tc_fence_before();
+      } else {
+        fence_proxy_async_smem();
+      }
       mbar_arrive_warp(&a_full[sa]);
       if (kb % QK == QK - 1) {
         mbar_arrive_warp(&q_empty[sq]);
@@ -533,18 +561,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
   } else if (warp >= 12) {
     // ------------------------------------------------------------ epilogue
     // TMEM -> registers -> (NONE) direct fp32 stores, or (SWIGLU, COMBINE) a
-    // per-warp shared-memory staging tile of CH token rows x the warp's 32
-    // outputs, double buffered, written back one token-row segment per lane
-    // with a TMA bulk copy: a plain store (SWIGLU) or an fp32 add into the
-    // token's output row at L2 (COMBINE, the weighted combine of the routed
-    // experts and the shared one). Only warp-level syncs per chunk.
+    // staging tile of CH token rows x the tile's 128 outputs shared by the 4
+    // epilogue warps (each fills its 32 outputs), double buffered, written
+    // back one whole token row per TMA bulk copy: a plain store (SWIGLU) or an
+    // fp32 add into the token's output row at L2 (COMBINE, the weighted
+    // combine of the routed experts and the shared one). Whole rows keep the
+    // number of bulk operations at one per token row (each has a fixed cost
+    // in the copy engine and at L2).
     const int ew = warp & 3;             // TMEM lane quarter = the warp's 32 outputs
     const int et = threadIdx.x - 384;    // 0..127 inside the epilogue group
     constexpr int CH = C::kCH;
-    constexpr int kWarpStage = CH * 32;  // elements per staging buffer of one warp
+    constexpr int kRowsPerWarp = CH / 4;  // token rows each warp writes back per chunk
+    constexpr int kStage = CH * kTileM;   // elements per staging buffer
     float* s_rscale = reinterpret_cast<float*>(smem + C::kOffRowInfo);
     int* s_orow = reinterpret_cast<int*>(s_rscale + BN);
-    uint8_t* stage_w = smem + C::kOffEpi + ew * 2 * kWarpStage * C::kStageElem;
+    uint8_t* stage = smem + C::kOffEpi;
     uint32_t acc_it = 0, chunk = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const TileInfo t = load_tile(g, u, MT);
@@ -568,6 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
       }
       const uint32_t taddr = tmem_base + ((uint32_t)(ew * 32) << 16) + buf * (NMAT * BN);
       const int64_t col0 = (int64_t)t.mt * kTileM + ew * 32;  // this warp's first output
+      const int64_t tcol0 = (int64_t)t.mt * kTileM;           // the tile's first output
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += CH, ++chunk) {
         uint32_t v0[32], v1[32];
@@ -595,34 +627,36 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
           }
         } else {
           const int sb = chunk & 1;
-          if (lane < CH) bulk_wait_read<1>();  // copies from two chunks ago read this buffer
-          __syncwarp();
+          // the copies issued from this buffer two chunks ago have read it
+          if (lane < kRowsPerWarp) bulk_wait_read<1>();
+          named_bar_sync(2, 128);
           if constexpr (EPI == MOE_EPI_COMBINE) {
-            float* S = reinterpret_cast<float*>(stage_w) + sb * kWarpStage;
+            float* S = reinterpret_cast<float*>(stage) + sb * kStage + ew * 32;
 #pragma unroll
-            for (int i = 0; i < CH; ++i) S[i * 32 + lane] = __uint_as_float(v0[i]) * s_rscale[c0 + i];
+            for (int i = 0; i < CH; ++i) S[i * kTileM + lane] = __uint_as_float(v0[i]) * s_rscale[c0 + i];
           } else {
-            uint16_t* S = reinterpret_cast<uint16_t*>(stage_w) + sb * kWarpStage;
+            uint16_t* S = reinterpret_cast<uint16_t*>(stage) + sb * kStage + ew * 32;
 #pragma unroll
             for (int i = 0; i < CH; ++i) {
               const float a = __uint_as_float(v0[i]);
-              S[i * 32 + lane] = to_operand<F16>(a / (1.f + __expf(-a)) * __uint_as_float(v1[i]));
+              S[i * kTileM + lane] = to_operand<F16>(a / (1.f + __expf(-a)) * __uint_as_float(v1[i]));
             }
           }
           fence_proxy_async_smem();
-          __syncwarp();
-          if (lane < CH) {
-            const int n = c0 + lane;
+          named_bar_sync(2, 128);  // the chunk's rows are complete
+          if (lane < kRowsPerWarp) {
+            const int i = ew * kRowsPerWarp + lane, n = c0 + i;
             if (n < t.rows) {
               if constexpr (EPI == MOE_EPI_COMBINE) {
                 const int orow = s_orow[n];
-                const float* src = reinterpret_cast<const float*>(stage_w) + sb * kWarpStage + lane * 32;
+                const float* src = reinterpret_cast<const float*>(stage) + sb * kStage + i * kTileM;
                 if (orow >= 0)
-                  bulk_reduce_add_f32(static_cast<float*>(g.C) + (int64_t)orow * g.ldc + col0, src, 128);
+                  bulk_reduce_add_f32(static_cast<float*>(g.C) + (int64_t)orow * g.ldc + tcol0, src,
+                                      kTileM * 4);
               } else {
-                const uint16_t* src =
-                    reinterpret_cast<const uint16_t*>(stage_w) + sb * kWarpStage + lane * 32;
-                bulk_store(static_cast<uint16_t*>(g.C) + ((int64_t)t.row0 + n) * g.ldc + col0, src, 64);
+                const uint16_t* src = reinterpret_cast<const uint16_t*>(stage) + sb * kStage + i * kTileM;
+                bulk_store(static_cast<uint16_t*>(g.C) + ((int64_t)t.row0 + n) * g.ldc + tcol0, src,
+                           kTileM * 2);
               }
             }
             bulk_commit();
@@ -633,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
       mbar_arrive_warp(&acc_empty[buf]);
       ++acc_it;
     }
-    if (lane < CH) bulk_wait_all();  // every bulk copy has landed before the CTA exits
+    if (lane < kRowsPerWarp) bulk_wait_all();  // every bulk copy has landed before the CTA exits
   }
 
   tc_fence_before();
