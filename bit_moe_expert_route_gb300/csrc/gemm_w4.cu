@@ -677,19 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() { return tensor_map_encoder(); }
 
 // Packed codes viewed as a 2-D uint32 tensor [rows][K/8]; box 8 words x 128 rows.
 bool make_q_map(CUtensorMap* tm, const uint32_t* q, int64_t rows, int K, int qk) {
@@ -759,6 +747,20 @@ cudaError_t launch_epi(const KParams& kp, cudaStream_t s) {
 }
 
 }  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
 
 cudaError_t gemm_w4_launch(const GemmParams& p, cudaStream_t s) {
   KParams kp;

@@ -3,6 +3,8 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "moe.h"
@@ -16,11 +18,6 @@ struct RouteParams {
   const float* logits;     // [T][E]
   const float* bias;       // [E] or null
   int T, E, k, block_n, with_shared;
-  // optional shared-expert gate (moe_forward): gate_logit[t] = x_t . wsg
-  const uint16_t* x;       // [T][d] bf16 or null
-  const float* wsg;        // [d]
-  int d;
-  float* gate_logit;       // [T]
   // outputs
   int32_t* ids;            // [T][k]
   float* w;                // [T][k]
@@ -42,10 +39,27 @@ inline int route_nblk(int T) { return (T + kRouteTPB - 1) / kRouteTPB; }
 cudaError_t route_launch(const RouteParams& p, cudaStream_t s);
 
 // ---------------------------------------------------------------- router GEMM
-// logits[t][e] = sum_k x[t][k] * Wr[k][e]   (fp32 accumulate)
-// Optionally also writes x16 = f16(x) (saturated), the tensor-core operand copy.
-cudaError_t router_gemm_launch(const uint16_t* x, const float* Wr, int T, int d, int E,
-                               float* logits, uint16_t* x16, cudaStream_t s);
+// logits[t][e] = sum_k x[t][k] * Wr[k][e] and gate_logit[t] = x_t . wsg, fp32
+// accumulation of exact products (the fp32 weights are split into three bf16
+// planes, wsplit, rebuilt on every call). Optionally also writes
+// x16 = f16(x) (saturated), the tensor-core operand copy.
+struct RouterParams {
+  const uint16_t* x;        // [T][d] bf16
+  int T, d, E, k;
+  const float* Wr;          // [d][E]
+  const float* wsg;         // [d] or null (no shared expert)
+  uint16_t* wsplit;         // scratch [3][router_split_rows(E, wsg != null)][d] bf16
+  float* logits;            // [T][E]
+  float* gate_logit;        // [T] (with wsg)
+  float* row_weight;        // [T*k + T] or null: row T*k + t gets sigmoid(gate_logit[t])
+  uint16_t* x16;            // [T][d] or null
+  int32_t* status;
+};
+inline int router_split_rows(int E, bool gate) { return E + (gate ? 16 : 0); }
+cudaError_t router_launch(const RouterParams& p, cudaStream_t s);
+
+// cuTensorMapEncodeTiled from the driver (null if unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // ---------------------------------------------------------------- grouped GEMM
 struct GemmW4 {

@@ -79,6 +79,7 @@ bool shape_ok(const moe_shape_t* s, bool need_tokens) {
 struct FwdWs {
   moe_forward_views_t v;
   int32_t* blk;  // routing scratch [route_nblk(T)][E]
+  uint16_t* wsplit;  // router weights as three bf16 planes [3][Ep][d]
   size_t bytes;
 };
 
@@ -104,6 +105,7 @@ FwdWs forward_ws(void* ws, const moe_shape_t* s, int bn) {
   r.v.block_map = c.take<int32_t>((size_t)r.v.max_tiles * 4);
   r.v.num_tiles = c.take<int32_t>(1);
   r.blk = c.take<int32_t>((size_t)moe::route_nblk(T) * E);
+  r.wsplit = c.take<uint16_t>((size_t)3 * moe::router_split_rows(E, true) * s->d_model);
   r.v.x16 = c.take<uint16_t>((size_t)T * s->d_model);
   r.v.h = c.take<uint16_t>((size_t)rows * s->d_ff);
   r.v.out_acc = c.take<float>((size_t)T * s->d_model);
@@ -356,10 +358,23 @@ int moe_forward(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* sh
   const bool shared = w->shared_gate != nullptr;
   const int64_t rows = (int64_t)T * k + (shared ? T : 0);
 
-  // 1. router logits
-  if ((rc = cuda_status(moe::router_gemm_launch(x, w->router, T, d, E, v.logits, v.x16, s))) !=
-      MOE_OK)
-    return rc;
+  // 1. router logits, shared-expert gate logit and the f16 copy of x
+  moe::RouterParams rt;
+  memset(&rt, 0, sizeof rt);
+  rt.x = x;
+  rt.T = T;
+  rt.d = d;
+  rt.E = E;
+  rt.k = k;
+  rt.Wr = w->router;
+  rt.wsg = w->shared_gate;
+  rt.wsplit = fw.wsplit;
+  rt.logits = v.logits;
+  rt.gate_logit = v.gate_logit;
+  rt.row_weight = v.row_weight;
+  rt.x16 = v.x16;
+  rt.status = v.status;
+  if ((rc = cuda_status(moe::router_launch(rt, s))) != MOE_OK) return rc;
   // 2. top-k, shared gate, histogram, scan, scatter, block map
   moe::RouteParams rp;
   memset(&rp, 0, sizeof rp);
@@ -370,10 +385,6 @@ int moe_forward(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* sh
   rp.k = k;
   rp.block_n = block_n;
   rp.with_shared = shared ? 1 : 0;
-  rp.x = shared ? x : nullptr;
-  rp.wsg = w->shared_gate;
-  rp.d = d;
-  rp.gate_logit = v.gate_logit;
   rp.ids = v.topk_ids;
   rp.w = v.topk_w;
   rp.counts = v.counts;

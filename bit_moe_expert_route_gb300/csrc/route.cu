@@ -6,10 +6,12 @@
 // prefix scan, scatter and block-map build all stay on the GPU.)
 //
 // Three launches, no host round trip:
-//   1. route_topk_kernel    one warp per token: top-k by warp argmax (value
-//                           descending, ties to the lower id), softmax over the
-//                           selected logits, optional shared-expert gate,
-//                           per-block expert histogram (shared-memory counts).
+//   1. route_topk_kernel    one warp per token (32 warps per block, the next
+//                           token's logits loaded while the current one is
+//                           ranked): top-k by warp argmax (value descending,
+//                           ties to the lower id) with two warp reductions per
+//                           round, softmax over the selected logits, per-block
+//                           expert histogram (shared-memory counts).
 //   2. route_scan_kernel    one CTA: per-(block, expert) bases, counts,
 //                           offsets, tile offsets and the block map.
 //   3. route_scatter_kernel per block: stable rank of each assignment inside
@@ -27,55 +29,77 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
+// Threads per top-k block: 32 warps (4 tokens each) while the per-lane
+// logit registers stay small, 8 warps for very wide routers.
+template <int NPL>
+constexpr int topk_threads() { return NPL <= 8 ? 1024 : 256; }
+
+// Order-preserving map of a float onto uint32 (larger value, larger key);
+// -0 is folded onto +0 so that equal values give equal keys. Key 0 (a NaN
+// pattern) is never produced by a logit and marks "nothing left".
+MOE_DEVINL uint32_t order_key(float v) {
+  const uint32_t u = v == 0.f ? 0u : __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+MOE_DEVINL float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 template <int NPL>  // logits per lane: E <= 32 * NPL
-__global__ void __launch_bounds__(kThreads) route_topk_kernel(RouteParams p) {
+__global__ void __launch_bounds__(topk_threads<NPL>()) route_topk_kernel(RouteParams p) {
+  constexpr int kW = topk_threads<NPL>() / 32;
+  constexpr bool kPrefetch = NPL <= 8;
   extern __shared__ int hist[];  // [E]
-  for (int e = threadIdx.x; e < p.E; e += kThreads) hist[e] = 0;
+  for (int e = threadIdx.x; e < p.E; e += kW * 32) hist[e] = 0;
   __syncthreads();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t_begin = blockIdx.x * kRouteTPB;
   const int t_end = min(p.T, t_begin + kRouteTPB);
-  for (int t = t_begin + warp; t < t_end; t += kWarps) {
-    float z[NPL];
+  // keys of z = logit + bias (fp32 add, the decision precision) for one token
+  auto load_keys = [&](int t, uint32_t (&key)[NPL]) {
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
       const int e = i * 32 + lane;
-      float v = 0.f;
+      uint32_t kv = 0u;
       if (e < p.E) {
-        v = p.logits[(size_t)t * p.E + e];
-        if (p.bias) v = v + p.bias[e];  // fp32 add, as the decision precision
+        float v = p.logits[(size_t)t * p.E + e];
+        if (p.bias) v = v + p.bias[e];
+        kv = order_key(v);
       }
-      z[i] = v;
+      key[i] = kv;
     }
+  };
+  uint32_t next[NPL];
+  if (kPrefetch && t_begin + warp < t_end) load_keys(t_begin + warp, next);
+  for (int t = t_begin + warp; t < t_end; t += kW) {
+    uint32_t key[NPL];
+    if (kPrefetch) {
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) key[i] = next[i];
+      if (t + kW < t_end) load_keys(t + kW, next);
+    } else {
+      load_keys(t, key);
+    }
+    // k rounds of a warp argmax: the largest key, then among the lanes that
+    // hold it the lowest expert id (ties go to the lower id)
     uint32_t taken = 0;
     float my_z = 0.f;
     int my_e = 0;
     for (int j = 0; j < p.k; ++j) {
-      float bv = 0.f;
-      int be = INT_MAX;
+      uint32_t bk = 0u, be = 0xFFFFFFFFu;
 #pragma unroll
-      for (int i = 0; i < NPL; ++i) {
-        const int e = i * 32 + lane;
-        const bool ok = e < p.E && !((taken >> i) & 1u);
-        if (ok && (be == INT_MAX || z[i] > bv)) {
-          bv = z[i];
-          be = e;
+      for (int i = 0; i < NPL; ++i)
+        if (!((taken >> i) & 1u) && key[i] > bk) {
+          bk = key[i];
+          be = (uint32_t)(i * 32 + lane);
         }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(kFull, bv, off);
-        const int oe = __shfl_xor_sync(kFull, be, off);
-        if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      const uint32_t m = __reduce_max_sync(kFull, bk);
+      const uint32_t e = __reduce_min_sync(kFull, bk == m ? be : 0xFFFFFFFFu);
+      if ((int)(e & 31u) == lane) taken |= 1u << (e >> 5);
       if (lane == j) {
-        my_z = bv;
-        my_e = be;
+        my_z = key_value(m);
+        my_e = (int)e;
       }
     }
     const float zmax = __shfl_sync(kFull, my_z, 0);
@@ -89,31 +113,9 @@ __global__ void __launch_bounds__(kThreads) route_topk_kernel(RouteParams p) {
       p.w[a] = ex / sum;
       atomicAdd(&hist[my_e], 1);
     }
-    if (p.x) {  // shared-expert gate logit x_t . w_sg and sigmoid gate
-      float acc = 0.f;
-      const uint4* xr = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.d);
-      const float4* wr = reinterpret_cast<const float4*>(p.wsg);
-      for (int c = lane; c < p.d / 8; c += 32) {
-        const uint4 xv = xr[c];
-        const float4 w0 = wr[2 * c], w1 = wr[2 * c + 1];
-        const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
-        const float ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          acc = fmaf(__uint_as_float(xs[i] << 16), ws[2 * i], acc);
-          acc = fmaf(__uint_as_float(xs[i] & 0xFFFF0000u), ws[2 * i + 1], acc);
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
-      if (lane == 0) {
-        p.gate_logit[t] = acc;
-        if (p.row_weight) p.row_weight[(size_t)p.T * p.k + t] = 1.f / (1.f + expf(-acc));
-      }
-    }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < p.E; e += kThreads) p.blk[(size_t)blockIdx.x * p.E + e] = hist[e];
+  for (int e = threadIdx.x; e < p.E; e += kW * 32) p.blk[(size_t)blockIdx.x * p.E + e] = hist[e];
 }
 
 // Exclusive scan over the CTA (blockDim.x == 1024). Returns the exclusive
@@ -273,12 +275,12 @@ cudaError_t route_launch(const RouteParams& p, cudaStream_t s) {
   const int nblk = route_nblk(p.T);
   const size_t hist_bytes = (size_t)p.E * sizeof(int);
   const int npl = (p.E + 31) / 32;
-  if (npl <= 1) route_topk_kernel<1><<<nblk, kThreads, hist_bytes, s>>>(p);
-  else if (npl <= 2) route_topk_kernel<2><<<nblk, kThreads, hist_bytes, s>>>(p);
-  else if (npl <= 4) route_topk_kernel<4><<<nblk, kThreads, hist_bytes, s>>>(p);
-  else if (npl <= 8) route_topk_kernel<8><<<nblk, kThreads, hist_bytes, s>>>(p);
-  else if (npl <= 16) route_topk_kernel<16><<<nblk, kThreads, hist_bytes, s>>>(p);
-  else route_topk_kernel<32><<<nblk, kThreads, hist_bytes, s>>>(p);
+  if (npl <= 1) route_topk_kernel<1><<<nblk, topk_threads<1>(), hist_bytes, s>>>(p);
+  else if (npl <= 2) route_topk_kernel<2><<<nblk, topk_threads<2>(), hist_bytes, s>>>(p);
+  else if (npl <= 4) route_topk_kernel<4><<<nblk, topk_threads<4>(), hist_bytes, s>>>(p);
+  else if (npl <= 8) route_topk_kernel<8><<<nblk, topk_threads<8>(), hist_bytes, s>>>(p);
+  else if (npl <= 16) route_topk_kernel<16><<<nblk, topk_threads<16>(), hist_bytes, s>>>(p);
+  else route_topk_kernel<32><<<nblk, topk_threads<32>(), hist_bytes, s>>>(p);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   route_scan_kernel<<<1, 1024, 0, s>>>(p, nblk);
