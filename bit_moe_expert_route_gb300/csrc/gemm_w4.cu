@@ -16,9 +16,12 @@
 //                  4 KB per projection) into a ring of shared-memory stages.
 //   * warp 1       allocates TMEM and issues tcgen05.mma (one thread).
 //   * warps 4-11   dequantise: two threads per weight row, 32 codes each;
-//                  RNE(scale*q + bias) (f16 or bf16) goes into the
-//                  128-byte-swizzled K-major A operand, then the packed-code
-//                  stage is freed (only after its codes are consumed).
+//                  RNE(scale*q + bias) (f16 or bf16) goes into the A operand:
+//                  in tensor memory (tcgen05.st: row = TMEM lane, two K
+//                  elements per column) where it fits beside the
+//                  accumulators, else the 128-byte-swizzled K-major tile in
+//                  shared memory; then the packed-code stage is freed (only
+//                  after its codes are consumed).
 //   * warps 2-3    gather: token rows (through row_index) are copied with
 //                  16-byte cp.async into the swizzled K-major B operand;
 //                  rows past the tile's end are zero-filled. Without a
@@ -67,15 +70,21 @@ struct Cfg {
   // Rings: packed codes (TMA), dequantised A tiles (dequant warps), token
   // tiles B (gather warps or TMA). B tiles are small, so B runs deepest: it
   // has the longest latency to cover (row gathers from L2/HBM).
-  // One weight matrix (down projection): the dequantised A operand goes to
-  // tensor memory instead of shared memory, so the MMA reads only B from
-  // shared memory (the shared-memory traffic per k-block roughly halves).
-  static constexpr bool kATmem = NMAT == 1;
+  // The dequantised A operand goes to tensor memory instead of shared
+  // memory where it fits next to two buffers of accumulators (NMAT x BN
+  // columns each; TMEM has 512): the MMA then reads only B from shared memory
+  // (the shared-memory traffic per k-block roughly halves). The gate/up GEMM
+  // at block_n 128 fills TMEM with its accumulators and keeps A in shared
+  // memory: a single accumulator buffer would hold every tile's MMAs behind
+  // the previous tile's epilogue, which costs more than the traffic saved.
+  static constexpr int kAColsStage = NMAT * (kKB / 2);
+  static constexpr int kSA = 2 * NMAT * BN + 4 * kAColsStage <= 512 ? 4 : 2;
+  static constexpr bool kATmem = 2 * NMAT * BN + kSA * kAColsStage <= 512;
   static constexpr int kAStage = kATmem ? 0 : NMAT * kABytes;
   static constexpr int kBBytes = BN * kKB * 2;
   static constexpr int kQRing = kSQ * NMAT * kQStage;
-  static constexpr int kSA = NMAT == 2 ? 2 : 4;
-  static constexpr int kACol = 2 * NMAT * BN;  // first TMEM column of the A stages (kATmem)
+  static constexpr int kAccBufs = 2;
+  static constexpr int kACol = kAccBufs * NMAT * BN;  // first TMEM column of the A stages
   static constexpr int kSB0 =
       (kSmemBudget - kQRing - kEpiBytes - kRowInfoBytes - kSA * kAStage) / kBBytes;
   static constexpr int kSB = kSB0 > 8 ? 8 : kSB0;
@@ -87,7 +96,7 @@ struct Cfg {
   static constexpr int kOffBar = kOffRowInfo + kRowInfoBytes;
   static constexpr int kBarBytes = 8 * (2 * kSQ + 2 * kSA + 2 * kSB + 5) + 16;
   static constexpr int kSmem = kOffBar + kBarBytes + 1024;  // + alignment slack
-  static constexpr int kTmemCols0 = 2 * NMAT * BN + (kATmem ? kSA * (kKB / 2) : 0);
+  static constexpr int kTmemCols0 = kAccBufs * NMAT * BN + (kATmem ? kSA * kAColsStage : 0);
   static constexpr int kTmemCols = kTmemCols0 <= 32 ? 32 : kTmemCols0 <= 64 ? 64
                                    : kTmemCols0 <= 128 ? 128 : kTmemCols0 <= 256 ? 256 : 512;
   static_assert(kSB >= 3, "not enough shared memory for three token-tile stages");
@@ -320,8 +329,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
       for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
         const TileInfo t = load_tile(g, u, MT);
         if (!t.ok) continue;
-        const uint32_t buf = acc_it & 1;
-        if (!mbar_wait(&acc_empty[buf], ((acc_it >> 1) & 1) ^ 1, abort_flag, g.status, 3)) break;
+        const uint32_t buf = acc_it % C::kAccBufs;
+        if (!mbar_wait(&acc_empty[buf], ((acc_it / C::kAccBufs) & 1) ^ 1, abort_flag, g.status, 3))
+          break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * (NMAT * BN);
         for (int kb = 0; kb < KB; ++kb, ++it) {
@@ -334,10 +344,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
           tc_fence_after();
           const uint32_t b_addr = smem_u32(smem + C::kOffB + sb * C::kBBytes);
           if constexpr (C::kATmem) {
-            const uint32_t a_tmem = tmem_base + C::kACol + s * (kKB / 2);
 #pragma unroll
-            for (int kk = 0; kk < kKB / 16; ++kk)
-              tc_mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0);
+            for (int j = 0; j < NMAT; ++j) {
+              const uint32_t a_tmem = tmem_base + C::kACol + s * C::kAColsStage + j * (kKB / 2);
+#pragma unroll
+              for (int kk = 0; kk < kKB / 16; ++kk)
+                tc_mma_ts(d_tmem + j * BN, a_tmem + kk * 8, smem_desc_sw128(b_addr + kk * 32), idesc,
+                          (kb | kk) != 0);
+            }
           } else {
 #pragma unroll
             for (int j = 0; j < NMAT; ++j) {
@@ -410,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
         }
         if constexpr (C::kATmem)  // row m = lane (quarter warp % 4), columns half*16 .. +15 of the stage
           tmem_st_32x32b_x16(tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + C::kACol +
-                                 sa * (kKB / 2) + half * 16, r);
+                                 sa * C::kAColsStage + j * (kKB / 2) + half * 16, r);
       }
       if constexpr (C::kATmem) {
         tc_wait_st();
@@ -580,9 +594,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const TileInfo t = load_tile(g, u, MT);
       if (!t.ok) continue;
-      const uint32_t buf = acc_it & 1;
-      if (!mbar_wait(&acc_full[buf], (acc_it >> 1) & 1, abort_flag, g.status, 9)) break;
+      const uint32_t buf = acc_it % C::kAccBufs;
+      if (!mbar_wait(&acc_full[buf], (acc_it / C::kAccBufs) & 1, abort_flag, g.status, 9)) break;
       tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(ew * 32) << 16) + buf * (NMAT * BN);
+      const int64_t tcol0 = (int64_t)t.mt * kTileM;  // the tile's first output
       if constexpr (EPI == MOE_EPI_COMBINE) {
         named_bar_sync(1, 128);  // every epilogue warp is done with the previous tile's rows
         for (int n = et; n < t.rows; n += 128) {
@@ -597,9 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
         }
         named_bar_sync(1, 128);
       }
-      const uint32_t taddr = tmem_base + ((uint32_t)(ew * 32) << 16) + buf * (NMAT * BN);
-      const int64_t col0 = (int64_t)t.mt * kTileM + ew * 32;  // this warp's first output
-      const int64_t tcol0 = (int64_t)t.mt * kTileM;           // the tile's first output
+      const int64_t col0 = tcol0 + ew * 32;  // this warp's first output
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += CH, ++chunk) {
         uint32_t v0[32], v1[32];
