@@ -427,15 +427,13 @@ CONFIG = {
     "parallelism": "replicas",
 }
 
-# DRAM bytes per launch unit from the committed ncu summaries (profiles/); None
-# until counters for the current kernels are taken.
-# dram__bytes_read.sum + dram__bytes_write.sum per launch from ncu --set full captures
-# (profiles/): the decode kernel on one layer (cold cache: all of its weights come from
-# HBM), and both grouped GEMMs of one T = 4096 forward. None where no capture of the
-# current kernel exists.
+# dram__bytes_read.sum + dram__bytes_write.sum per launch unit, from the ncu captures
+# summarised under profiles/: the decode kernel on one layer (cold cache: all of its
+# weights come from HBM), and both grouped GEMMs of one T = 4096 forward (mean of three
+# forwards). None where no capture of the current kernel exists.
 TRAFFIC: dict = {
     "decode_layer": 18_132_992,
-    "gemm_T4096": 345_815_040 + 27_454_208 + 231_386_368 + 16_433_664,
+    "gemm_T4096": 345_683_200 + 24_180_565 + 231_067_648 + 12_423_168,
 }
 
 
