@@ -10,21 +10,25 @@
 //   hi = bf16(w),  lo = bf16(w - hi),  lo2 = bf16(w - hi - lo)
 // (each residual is exact in fp32, and the last one has at most 8
 // significant bits), and the product of two bf16 numbers is exact in fp32.
-// So x . w = x . hi + x . lo + x . lo2 runs as three bf16 tcgen05 MMAs into
-// one fp32 accumulator in tensor memory: the only rounding is the fp32
-// accumulation, as in an fp32 dot product.
+// So x . hi, x . lo and x . lo2 are three exact-product bf16 dot products
+// with fp32 accumulation; their sum is x . w up to the rounding of fp32
+// accumulation, as in an fp32 dot product. The three weight tiles of a K
+// step are stacked along N (N = 3 x the tile's experts), so one tcgen05 MMA
+// per 16-wide K step reads the x tile once for all three.
 //
 //   router_split_kernel  Wr [d][E] (+ w_sg) -> planes [3][Ep][d] bf16, K-major
 //   router_tc_kernel     one CTA per (128-token tile, expert tile):
 //                          warp 0     TMA producer (x tile + 3 weight tiles
 //                                     per 64-wide K step, 4-stage ring)
 //                          warp 1     TMEM allocation, tcgen05.mma issue
+//                                     (three accumulators side by side)
 //                          warps 2-5  during the main loop, in the CTAs of
 //                                     expert tile 0: the f16 copy of x read
 //                                     back from the staged x tiles; then the
-//                                     epilogue: tcgen05.ld of the logits and
-//                                     the gate logit (sigmoid weight of the
-//                                     shared rows)
+//                                     epilogue: tcgen05.ld of the three
+//                                     accumulators, hi + lo + lo2 per logit,
+//                                     and the gate logit (sigmoid weight of
+//                                     the shared rows)
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -88,7 +92,6 @@ struct RouterKParams {
   int Ep;               // rows per plane
   int n_tiles;          // expert tiles
   int n_last;           // MMA N of the last tile (16..80, a multiple of 16)
-  uint32_t b_stride;    // bytes per weight plane tile in a stage
   uint32_t stage_bytes;
   uint32_t tmem_cols;
 };
@@ -118,7 +121,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
   const int nt = blockIdx.x, m0 = blockIdx.y * kRTM;
   const bool last = nt == kp.n_tiles - 1;
   const int n0 = nt * kRBn;
-  const int n_mma = last ? kp.n_last : kRBn;
+  const int n_mma = last ? kp.n_last : kRBn;   // experts (+ gate) of this tile
+  const uint32_t b_stride = (uint32_t)n_mma * 128u;  // one plane's tile: n_mma rows of 128 B
   const bool convert = p.x16 != nullptr && nt == 0;
   const int KB = p.d / kRKB;
 
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
         mbar_arrive_expect_tx(&full[s], kRATile + 3 * (uint32_t)n_mma * 128u);
         tma_load_2d(st, &kp.tm_x, kb * kRKB, m0, &full[s], pol_x);
         for (int j = 0; j < 3; ++j)
-          tma_load_2d(st + kRATile + j * kp.b_stride, last ? &kp.tm_wl : &kp.tm_w, kb * kRKB,
+          tma_load_2d(st + kRATile + j * b_stride, last ? &kp.tm_wl : &kp.tm_w, kb * kRKB,
                       j * kp.Ep + n0, &full[s], pol_w);
         ++issued;
       }
@@ -166,20 +170,17 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issue
-      const uint32_t idesc = idesc_bf16_f32(kRTM, n_mma);
+      const uint32_t idesc = idesc_bf16_f32(kRTM, 3 * n_mma);  // planes stacked along N
       for (int kb = 0; kb < KB; ++kb) {
         const int s = kb % kRStages;
         if (!mbar_wait(&full[s], (kb / kRStages) & 1, abort_flag, p.status, 41)) break;
         tc_fence_after();
         const uint32_t a = smem_u32(smem + (size_t)s * kp.stage_bytes);
+        const uint32_t b = a + kRATile;
 #pragma unroll
-        for (int j = 0; j < 3; ++j) {
-          const uint32_t b = a + kRATile + j * kp.b_stride;
-#pragma unroll
-          for (int kk = 0; kk < kRKB / 16; ++kk)
-            tc_mma_bf16(tmem, smem_desc_sw128(a + kk * 32), smem_desc_sw128(b + kk * 32), idesc,
-                        (kb | j | kk) != 0);
-        }
+        for (int kk = 0; kk < kRKB / 16; ++kk)
+          tc_mma_bf16(tmem, smem_desc_sw128(a + kk * 32), smem_desc_sw128(b + kk * 32), idesc,
+                      (kb | kk) != 0);
         tc_commit(&empty[s]);
       }
       tc_commit(acc_full);  // also issued after an abort: tracks every MMA issued
@@ -218,35 +219,35 @@ __global__ void __launch_bounds__(kRThreads, 1)
     if (mbar_wait(acc_full, 0, abort_flag, p.status, 43)) {
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
-      uint32_t r[5][16];
-#pragma unroll
-      for (int c = 0; c < 5; ++c)
-        if (c * 16 < n_mma) tmem_ld_32x32b_x16(taddr + c * 16, r[c]);
-      tc_wait_ld();
       const int t = m0 + quarter * 32 + lane;
-      if (t < p.T) {
-        float* row = p.logits + (size_t)t * p.E;
+      float* row = p.logits + (size_t)t * p.E;
+      const int gcol = last && p.wsg ? p.E - n0 : -1;  // the gate column follows the last expert
+#pragma unroll 1
+      for (int c0 = 0; c0 < n_mma; c0 += 16) {
+        uint32_t hi[16], lo[16], lo2[16];
+        tmem_ld_32x32b_x16(taddr + c0, hi);
+        tmem_ld_32x32b_x16(taddr + n_mma + c0, lo);
+        tmem_ld_32x32b_x16(taddr + 2 * n_mma + c0, lo2);
+        tc_wait_ld();
+        float v[16];
 #pragma unroll
-        for (int c = 0; c < 5; ++c) {
+        for (int j = 0; j < 16; ++j)
+          v[j] = (__uint_as_float(hi[j]) + __uint_as_float(lo[j])) + __uint_as_float(lo2[j]);
+        if (t < p.T) {
 #pragma unroll
           for (int j = 0; j < 16; j += 4) {
-            const int e = n0 + c * 16 + j;  // E - n0 is a multiple of 8
-            if (c * 16 < n_mma && e < p.E)
-              *reinterpret_cast<float4*>(row + e) =
-                  make_float4(__uint_as_float(r[c][j]), __uint_as_float(r[c][j + 1]),
-                              __uint_as_float(r[c][j + 2]), __uint_as_float(r[c][j + 3]));
+            const int e = n0 + c0 + j;  // E - n0 is a multiple of 8
+            if (e < p.E)
+              *reinterpret_cast<float4*>(row + e) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
           }
-        }
-        if (last && p.wsg) {  // the gate column sits right after the last expert
-          const int col = p.E - n0;
-          float g = 0.f;
-#pragma unroll
-          for (int c = 0; c < 5; ++c)
+          if (gcol >= c0 && gcol < c0 + 16) {
+            float g = 0.f;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              if (c * 16 + j == col) g = __uint_as_float(r[c][j]);
-          p.gate_logit[t] = g;
-          if (p.row_weight) p.row_weight[(size_t)p.T * p.k + t] = 1.f / (1.f + expf(-g));
+              if (c0 + j == gcol) g = v[j];
+            p.gate_logit[t] = g;
+            if (p.row_weight) p.row_weight[(size_t)p.T * p.k + t] = 1.f / (1.f + expf(-g));
+          }
         }
       }
     }
@@ -303,9 +304,8 @@ cudaError_t router_launch(const RouterParams& p, cudaStream_t s) {
   const int rem = p.E - (kp.n_tiles - 1) * kRBn;  // experts in the last tile (8..64)
   kp.n_last = ((rem + (gate ? 1 : 0)) + 15) / 16 * 16;
   const int n_max = std::max(kp.n_tiles > 1 ? kRBn : 0, kp.n_last);
-  kp.b_stride = (uint32_t)n_max * 128u;
-  kp.stage_bytes = kRATile + 3 * kp.b_stride;
-  kp.tmem_cols = n_max > 64 ? 128 : 64;
+  kp.stage_bytes = kRATile + 3 * (uint32_t)n_max * 128u;
+  kp.tmem_cols = 3 * n_max > 128 ? 256 : 3 * n_max > 64 ? 128 : 64;
   if (!make_bf16_map(&kp.tm_x, p.x, p.T, p.d, kRTM)) return cudaErrorInvalidValue;
   if (!make_bf16_map(&kp.tm_wl, p.wsplit, 3LL * Ep, p.d, kp.n_last)) return cudaErrorInvalidValue;
   if (kp.n_tiles > 1 && !make_bf16_map(&kp.tm_w, p.wsplit, 3LL * Ep, p.d, kRBn))

@@ -102,12 +102,16 @@ def test_forward_T32768_zipf(orc, host_layer, dev_layers):
 
 
 def test_forward_small_shapes(orc):
-    """Ragged everything: 1 token, odd token counts, no shared expert, k = E."""
+    """Ragged everything: 1 token, odd token counts, no shared expert, k = E, and router
+    widths that leave a partial last expert tile (64-expert tiles; the gate column rides
+    on the last one) with and without the shared expert."""
     from bit_moe_expert_route_gb300 import ops
     from bit_moe_expert_route_gb300.synth import LayerShape
     cases = [(LayerShape(d_model=256, n_experts=32, top_k=4, d_ff=128, d_ff_shared=128), 1, True),
              (LayerShape(d_model=384, n_experts=16, top_k=3, d_ff=256, d_ff_shared=256), 77, True),
-             (LayerShape(d_model=256, n_experts=8, top_k=8, d_ff=128, d_ff_shared=128), 50, False)]
+             (LayerShape(d_model=256, n_experts=8, top_k=8, d_ff=128, d_ff_shared=128), 50, False),
+             (LayerShape(d_model=128, n_experts=72, top_k=2, d_ff=128, d_ff_shared=128), 130, True),
+             (LayerShape(d_model=640, n_experts=136, top_k=5, d_ff=128, d_ff_shared=128), 3, False)]
     for shape, T, shared in cases:
         host = synth.layer_weights(shape, seed=T, shared=shared)
         fwd = ops.Forward(ops.DeviceLayer(host, shape), T)
@@ -116,6 +120,11 @@ def test_forward_small_shapes(orc):
         torch.cuda.synchronize()
         assert ops.device_status(fwd.ws) == 0
         lg = to_np(fwd.view("logits", (T, shape.n_experts), torch.float32))
+        ref_lg, ref_gl = orc.router(x, host["router"], host["shared_gate"])
+        np.testing.assert_allclose(lg, ref_lg, rtol=1e-5, atol=2e-5)
+        if shared:
+            gl = to_np(fwd.view("gate_logit", (T,), torch.float32))
+            np.testing.assert_allclose(gl, ref_gl, rtol=1e-5, atol=2e-5)
         ref = orc.moe_forward(x, host, shape, logits_in=lg)
         acc = to_np(fwd.view("out_acc", (T, shape.d_model), torch.float32))
         ok, info = tolerance_check(acc, ref["out"])
