@@ -62,10 +62,9 @@ struct Cfg {
   static constexpr int kSQ = QK == 1 ? 4 : 2;      // packed-code stages
   static constexpr int kQStage = kQBytes * QK;     // bytes per matrix per stage
   static constexpr int kCH = BN < 32 ? BN : 32;  // epilogue chunk: token columns per pass
-  // Epilogue staging: two buffers of kCH token rows x 128 outputs
-  // (fp32 for COMBINE, 16-bit for SWIGLU), plus per-row scale and output row.
-  static constexpr int kStageElem = EPI == MOE_EPI_COMBINE ? 4 : EPI == MOE_EPI_SWIGLU ? 2 : 0;
-  static constexpr int kEpiBytes = 2 * kCH * kTileM * kStageElem;
+  // Epilogue staging (COMBINE only): two buffers of kCH token rows x 128
+  // fp32 outputs, plus per-row scale and output row.
+  static constexpr int kEpiBytes = EPI == MOE_EPI_COMBINE ? 2 * kCH * kTileM * 4 : 0;
   static constexpr int kRowInfoBytes = EPI == MOE_EPI_COMBINE ? 2 * BN * 4 : 0;
   // Rings: packed codes (TMA), dequantised A tiles (dequant warps), token
   // tiles B (gather warps or TMA). B tiles are small, so B runs deepest: it
@@ -101,6 +100,7 @@ struct Cfg {
                                    : kTmemCols0 <= 128 ? 128 : kTmemCols0 <= 256 ? 256 : 512;
   static_assert(kSB >= 3, "not enough shared memory for three token-tile stages");
   static_assert(kTmemCols0 <= 512, "accumulators and A stages exceed TMEM");
+  static_assert(!kATmem || kACol + kSA * kAColsStage <= 512, "A stages past the end of TMEM");
   static_assert(kSmem <= 232448, "shared memory per CTA exceeded");
 };
 
@@ -568,20 +568,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
           ++arrived;
         }
       }
+      // End of the tile: signal its last steps as soon as they land. Deferring
+      // them behind the next tile's first issues would hold the MMA until the
+      // next tile's block-map entry and row indices have come back from memory
+      // (several thousand cycles per tile, seen in per-role timestamps).
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      for (; arrived < it; ++arrived) mbar_arrive_warp(&b_full[arrived % C::kSB]);
     }
     cp_async_wait<0>();
     fence_proxy_async_smem();
     for (; arrived < it; ++arrived) mbar_arrive_warp(&b_full[arrived % C::kSB]);
   } else if (warp >= 12) {
     // ------------------------------------------------------------ epilogue
-    // TMEM -> registers -> (NONE) direct fp32 stores, or (SWIGLU, COMBINE) a
-    // staging tile of CH token rows x the tile's 128 outputs shared by the 4
-    // epilogue warps (each fills its 32 outputs), double buffered, written
-    // back one whole token row per TMA bulk copy: a plain store (SWIGLU) or an
-    // fp32 add into the token's output row at L2 (COMBINE, the weighted
-    // combine of the routed experts and the shared one). Whole rows keep the
-    // number of bulk operations at one per token row (each has a fixed cost
-    // in the copy engine and at L2).
+    // TMEM -> registers -> (NONE) direct fp32 stores; (SWIGLU) silu(g)*u in
+    // the operand type, stored directly (64 contiguous bytes per warp and
+    // token row); (COMBINE) a staging tile of CH token rows x the tile's 128
+    // outputs shared by the 4 epilogue warps (each fills its 32 outputs),
+    // double buffered, each row added into the token's fp32 output row at L2
+    // by one TMA bulk reduce (the weighted combine of the routed experts and
+    // the shared one). Whole rows keep the number of bulk reductions at one
+    // per token row (each has a fixed cost in the copy engine and at L2).
     const int ew = warp & 3;             // TMEM lane quarter = the warp's 32 outputs
     const int et = threadIdx.x - 384;    // 0..127 inside the epilogue group
     constexpr int CH = C::kCH;
@@ -639,39 +646,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
             static_cast<float*>(g.C)[((int64_t)t.row0 + n) * g.ldc + col0 + lane] =
                 __uint_as_float(v0[i]);
           }
+        } else if constexpr (EPI == MOE_EPI_SWIGLU) {
+          // straight from registers: per token row, the warp's 32 outputs are
+          // 64 contiguous bytes of h (no staging, barriers or bulk copies)
+          uint16_t* hrow = static_cast<uint16_t*>(g.C) + (int64_t)t.row0 * g.ldc + col0 + lane;
+#pragma unroll
+          for (int i = 0; i < CH; ++i) {
+            const int n = c0 + i;
+            if (n >= t.rows) break;
+            const float a = __uint_as_float(v0[i]);
+            hrow[(int64_t)n * g.ldc] = to_operand<F16>(__fdividef(a, 1.f + __expf(-a)) * __uint_as_float(v1[i]));
+          }
         } else {
           const int sb = chunk & 1;
           // the copies issued from this buffer two chunks ago have read it
           if (lane < kRowsPerWarp) bulk_wait_read<1>();
           named_bar_sync(2, 128);
-          if constexpr (EPI == MOE_EPI_COMBINE) {
+          {
             float* S = reinterpret_cast<float*>(stage) + sb * kStage + ew * 32;
 #pragma unroll
             for (int i = 0; i < CH; ++i) S[i * kTileM + lane] = __uint_as_float(v0[i]) * s_rscale[c0 + i];
-          } else {
-            uint16_t* S = reinterpret_cast<uint16_t*>(stage) + sb * kStage + ew * 32;
-#pragma unroll
-            for (int i = 0; i < CH; ++i) {
-              const float a = __uint_as_float(v0[i]);
-              S[i * kTileM + lane] = to_operand<F16>(a / (1.f + __expf(-a)) * __uint_as_float(v1[i]));
-            }
           }
           fence_proxy_async_smem();
           named_bar_sync(2, 128);  // the chunk's rows are complete
           if (lane < kRowsPerWarp) {
             const int i = ew * kRowsPerWarp + lane, n = c0 + i;
             if (n < t.rows) {
-              if constexpr (EPI == MOE_EPI_COMBINE) {
-                const int orow = s_orow[n];
-                const float* src = reinterpret_cast<const float*>(stage) + sb * kStage + i * kTileM;
-                if (orow >= 0)
-                  bulk_reduce_add_f32(static_cast<float*>(g.C) + (int64_t)orow * g.ldc + tcol0, src,
-                                      kTileM * 4);
-              } else {
-                const uint16_t* src = reinterpret_cast<const uint16_t*>(stage) + sb * kStage + i * kTileM;
-                bulk_store(static_cast<uint16_t*>(g.C) + ((int64_t)t.row0 + n) * g.ldc + tcol0, src,
-                           kTileM * 2);
-              }
+              const int orow = s_orow[n];
+              const float* src = reinterpret_cast<const float*>(stage) + sb * kStage + i * kTileM;
+              if (orow >= 0)
+                bulk_reduce_add_f32(static_cast<float*>(g.C) + (int64_t)orow * g.ldc + tcol0, src,
+                                    kTileM * 4);
             }
             bulk_commit();
           }
