@@ -79,10 +79,11 @@ def gemm_call(A, projs, n_groups, N, m, bn, epi, fmt, row_index=None, extra=None
 
 
 @pytest.mark.parametrize("fmt", ["f16", "bf16"])
-@pytest.mark.parametrize("bn", [16, 32, 64, 128])
-def test_integer_exact_none_epilogue(orc, bn, fmt):
+@pytest.mark.parametrize("bn,K", [(16, 512), (32, 512), (64, 512), (128, 512), (32, 192), (128, 320)])
+def test_integer_exact_none_epilogue(orc, bn, K, fmt):
+    """K = 192 and 320: an odd number of 64-wide k-blocks per tile."""
     from bit_moe_expert_route_gb300 import ops
-    E, K, N, T, k = 8, 512, 256, 150, 2
+    E, N, T, k = 8, 256, 150, 2
     q = synth.q4(synth.key(1, 0, 300), E * N * K // 8).reshape(E, N, K // 8)
     s = np.full((E, N, K // 64), 0x3F80, np.uint16)   # 1.0
     b = np.full((E, N, K // 64), 0xC100, np.uint16)   # -8.0
