@@ -433,7 +433,7 @@ CONFIG = {
 # forwards). None where no capture of the current kernel exists.
 TRAFFIC: dict = {
     "decode_layer": 18_132_992,
-    "gemm_T4096": 345_683_200 + 24_180_565 + 231_067_648 + 12_423_168,
+    "gemm_T4096": 345_934_592 + 25_333_333 + 231_090_347 + 12_661_504,
 }
 
 
