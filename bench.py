@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill configurations")
+    ap.add_argument("--no-batch-decode", action="store_true",
+                    help="skip the small-batch decode lines (T = 2, 4, 8 tokens per layer)")
     ap.add_argument("--prefill-iters", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=["decode", "prefill"],
@@ -285,9 +287,68 @@ def run_decode(args, world, peaks):
     )
     if keep:
         res["cpu_baseline"] = decode_cpu_baseline(hosts, shape)
-    del layers, decs, g
+    del decs, g
+    if not args.no_batch_decode:
+        res["decode_batch"] = [run_decode_batch(layers, shape, T, stream, peaks) for T in (2, 4, 8)]
+    del layers
     torch.cuda.empty_cache()
     return res
+
+
+EXPERT_BYTES = 1_769_472       # one expert's packed codes, scales and biases (3 projections)
+ROUTER_BYTES = 2_105_344       # fp32 router [2048][256] and w_sg
+
+
+def run_decode_batch(layers, shape, T, stream, peaks, steps=50, warmup=5):
+    """T tokens per layer through the same 40 layers (moe_decode_batch_w4,
+    PDL-chained in one CUDA graph), fresh tokens each step; bytes per layer
+    count every distinct selected expert once, plus the shared expert and
+    the router."""
+    import numpy as np
+    import torch
+    from bit_moe_expert_route_gb300 import ops, synth
+    d, L = shape.d_model, len(layers)
+    decs = [ops.DecodeBatch(dl, T) for dl in layers]
+    n = warmup + steps
+    xs = torch.empty(n, L, T, d, dtype=torch.int16)
+    for l in range(L):
+        v = synth.tokens(shape, n * T, seed=1, layer=l, tensor=synth.X_DECODE)
+        xs[:, l].copy_(torch.from_numpy(v.view(np.int16)).view(n, T, d))
+    x_dev = xs.cuda()
+    x_stage = torch.empty(L, T, d, dtype=torch.int16, device="cuda")
+    out = torch.empty(L, T, d, dtype=torch.bfloat16, device="cuda")
+
+    def step():
+        for l in range(L):
+            decs[l](x_stage[l], out[l])
+
+    g = gpu_graph(step, stream)
+    with torch.cuda.stream(stream):
+        for s in range(warmup):
+            x_stage.copy_(x_dev[s], non_blocking=True)
+            g.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for s in range(warmup, n):
+            x_stage.copy_(x_dev[s], non_blocking=True)
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    t = e0.elapsed_time(e1) * 1e-3
+    ids = [torch.unique(dec.view("topk_ids", (T, shape.top_k), torch.int32)).numel() for dec in decs]
+    bytes_layer = float(np.mean(ids)) * EXPERT_BYTES + EXPERT_BYTES + ROUTER_BYTES
+    step_s = t / steps
+    achieved = L * bytes_layer / step_s / 1e9
+    del decs, g
+    return dict(T=T, tokens_per_s=round(T * steps / t, 1), ms_per_step=round(step_s * 1e3, 4),
+                us_per_layer=round(step_s / L * 1e6, 2), distinct_experts_per_layer=round(float(np.mean(ids)), 2),
+                roofline=dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
+                              frac=round(achieved / peaks["hbm_gbs"], 4), bytes_per_layer=int(bytes_layer),
+                              kernel="moe_decode_batch_w4: router, top-k + gate/up, down: 3 PDL-chained "
+                                     "launches per layer"),
+                gpu_launches=3 * L * steps)
 
 
 def decode_cpu_baseline(hosts, shape, steps_per_layer=48):
@@ -497,6 +558,8 @@ def main():
     }
     if "cpu_baseline" in res:
         line["cpu_baseline"] = res["cpu_baseline"]
+    if "decode_batch" in res:
+        line["decode_batch"] = res["decode_batch"]
     if prefill:
         line["prefill"] = prefill
     if rank == 0:

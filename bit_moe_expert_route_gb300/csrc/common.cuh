@@ -301,6 +301,17 @@ MOE_DEVINL uint32_t sw128_offset(uint32_t r, uint32_t chunk16) {
 }
 
 // ---------------------------------------------------------------- misc math
+// Order-preserving map of a float onto uint32 (larger value, larger key);
+// -0 is folded onto +0 so that equal values give equal keys. Key 0 (a NaN
+// pattern) is never produced by a logit and marks "nothing left".
+MOE_DEVINL uint32_t order_key(float v) {
+  const uint32_t u = v == 0.f ? 0u : __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+MOE_DEVINL float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 MOE_DEVINL float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
 
 MOE_DEVINL uint32_t lanemask_lt() {

@@ -48,6 +48,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "gemv_dot.cuh"
 #include "kernels.h"
 
 namespace moe {
@@ -84,48 +85,6 @@ MOE_DEVINL void bar_wait(uint64_t* bar, uint32_t parity, int32_t* status, int wh
 }
 
 // ---------------------------------------------------------------- dot products
-// a0 += f_lo * v_lo, a1 += f_hi * v_hi for one pair of 16-bit values.
-template <bool BF16>
-MOE_DEVINL void fma_pair(float& a0, float& a1, uint32_t f, uint32_t v) {
-  if constexpr (BF16)
-    asm("{ .reg .b16 fl, fh, vl, vh;\n\t mov.b32 {fl, fh}, %2;\n\t mov.b32 {vl, vh}, %3;\n\t"
-        "fma.rn.f32.bf16 %0, fl, vl, %0;\n\t fma.rn.f32.bf16 %1, fh, vh, %1; }"
-        : "+f"(a0), "+f"(a1)
-        : "r"(f), "r"(v));
-  else
-    asm("{ .reg .b16 fl, fh, vl, vh;\n\t mov.b32 {fl, fh}, %2;\n\t mov.b32 {vl, vh}, %3;\n\t"
-        "fma.rn.f32.f16 %0, fl, vl, %0;\n\t fma.rn.f32.f16 %1, fh, vh, %1; }"
-        : "+f"(a0), "+f"(a1)
-        : "r"(f), "r"(v));
-}
-
-// a0/a1 += sum over the 8 codes of word w of f_k * v_k, v given as the four
-// pairs (v_i, v_{i+4}), i = 0..3 (vp.x .. vp.w): shifting w puts codes i
-// and i+4 (bits 4i and 16 + 4i) at the two halves' mantissa tops together.
-template <bool BF16>
-MOE_DEVINL void word_fdot(uint32_t w, const uint4& vp, float& a0, float& a1) {
-  if constexpr (BF16) {
-    constexpr uint32_t m = 0x00780078u, one = 0x3F803F80u;
-    fma_pair<true>(a0, a1, ((w << 3) & m) | one, vp.x);
-    fma_pair<true>(a0, a1, ((w >> 1) & m) | one, vp.y);
-    fma_pair<true>(a0, a1, ((w >> 5) & m) | one, vp.z);
-    fma_pair<true>(a0, a1, ((w >> 9) & m) | one, vp.w);
-  } else {
-    constexpr uint32_t m = 0x03C003C0u, one = 0x3C003C00u;
-    fma_pair<false>(a0, a1, ((w << 6) & m) | one, vp.x);
-    fma_pair<false>(a0, a1, ((w << 2) & m) | one, vp.y);
-    fma_pair<false>(a0, a1, ((w >> 2) & m) | one, vp.z);
-    fma_pair<false>(a0, a1, ((w >> 6) & m) | one, vp.w);
-  }
-}
-
-// The four pairs (v_i, v_{i+4}) of 8 consecutive 16-bit values held as 4
-// words (v0 v1), (v2 v3), (v4 v5), (v6 v7).
-MOE_DEVINL uint4 pair_up(uint4 v) {
-  return make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
-                    __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
-}
-
 // 16 s and (b - 16 s) of a group, from bf16 scale/bias bits.
 MOE_DEVINL float2 affine_f(uint16_t sbits, uint16_t bbits) {
   const float s16 = 16.f * bf16_bits_to_f32(sbits);

@@ -61,6 +61,25 @@ cudaError_t router_launch(const RouterParams& p, cudaStream_t s);
 // cuTensorMapEncodeTiled from the driver (null if unavailable).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
+// ---------------------------------------------------------------- small-batch decode
+constexpr int kBatchMaxT = 8;  // tokens per small-batch decode call
+constexpr int kBatchKS = 4;    // router K slices
+struct BatchParams {
+  const uint16_t* x;        // [T][d] bf16
+  moe_weights_t w;
+  int T, d, E, k, f, shared;
+  float* part;              // [kBatchKS][T][E + 1] router partials (column E: the gate)
+  float* logits;            // [T][E]
+  float* gate_logit;        // [T]
+  int32_t* ids;             // [T][k]
+  float* wts;               // [T][k + 1]: routing weights, then the shared gate
+  float* h;                 // [T][k + 1][f] fp32
+  uint16_t* out;            // [T][d] bf16
+  int32_t* status;
+};
+bool batch_shape_supported(int T, int d, int E, int k, int f);
+cudaError_t decode_batch_launch(const BatchParams& p, cudaStream_t s);
+
 // ---------------------------------------------------------------- grouped GEMM
 struct GemmW4 {
   const uint32_t* q;

@@ -139,6 +139,36 @@ DecWs decode_ws(void* ws, const moe_shape_t* s) {
   return r;
 }
 
+struct BatchWs {
+  moe_decode_views_t v;
+  float* wts;   // [T][k + 1]
+  float* part;  // router partials [kBatchKS][T][E + 1]
+  size_t bytes;
+};
+
+BatchWs batch_ws(void* ws, const moe_shape_t* s) {
+  const int T = s->T, E = s->n_experts, k = s->top_k;
+  Carve c(ws);
+  BatchWs r;
+  memset(&r.v, 0, sizeof r.v);
+  r.v.status = c.take<int32_t>(kStatusWords);
+  r.v.logits = c.take<float>((size_t)T * E);
+  r.v.gate_logit = c.take<float>(T);
+  r.v.topk_ids = c.take<int32_t>((size_t)T * k);
+  r.wts = c.take<float>((size_t)T * (k + 1));
+  r.v.topk_w = r.wts;
+  r.v.h = c.take<float>((size_t)T * (k + 1) * s->d_ff);
+  r.part = c.take<float>((size_t)moe::kBatchKS * T * (E + 1));
+  r.bytes = c.off;
+  return r;
+}
+
+bool batch_shape_ok(const moe_shape_t* s) {
+  return shape_ok(s, true) && moe::batch_shape_supported(s->T, s->d_model, s->n_experts, s->top_k,
+                                                          s->d_ff);
+}
+
+
 bool w4_ok(const moe_w4_t& w) {
   return w.q && w.scale && w.bias && aligned(w.q, 16) && aligned(w.scale, 16) &&
          aligned(w.bias, 16);
@@ -501,6 +531,52 @@ int moe_decode_gemv_w4(const uint16_t* x, const moe_weights_t* w, const moe_shap
   p.pub_h = dw.pub_h;
   p.sync = dw.sync;
   return cuda_status(moe::decode_launch(p, s));
+}
+
+size_t moe_decode_batch_workspace_bytes(const moe_shape_t* shape) {
+  if (!batch_shape_ok(shape)) return 0;
+  return batch_ws(nullptr, shape).bytes;
+}
+
+int moe_decode_batch_views(void* ws, size_t ws_bytes, const moe_shape_t* shape,
+                           moe_decode_views_t* views) {
+  if (!batch_shape_ok(shape)) return MOE_ERR_SHAPE;
+  if (!views) return MOE_ERR_NULL;
+  const BatchWs bw = batch_ws(ws, shape);
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < bw.bytes) return MOE_ERR_WORKSPACE;
+  *views = bw.v;
+  return MOE_OK;
+}
+
+int moe_decode_batch_w4(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* shape,
+                        uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+  if (!batch_shape_ok(shape)) return MOE_ERR_SHAPE;
+  int rc = check_weights(w, shape);
+  if (rc != MOE_OK) return rc;
+  if (!x || !out) return MOE_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(out, 2)) return MOE_ERR_ALIGN;
+  const BatchWs bw = batch_ws(ws, shape);
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < bw.bytes) return MOE_ERR_WORKSPACE;
+  if ((rc = check_device()) != MOE_OK) return rc;
+  moe::BatchParams p;
+  memset(&p, 0, sizeof p);
+  p.x = x;
+  p.w = *w;
+  p.T = shape->T;
+  p.d = shape->d_model;
+  p.E = shape->n_experts;
+  p.k = shape->top_k;
+  p.f = shape->d_ff;
+  p.shared = w->shared_gate != nullptr;
+  p.part = bw.part;
+  p.logits = bw.v.logits;
+  p.gate_logit = bw.v.gate_logit;
+  p.ids = bw.v.topk_ids;
+  p.wts = bw.wts;
+  p.h = bw.v.h;
+  p.out = out;
+  p.status = bw.v.status;
+  return cuda_status(moe::decode_batch_launch(p, static_cast<cudaStream_t>(stream)));
 }
 
 int moe_get_device_status(const void* ws, void* stream, int32_t* device_status) {

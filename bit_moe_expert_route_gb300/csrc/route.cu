@@ -34,17 +34,6 @@ constexpr uint32_t kFull = 0xFFFFFFFFu;
 template <int NPL>
 constexpr int topk_threads() { return NPL <= 8 ? 1024 : 256; }
 
-// Order-preserving map of a float onto uint32 (larger value, larger key);
-// -0 is folded onto +0 so that equal values give equal keys. Key 0 (a NaN
-// pattern) is never produced by a logit and marks "nothing left".
-MOE_DEVINL uint32_t order_key(float v) {
-  const uint32_t u = v == 0.f ? 0u : __float_as_uint(v);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-MOE_DEVINL float key_value(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
 template <int NPL>  // logits per lane: E <= 32 * NPL
 __global__ void __launch_bounds__(topk_threads<NPL>()) route_topk_kernel(RouteParams p) {
   constexpr int kW = topk_threads<NPL>() / 32;

@@ -93,6 +93,10 @@ def lib():
         L.moe_decode_views.argtypes = [vp, sz, vp, vp]
         L.moe_decode_gemv_w4.argtypes = [vp, vp, vp, vp, vp, sz, vp]
         L.moe_decode_gemv_w4_noalloc.argtypes = [vp, vp, vp, vp, vp]
+        L.moe_decode_batch_workspace_bytes.restype = sz
+        L.moe_decode_batch_workspace_bytes.argtypes = [vp]
+        L.moe_decode_batch_views.argtypes = [vp, sz, vp, vp]
+        L.moe_decode_batch_w4.argtypes = [vp, vp, vp, vp, vp, sz, vp]
         L.moe_get_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
         _lib = L
     return _lib
@@ -278,6 +282,38 @@ class Forward:
         n = int(np.prod(shape))
         nbytes = n * torch.empty((), dtype=dtype).element_size()
         return self.ws[off:off + nbytes].view(dtype).view(*shape)
+
+
+class DecodeBatch:
+    """moe_decode_batch_w4 (1 <= T <= 8 tokens) with a reusable workspace."""
+
+    def __init__(self, layer: DeviceLayer, T: int, device="cuda"):
+        self.layer, self.T = layer, T
+        self.shape = Shape.of(layer.shape, T)
+        nbytes = lib().moe_decode_batch_workspace_bytes(ctypes.byref(self.shape))
+        if nbytes == 0:
+            raise MoeError("moe_decode_batch_workspace_bytes", -3)
+        self.ws = workspace(nbytes, device)
+        self.views = DecodeViews()
+        _check("moe_decode_batch_views", lib().moe_decode_batch_views(
+            _p(self.ws), self.ws.numel(), ctypes.byref(self.shape), ctypes.byref(self.views)))
+
+    def view(self, name: str, shape, dtype) -> torch.Tensor:
+        """A workspace array (logits [T][E], gate_logit [T], topk_ids [T][k],
+        topk_w [T][k+1] with the shared gate last, h fp32 [T][k+1][d_ff])."""
+        off = getattr(self.views, name) - self.ws.data_ptr()
+        n = int(np.prod(shape))
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return self.ws[off:off + nbytes].view(dtype).view(*shape)
+
+    def __call__(self, x: torch.Tensor, out: torch.Tensor | None = None, stream=None):
+        if out is None:
+            out = torch.empty(self.T, self.layer.shape.d_model, dtype=torch.bfloat16, device=x.device)
+        rc = lib().moe_decode_batch_w4(_p(x), ctypes.byref(self.layer.weights),
+                                       ctypes.byref(self.shape), _p(out), _p(self.ws),
+                                       self.ws.numel(), _stream(stream))
+        _check("moe_decode_batch_w4", rc)
+        return out
 
 
 class Decode:

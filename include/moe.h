@@ -290,6 +290,34 @@ int moe_decode_gemv_w4_noalloc(const uint16_t* x, const moe_weights_t* w,
                                const moe_shape_t* shape, uint16_t* out, void* stream);
 
 /*
+ * moe_decode_batch_w4: a small batch of tokens (1 <= shape->T <= 8, e.g. a
+ * speculative-decoding verification batch whose tokens select different
+ * experts) through the layer with matrix-vector work, as in
+ * moe_decode_gemv_w4 ("Why prefill and decode get different treatment"):
+ * the router, the shared expert and each selected expert's rows are read
+ * once per call and applied to every token that uses them. Three kernel
+ * launches chained by programmatic dependent launch; no waits between
+ * blocks, so the call shares the GPU with other work.
+ *   x bf16 [T][d_model] device (16-byte aligned); out bf16 [T][d_model].
+ *   Routing as in moe_forward: top_k by logit (plus router_bias), ties to the
+ *   lower id, softmax over the selected; the shared expert (if any) scaled by
+ *   sigmoid(x . shared_gate).
+ *   Shapes: d_model, d_ff multiples of 128, n_experts <= 1024, top_k <= 32,
+ *   and the per-block staging (about T*d_model*2 and T*(top_k+1)*d_ff*2
+ *   bytes) within 200 KB; otherwise MOE_ERR_SHAPE.
+ *   ws 256-byte aligned, >= moe_decode_batch_workspace_bytes(shape) bytes (no
+ *   initialisation needed). Calls on one workspace must not overlap on the GPU.
+ */
+size_t moe_decode_batch_workspace_bytes(const moe_shape_t* shape);
+int moe_decode_batch_w4(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* shape,
+                        uint16_t* out, void* ws, size_t ws_bytes, void* stream);
+/* Views of a batch-decode workspace, every array with a leading [T]: logits
+ * [T][E], gate_logit [T], topk_ids [T][k], topk_w [T][k + 1] (the shared
+ * gate last), h fp32 [T][k + 1][d_ff]. */
+int moe_decode_batch_views(void* ws, size_t ws_bytes, const moe_shape_t* shape,
+                           moe_decode_views_t* views);
+
+/*
  * Reads the device status word of a workspace (synchronises `stream`).
  * *device_status receives a moe_device_status value.
  */

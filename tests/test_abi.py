@@ -68,6 +68,11 @@ def test_workspace_sizes(L):
     assert L.moe_workspace_bytes(ctypes.byref(bad), 128) == 0
     assert L.moe_workspace_bytes(ctypes.byref(sh), 48) == 0  # block_n 48 unsupported
     assert L.moe_decode_workspace_bytes(ctypes.byref(ops.Shape.of(LayerShape(), 1))) > 0
+    for T, ok in ((1, True), (4, True), (8, True), (9, False), (0, False)):
+        n = L.moe_decode_batch_workspace_bytes(ctypes.byref(ops.Shape.of(LayerShape(), T)))
+        assert (n > 0) == ok, T
+        if ok:  # logits, gate, ids, weights, h of every token
+            assert n >= T * (256 * 4 + 4 + 8 * 4 + 9 * 4 + 9 * 512 * 4)
     assert L.moe_route_workspace_bytes(32768, 256) >= 256 * 256 * 4
 
 
