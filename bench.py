@@ -490,11 +490,13 @@ CONFIG = {
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch unit, from the ncu captures
 # summarised under profiles/: the decode kernel on one layer (cold cache: all of its
-# weights come from HBM), and both grouped GEMMs of one T = 4096 forward (mean of three
-# forwards). None where no capture of the current kernel exists.
+# weights come from HBM), and both grouped GEMMs of one forward at T = 512, 4096 and
+# 32768 (mean of three forwards). None where no capture of the current kernel exists.
 TRAFFIC: dict = {
     "decode_layer": 18_132_992,
+    "gemm_T512": 307_492_437 + 3_958_528 + 160_701_013 + 271_872,
     "gemm_T4096": 345_934_592 + 25_333_333 + 231_090_347 + 12_661_504,
+    "gemm_T32768": 1_174_975_744 + 286_252_117 + 2_231_807_659 + 1_943_127_808,
 }
 
 
