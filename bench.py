@@ -46,9 +46,10 @@ def parse():
                     help="skip the small-batch decode lines (T = 2, 4, 8 tokens per layer)")
     ap.add_argument("--prefill-iters", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["decode", "prefill"],
+    ap.add_argument("--profile", choices=["decode", "prefill", "decode-batch"],
                     help="no measurement: run one layer repeatedly (decode: 20 + 200 calls; prefill: "
-                         "3 forwards at --profile-T tokens) for a profiler to attach to")
+                         "3 forwards at --profile-T tokens; decode-batch: 8 calls at each of "
+                         "T = 2, 4, 8) for a profiler to attach to")
     ap.add_argument("--profile-T", type=int, default=4096)
     return ap.parse_args()
 
@@ -514,6 +515,12 @@ def profile_run(args):
         out = torch.empty(shape.d_model, dtype=torch.bfloat16, device="cuda")
         for _ in range(220):
             dec(x, out)
+    elif args.profile == "decode-batch":
+        for T in (2, 4, 8):
+            dec = ops.DecodeBatch(dl, T)
+            x = torch.from_numpy(synth.tokens(shape, T, seed=1, tensor=synth.X_DECODE).view(np.int16)).cuda()
+            for _ in range(8):
+                dec(x)
     else:
         T = args.profile_T
         fwd = ops.Forward(dl, T)
