@@ -198,9 +198,11 @@ int moe_grouped_gemm_w4a16(const uint16_t* A, int64_t A_rows, int K, const int32
  *   x    bf16 [T][d_model] device;  out bf16 [T][d_model] device.
  *   block_n  row-tile height (16/32/64/128) or 0 for moe_pick_block_n.
  *   ws   256-byte aligned, >= moe_workspace_bytes(shape, block_n) bytes.
- * Pipeline: router GEMM (also writing an f16 copy of x) -> top-k + shared
- * gate -> histogram -> scan -> scatter + block map -> grouped GEMM (gate/up +
- * SwiGLU) -> grouped GEMM (down + weighted combine) -> bf16 output.
+ * Pipeline: router and shared-gate logits on the tensor cores (the fp32
+ * router weights split exactly into three bf16 planes in the workspace on
+ * every call; fp32 accumulation; also writing an f16 copy of x) -> top-k ->
+ * histogram -> scan -> scatter + block map -> grouped GEMM (gate/up + SwiGLU)
+ * -> grouped GEMM (down + weighted combine) -> bf16 output.
  * The grouped GEMMs use f16 tensor-core operands (MOE_OPERAND_F16): x, the
  * dequantised weights and the intermediate h are f16 (11-bit significand),
  * accumulation is fp32. x, the weights and h must lie within the f16 range.
