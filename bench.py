@@ -407,8 +407,12 @@ def run_prefill(T, zipf, host0, args, peaks):
     g1 = gpu_graph(lambda: ops.grouped_gemm_w4a16(
         x16, [t["gate"], t["up"]], E, f, bm, nt, mt, bn, ops.EPI_SWIGLU, row_index=rt, n_rows=rows,
         W_extra=[t["sh_gate"], t["sh_up"]], C=h), stream)
+    # the down projection runs on its own (taller) tile map at large T
+    mt2, bn2 = fwd.views.down_max_tiles, fwd.views.down_block_n
+    bm2 = fwd.view("down_block_map", (mt2, 4), torch.int32)
+    nt2 = fwd.view("down_num_tiles", (1,), torch.int32)
     g2 = gpu_graph(lambda: ops.grouped_gemm_w4a16(
-        h, [t["down"]], E, d, bm, nt, mt, bn, ops.EPI_COMBINE, n_rows=rows,
+        h, [t["down"]], E, d, bm2, nt2, mt2, bn2, ops.EPI_COMBINE, n_rows=rows,
         W_extra=[t["sh_down"]], row_scale=rw, out_row=rt, C=acc), stream)
     t1 = statistics.median(timed_replays(g1, stream, args.prefill_iters, flush))
     t2 = statistics.median(timed_replays(g2, stream, args.prefill_iters, flush))
@@ -497,7 +501,7 @@ TRAFFIC: dict = {
     "decode_layer": 18_132_992,
     "gemm_T512": 307_492_437 + 3_958_528 + 160_701_013 + 271_872,
     "gemm_T4096": 345_934_592 + 25_333_333 + 231_090_347 + 12_661_504,
-    "gemm_T32768": 1_174_975_744 + 286_252_117 + 2_231_807_659 + 1_943_127_808,
+    "gemm_T32768": None,  # the down projection now runs 256-row tiles at this size
 }
 
 

@@ -749,6 +749,9 @@ cudaError_t launch_bn(const KParams& kp, cudaStream_t s) {
     case 32: return launch_t<32, NMAT, EPI, F16, QK>(kp, s);
     case 64: return launch_t<64, NMAT, EPI, F16, QK>(kp, s);
     case 128: return launch_t<128, NMAT, EPI, F16, QK>(kp, s);
+    case 256:  // one weight matrix only: two 256-column accumulators fill TMEM
+      if constexpr (NMAT == 1) return launch_t<256, NMAT, EPI, F16, QK>(kp, s);
+      return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }

@@ -30,6 +30,10 @@ struct RouteParams {
   int32_t* block_map;      // [max_tiles][4]
   int32_t* num_tiles;      // [1]
   int max_tiles;
+  // optional second block map of the same rows in tiles of block_n2 rows
+  int32_t* block_map2;     // [max_tiles2][4] or null
+  int32_t* num_tiles2;     // [1]
+  int max_tiles2, block_n2;
   // scratch
   int32_t* blk;            // [nblk][E]
   int32_t* status;

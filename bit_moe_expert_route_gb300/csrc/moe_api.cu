@@ -106,6 +106,20 @@ FwdWs forward_ws(void* ws, const moe_shape_t* s, int bn) {
   r.v.num_tiles = c.take<int32_t>(1);
   r.blk = c.take<int32_t>((size_t)moe::route_nblk(T) * E);
   r.wsplit = c.take<uint16_t>((size_t)3 * moe::router_split_rows(E, true) * s->d_model);
+  // 256-row tiles pay off once the experts average 256 rows or more: each
+  // tile's weights are dequantised once for twice the rows (below that they
+  // are mostly padding, and the combine epilogue's per-row copies dominate)
+  // (gate/up stays at 128: its two accumulators fill TMEM at that height)
+  r.v.down_block_n = bn == 128 && (int64_t)T * k >= (int64_t)256 * E ? 256 : bn;
+  if (r.v.down_block_n != bn) {
+    r.v.down_max_tiles = moe_max_tiles(T, E, k, r.v.down_block_n, 1);
+    r.v.down_block_map = c.take<int32_t>((size_t)r.v.down_max_tiles * 4);
+    r.v.down_num_tiles = c.take<int32_t>(1);
+  } else {  // one map serves both projections
+    r.v.down_max_tiles = r.v.max_tiles;
+    r.v.down_block_map = r.v.block_map;
+    r.v.down_num_tiles = r.v.num_tiles;
+  }
   r.v.x16 = c.take<uint16_t>((size_t)T * s->d_model);
   r.v.h = c.take<uint16_t>((size_t)rows * s->d_ff);
   r.v.out_acc = c.take<float>((size_t)T * s->d_model);
@@ -295,7 +309,10 @@ int moe_grouped_gemm_w4a16(const uint16_t* A, int64_t A_rows, int K, const int32
     return MOE_ERR_SHAPE;
   if (operand_format != MOE_OPERAND_BF16 && operand_format != MOE_OPERAND_F16) return MOE_ERR_SHAPE;
   if (K < 64 || K % 64 || N < 128 || N % 128 || n_groups < 1 || A_rows < 0 || n_rows < 0 ||
-      max_tiles < 0 || !valid_block_n(block_n, false) || ldc < N || C_rows < 0)
+      max_tiles < 0 || ldc < N || C_rows < 0)
+    return MOE_ERR_SHAPE;
+  // 256-row tiles hold two 256-column accumulators: one weight matrix only
+  if (!valid_block_n(block_n, false) && !(block_n == 256 && epilogue != MOE_EPI_SWIGLU))
     return MOE_ERR_SHAPE;
   if (epilogue != MOE_EPI_COMBINE && C_rows < n_rows) return MOE_ERR_SHAPE;
   // SWIGLU and COMBINE write 16-byte token-row segments (bulk copies)
@@ -428,6 +445,12 @@ int moe_forward(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* sh
   rp.max_tiles = v.max_tiles;
   rp.blk = fw.blk;
   rp.status = v.status;
+  if (v.down_block_map != v.block_map) {  // a second map for the down projection
+    rp.block_map2 = v.down_block_map;
+    rp.num_tiles2 = v.down_num_tiles;
+    rp.max_tiles2 = v.down_max_tiles;
+    rp.block_n2 = v.down_block_n;
+  }
   if ((rc = cuda_status(moe::route_launch(rp, s))) != MOE_OK) return rc;
   // 3. gate/up grouped GEMM with SwiGLU -> h (rows in expert order, shared rows last)
   moe::GemmParams g;
@@ -468,6 +491,10 @@ int moe_forward(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* sh
   g2.X[0] = shared ? moe::GemmW4{w->sh_down.q, w->sh_down.scale, w->sh_down.bias} : moe::GemmW4{};
   g2.X[1] = {};
   g2.N = d;
+  g2.block_map = v.down_block_map;
+  g2.num_tiles = v.down_num_tiles;
+  g2.max_tiles = v.down_max_tiles;
+  g2.block_n = v.down_block_n;
   g2.epilogue = MOE_EPI_COMBINE;
   g2.row_scale = v.row_weight;
   g2.out_row = v.row_token;

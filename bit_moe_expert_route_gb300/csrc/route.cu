@@ -137,6 +137,53 @@ __device__ int block_exclusive_scan_1024(int v, int* total) {
   return r;
 }
 
+// Block map of the routed rows (expert after expert) and the shared rows in
+// tiles of bn rows: {group, first row, rows, 0} per tile, num_tiles on the
+// device. Every thread of the 1024-thread block calls it; `total` is the
+// thread's expert's row count, s_off / s_cnt the experts' offsets and counts.
+__device__ void build_block_map(const RouteParams& p, int bn, int total, const int* s_off,
+                                const int* s_cnt, int* s_toff, int* s_tiles, int32_t* block_map,
+                                int32_t* num_tiles, int max_tiles, int where) {
+  const int e = threadIdx.x;
+  const int nt = e < p.E ? (total + bn - 1) / bn : 0;
+  const int toff = block_exclusive_scan_1024(nt, s_tiles);
+  if (e < p.E) s_toff[e] = toff;
+  if (e == 0) s_toff[p.E] = *s_tiles;
+  __syncthreads();
+  const int routed_tiles = *s_tiles;
+  const int shared_tiles = p.with_shared ? (p.T + bn - 1) / bn : 0;
+  int num = routed_tiles + shared_tiles;
+  if (num > max_tiles) {
+    if (e == 0) report(p.status, MOE_DEV_BAD_TILE, where, num);
+    num = max_tiles;
+  }
+  if (e == 0) *num_tiles = num;
+  const int kT = p.T * p.k;
+  for (int i = e; i < num; i += blockDim.x) {
+    int4 m;
+    if (i < routed_tiles) {
+      // last expert g with s_toff[g] <= i (experts without tiles share offsets)
+      int lo = 0, hi = p.E - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_toff[mid] <= i) lo = mid; else hi = mid - 1;
+      }
+      const int j = i - s_toff[lo];
+      m.x = lo;
+      m.y = s_off[lo] + j * bn;
+      m.z = min(bn, s_cnt[lo] - j * bn);
+    } else {
+      const int j = i - routed_tiles;
+      m.x = p.E;
+      m.y = kT + j * bn;
+      m.z = min(bn, p.T - j * bn);
+    }
+    m.w = 0;
+    reinterpret_cast<int4*>(block_map)[i] = m;
+  }
+  __syncthreads();  // s_toff and s_tiles are reused by a second call
+}
+
 __global__ void __launch_bounds__(1024) route_scan_kernel(RouteParams p, int nblk) {
   __shared__ int s_off[1025];
   __shared__ int s_cnt[1024];
@@ -164,43 +211,12 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(RouteParams p, int nbl
     p.offsets[p.E] = s_total;
     s_off[p.E] = s_total;
   }
-  const int bn = p.block_n;
-  const int nt = e < p.E ? (total + bn - 1) / bn : 0;
-  const int toff = block_exclusive_scan_1024(nt, &s_tiles);
-  if (e < p.E) s_toff[e] = toff;
-  if (e == 0) s_toff[p.E] = s_tiles;
   __syncthreads();
-  const int routed_tiles = s_tiles;
-  const int shared_tiles = p.with_shared ? (p.T + bn - 1) / bn : 0;
-  int num = routed_tiles + shared_tiles;
-  if (num > p.max_tiles) {
-    if (e == 0) report(p.status, MOE_DEV_BAD_TILE, 11, num);
-    num = p.max_tiles;
-  }
-  if (e == 0) *p.num_tiles = num;
-  const int kT = p.T * p.k;
-  for (int i = e; i < num; i += blockDim.x) {
-    int4 m;
-    if (i < routed_tiles) {
-      // last expert g with s_toff[g] <= i (experts without tiles share offsets)
-      int lo = 0, hi = p.E - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_toff[mid] <= i) lo = mid; else hi = mid - 1;
-      }
-      const int j = i - s_toff[lo];
-      m.x = lo;
-      m.y = s_off[lo] + j * bn;
-      m.z = min(bn, s_cnt[lo] - j * bn);
-    } else {
-      const int j = i - routed_tiles;
-      m.x = p.E;
-      m.y = kT + j * bn;
-      m.z = min(bn, p.T - j * bn);
-    }
-    m.w = 0;
-    reinterpret_cast<int4*>(p.block_map)[i] = m;
-  }
+  build_block_map(p, p.block_n, total, s_off, s_cnt, s_toff, &s_tiles, p.block_map, p.num_tiles,
+                  p.max_tiles, 11);
+  if (p.block_map2)  // the same rows in tiles of block_n2 (a second GEMM's tile height)
+    build_block_map(p, p.block_n2, total, s_off, s_cnt, s_toff, &s_tiles, p.block_map2,
+                    p.num_tiles2, p.max_tiles2, 13);
 }
 
 __global__ void __launch_bounds__(kThreads) route_scatter_kernel(RouteParams p) {

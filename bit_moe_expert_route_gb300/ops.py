@@ -53,7 +53,9 @@ class ForwardViews(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "logits", "gate_logit", "topk_ids", "topk_w", "counts", "offsets", "perm", "inv_perm",
         "row_token", "row_weight", "block_map", "num_tiles", "x16", "h", "out_acc", "status")] + [
-        ("max_tiles", ctypes.c_int32), ("block_n", ctypes.c_int32)]
+        ("max_tiles", ctypes.c_int32), ("block_n", ctypes.c_int32),
+        ("down_block_map", ctypes.c_void_p), ("down_num_tiles", ctypes.c_void_p),
+        ("down_max_tiles", ctypes.c_int32), ("down_block_n", ctypes.c_int32)]
 
 
 class DecodeViews(ctypes.Structure):

@@ -181,7 +181,7 @@ int moe_route(const float* logits, const float* logit_bias, int T, int n_experts
  *               SWIGLU needs ldc % 8 == 0, COMBINE ldc % 4 == 0.
  *   N           output columns (multiple of 128); K multiple of 64.
  *   ws          256-byte aligned, >= moe_gemm_workspace_bytes() bytes.
- * block_n in {16, 32, 64, 128}.
+ * block_n in {16, 32, 64, 128}, or 256 for NONE and COMBINE (one weight matrix).
  */
 size_t moe_gemm_workspace_bytes(void);
 int moe_grouped_gemm_w4a16(const uint16_t* A, int64_t A_rows, int K, const int32_t* row_index,
@@ -230,7 +230,14 @@ typedef struct {
   float* out_acc;      /* fp32 [T][d_model] */
   int32_t* status;     /* device status word */
   int32_t max_tiles;
-  int32_t block_n;
+  int32_t block_n;     /* gate/up row-tile height */
+  /* The down projection's block map. Equal to block_map/num_tiles/max_tiles
+     unless block_n is 128 and T*top_k >= 256*n_experts: the down projection
+     (one weight matrix) then runs on 256-row tiles of a second map. */
+  int32_t* down_block_map;
+  int32_t* down_num_tiles;
+  int32_t down_max_tiles;
+  int32_t down_block_n;
 } moe_forward_views_t;
 int moe_forward_views(void* ws, size_t ws_bytes, const moe_shape_t* shape, int block_n,
                       moe_forward_views_t* views);

@@ -76,6 +76,32 @@ def test_workspace_sizes(L):
     assert L.moe_route_workspace_bytes(32768, 256) >= 256 * 256 * 4
 
 
+def test_forward_views_pick_the_down_tile_map(L):
+    """The down projection gets a second, 256-row block map only when gate/up runs
+    128-row tiles and the experts average 256 or more rows; otherwise both
+    projections share one map. (The views only carve a workspace: host memory
+    serves here.)"""
+    from bit_moe_expert_route_gb300 import ops
+    from bit_moe_expert_route_gb300.synth import LayerShape
+    for T, bn, separate in ((32768, 128, True), (8192, 128, True), (8191, 128, False),
+                            (32768, 64, False), (4096, 128, False)):
+        sh = ops.Shape.of(LayerShape(), T)
+        n = L.moe_workspace_bytes(ctypes.byref(sh), bn)
+        buf = ctypes.create_string_buffer(n + 256)
+        base = (ctypes.addressof(buf) + 255) // 256 * 256
+        v = ops.ForwardViews()
+        assert L.moe_forward_views(ctypes.c_void_p(base), n, ctypes.byref(sh), bn,
+                                   ctypes.byref(v)) == 0
+        assert v.block_n == bn
+        if separate:
+            assert v.down_block_n == 256 and v.down_block_map != v.block_map
+            assert v.down_max_tiles == L.moe_max_tiles(T, 256, 8, 256, 1)
+            assert base <= v.down_block_map and v.down_num_tiles + 4 <= base + n
+        else:
+            assert (v.down_block_n, v.down_max_tiles) == (bn, v.max_tiles)
+            assert (v.down_block_map, v.down_num_tiles) == (v.block_map, v.num_tiles)
+
+
 def test_bad_arguments_are_rejected_on_the_host(L):
     vp = ctypes.c_void_p
     fake = vp(0x10000)  # never dereferenced: every call below fails validation first

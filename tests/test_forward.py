@@ -68,6 +68,13 @@ def run_layer(orc, host_layer, dev_layers, T, zipf, block_n=0):
     nt = int(to_np(fwd.view("num_tiles", (1,), torch.int32))[0])
     assert nt == m["num_tiles"]
     assert np.array_equal(to_np(fwd.view("block_map", (nt, 4), torch.int32)), m["block_map"])
+    v = fwd.views
+    if v.down_block_map != v.block_map:  # the down projection's own, taller tiles
+        m2 = orc.route_meta(ids, E, v.down_block_n, True)
+        nt2 = int(to_np(fwd.view("down_num_tiles", (1,), torch.int32))[0])
+        assert nt2 == m2["num_tiles"] <= v.down_max_tiles
+        assert np.array_equal(to_np(fwd.view("down_block_map", (nt2, 4), torch.int32)),
+                              m2["block_map"])
     # 3. layer output
     ref = orc.moe_forward(x[idx], host, FULL, logits_in=lg[idx])
     assert np.array_equal(ref["ids"], ids[idx])

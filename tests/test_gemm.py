@@ -79,7 +79,8 @@ def gemm_call(A, projs, n_groups, N, m, bn, epi, fmt, row_index=None, extra=None
 
 
 @pytest.mark.parametrize("fmt", ["f16", "bf16"])
-@pytest.mark.parametrize("bn,K", [(16, 512), (32, 512), (64, 512), (128, 512), (32, 192), (128, 320)])
+@pytest.mark.parametrize("bn,K", [(16, 512), (32, 512), (64, 512), (128, 512), (256, 512),
+                                  (32, 192), (128, 320), (256, 192)])
 def test_integer_exact_none_epilogue(orc, bn, K, fmt):
     """K = 192 and 320: an odd number of 64-wide k-blocks per tile."""
     from bit_moe_expert_route_gb300 import ops
@@ -151,7 +152,7 @@ def test_swiglu_epilogue_with_shared_group(orc, bn, fmt):
     assert np.max(np.abs(err) / (np.abs(ref) + 1e-2 * np.sqrt(np.mean(ref ** 2)))) < 5 * tol
 
 
-@pytest.mark.parametrize("fmt,bn", [("f16", 32), ("bf16", 64)])
+@pytest.mark.parametrize("fmt,bn", [("f16", 32), ("bf16", 64), ("f16", 256)])
 def test_combine_epilogue(orc, bn, fmt):
     from bit_moe_expert_route_gb300 import ops
     shape = LayerShape(d_model=512, n_experts=8, top_k=3, d_ff=256, d_ff_shared=256)
