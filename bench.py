@@ -501,7 +501,7 @@ TRAFFIC: dict = {
     "decode_layer": 18_132_992,
     "gemm_T512": 307_492_437 + 3_958_528 + 160_701_013 + 271_872,
     "gemm_T4096": 345_934_592 + 25_333_333 + 231_090_347 + 12_661_504,
-    "gemm_T32768": None,  # the down projection now runs 256-row tiles at this size
+    "gemm_T32768": 1_175_549_525 + 287_004_501 + 2_233_447_339 + 1_945_131_691,
 }
 
 
