@@ -416,6 +416,13 @@ def run_prefill(T, zipf, host0, args, peaks):
         W_extra=[t["sh_down"]], row_scale=rw, out_row=rt, C=acc), stream)
     t1 = statistics.median(timed_replays(g1, stream, args.prefill_iters, flush))
     t2 = statistics.median(timed_replays(g2, stream, args.prefill_iters, flush))
+    # the same layer with MOE_FWD_DETERMINISTIC (fixed-order combine)
+    fwd_det = ops.Forward(dl, T, deterministic=True)
+    gd = gpu_graph(lambda: fwd_det(x, out), stream)
+    for _ in range(3):
+        gd.replay()
+    t_det = statistics.median(timed_replays(gd, stream, args.prefill_iters, flush))
+    del gd, fwd_det
     f1 = 2 * 2 * d * f * rows
     f2 = 2 * f * d * rows
     achieved = (f1 + f2) / (t1 + t2) / 1e12
@@ -424,6 +431,7 @@ def run_prefill(T, zipf, host0, args, peaks):
     res = dict(
         T=T, router_bias="zipf 1.5*ln(1/rank)" if zipf else None, block_n=bn,
         tokens_per_s=round(T / t_layer, 1), ms=round(t_layer * 1e3, 4),
+        deterministic_ms=round(t_det * 1e3, 4),
         layer_tflops=round(FLOP_PER_TOKEN * T / t_layer / 1e12, 2),
         layer_frac_of_bf16_peak=round(FLOP_PER_TOKEN * T / t_layer / 1e12 / peaks["bf16"], 4),
         weights_hbm_frac=round(weight_bytes / t_layer / 1e9 / peaks["hbm_gbs"], 4),

@@ -271,6 +271,50 @@ __global__ void f32_to_bf16_kernel(const float4* __restrict__ in, uint2* __restr
   }
 }
 
+// Deterministic combine of the down projection's per-row outputs y [rows][d]
+// (unweighted; rows in expert order, the shared rows last): for every token t
+// and output column, acc = 0, then acc = w * y[row] + acc (one fused
+// multiply-add) for the token's routed rows in slot order j = 0..k-1 (row
+// inv_perm[t*k + j], weight row_weight[row]) and last for its shared row
+// T*k + t (weight = the sigmoid gate). The order is fixed, so the result does
+// not depend on how the GEMM scheduled its tiles. Writes the fp32 sum and its
+// bf16 rounding. One float4 of one token per thread, d/4 threads per token.
+__global__ void combine_rows_kernel(const float4* __restrict__ y, const int32_t* __restrict__ inv_perm,
+                                    const float* __restrict__ row_weight, int T, int k, int d4,
+                                    int shared, float4* __restrict__ acc_out,
+                                    uint2* __restrict__ out, int32_t* status) {
+  const int64_t n = (int64_t)T * d4, rows_routed = (int64_t)T * k;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / d4), c = (int)(i - (int64_t)t * d4);
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j <= k; ++j) {
+      int64_t r;
+      if (j < k) {
+        r = __ldg(inv_perm + (int64_t)t * k + j);
+        if (r < 0 || r >= rows_routed) {
+          report(status, MOE_DEV_BAD_ROW, 60, (int)r);
+          continue;
+        }
+      } else {
+        if (!shared) break;
+        r = rows_routed + t;
+      }
+      const float w = __ldg(row_weight + r);
+      const float4 v = __ldcs(y + r * d4 + c);  // read once: stream past L2
+      a.x = fmaf(w, v.x, a.x);
+      a.y = fmaf(w, v.y, a.y);
+      a.z = fmaf(w, v.z, a.z);
+      a.w = fmaf(w, v.w, a.w);
+    }
+    acc_out[i] = a;
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
+    out[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo),
+                        *reinterpret_cast<const uint32_t*>(&hi));
+  }
+}
+
 // bf16 tensor [rows][cols] (row stride cols), box 64 columns x box_rows, 128-byte swizzle.
 bool make_bf16_map(CUtensorMap* tm, const uint16_t* base, int64_t rows, int cols, int box_rows) {
   auto fn = tensor_map_encoder();
@@ -326,6 +370,22 @@ cudaError_t f32_to_bf16_launch(const float* in, uint16_t* out, int64_t n, cudaSt
   const int64_t blocks = std::min<int64_t>((n4 + 255) / 256, (int64_t)sms * 8);
   f32_to_bf16_kernel<<<(int)std::max<int64_t>(blocks, 1), 256, 0, s>>>(
       reinterpret_cast<const float4*>(in), reinterpret_cast<uint2*>(out), n4);
+  return cudaGetLastError();
+}
+
+cudaError_t combine_rows_launch(const float* y, const int32_t* inv_perm, const float* row_weight,
+                                int T, int k, int d, bool shared, float* acc, uint16_t* out,
+                                int32_t* status, cudaStream_t s) {
+  if (T < 1) return cudaSuccess;
+  if (d % 4) return cudaErrorInvalidValue;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t n = (int64_t)T * (d / 4);
+  const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)sms * 8);
+  combine_rows_kernel<<<(int)std::max<int64_t>(blocks, 1), 256, 0, s>>>(
+      reinterpret_cast<const float4*>(y), inv_perm, row_weight, T, k, d / 4, shared ? 1 : 0,
+      reinterpret_cast<float4*>(acc), reinterpret_cast<uint2*>(out), status);
   return cudaGetLastError();
 }
 

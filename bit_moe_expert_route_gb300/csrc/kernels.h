@@ -120,6 +120,13 @@ cudaError_t gemm_w4_launch(const GemmParams& p, cudaStream_t s);
 // ---------------------------------------------------------------- elementwise
 cudaError_t f32_to_bf16_launch(const float* in, uint16_t* out, int64_t n, cudaStream_t s);
 
+// Deterministic combine: acc[t] = sum, in slot order (routed slots, then the
+// shared row when `shared`), of row_weight[row] * y[row], fp32 fused
+// multiply-adds; out = bf16 RNE of acc. y [T*k (+T)][d] fp32, d % 4 == 0.
+cudaError_t combine_rows_launch(const float* y, const int32_t* inv_perm, const float* row_weight,
+                                int T, int k, int d, bool shared, float* acc, uint16_t* out,
+                                int32_t* status, cudaStream_t s);
+
 // ---------------------------------------------------------------- decode
 struct DecodeParams {
   const uint16_t* x;        // [d]

@@ -83,7 +83,7 @@ struct FwdWs {
   size_t bytes;
 };
 
-FwdWs forward_ws(void* ws, const moe_shape_t* s, int bn) {
+FwdWs forward_ws(void* ws, const moe_shape_t* s, int bn, int flags) {
   const int T = s->T, E = s->n_experts, k = s->top_k;
   const int64_t rows = (int64_t)T * k + T;
   Carve c(ws);
@@ -123,9 +123,13 @@ FwdWs forward_ws(void* ws, const moe_shape_t* s, int bn) {
   r.v.x16 = c.take<uint16_t>((size_t)T * s->d_model);
   r.v.h = c.take<uint16_t>((size_t)rows * s->d_ff);
   r.v.out_acc = c.take<float>((size_t)T * s->d_model);
+  // deterministic mode: the down projection's unweighted output rows
+  r.v.y = (flags & MOE_FWD_DETERMINISTIC) ? c.take<float>((size_t)rows * s->d_model) : nullptr;
   r.bytes = c.off;
   return r;
 }
+
+bool flags_ok(int flags) { return (flags & ~MOE_FWD_DETERMINISTIC) == 0; }
 
 struct DecWs {
   moe_decode_views_t v;
@@ -365,28 +369,43 @@ int moe_grouped_gemm_w4a16(const uint16_t* A, int64_t A_rows, int K, const int32
   return cuda_status(moe::gemm_w4_launch(p, s));
 }
 
-size_t moe_workspace_bytes(const moe_shape_t* shape, int block_n) {
-  if (!shape_ok(shape, false)) return 0;
+size_t moe_workspace_bytes_ex(const moe_shape_t* shape, int block_n, int flags) {
+  if (!shape_ok(shape, false) || !flags_ok(flags)) return 0;
   if (block_n == 0) block_n = moe_pick_block_n(shape->T, shape->n_experts, shape->top_k);
   if (!valid_block_n(block_n, false)) return 0;
-  return forward_ws(nullptr, shape, block_n).bytes;
+  return forward_ws(nullptr, shape, block_n, flags).bytes;
 }
 
-int moe_forward_views(void* ws, size_t ws_bytes, const moe_shape_t* shape, int block_n,
-                      moe_forward_views_t* views) {
-  if (!shape_ok(shape, false)) return MOE_ERR_SHAPE;
+size_t moe_workspace_bytes(const moe_shape_t* shape, int block_n) {
+  return moe_workspace_bytes_ex(shape, block_n, 0);
+}
+
+int moe_forward_views_ex(void* ws, size_t ws_bytes, const moe_shape_t* shape, int block_n,
+                         int flags, moe_forward_views_t* views) {
+  if (!shape_ok(shape, false) || !flags_ok(flags)) return MOE_ERR_SHAPE;
   if (block_n == 0) block_n = moe_pick_block_n(shape->T, shape->n_experts, shape->top_k);
   if (!valid_block_n(block_n, false)) return MOE_ERR_SHAPE;
   if (!views) return MOE_ERR_NULL;
-  const FwdWs fw = forward_ws(ws, shape, block_n);
+  const FwdWs fw = forward_ws(ws, shape, block_n, flags);
   if (!ws || !aligned(ws, kAlign) || ws_bytes < fw.bytes) return MOE_ERR_WORKSPACE;
   *views = fw.v;
   return MOE_OK;
 }
 
+int moe_forward_views(void* ws, size_t ws_bytes, const moe_shape_t* shape, int block_n,
+                      moe_forward_views_t* views) {
+  return moe_forward_views_ex(ws, ws_bytes, shape, block_n, 0, views);
+}
+
 int moe_forward(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* shape, int block_n,
                 uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
-  if (!shape_ok(shape, false)) return MOE_ERR_SHAPE;
+  return moe_forward_ex(x, w, shape, block_n, 0, out, ws, ws_bytes, stream);
+}
+
+int moe_forward_ex(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* shape,
+                   int block_n, int flags, uint16_t* out, void* ws, size_t ws_bytes,
+                   void* stream) {
+  if (!shape_ok(shape, false) || !flags_ok(flags)) return MOE_ERR_SHAPE;
   if (block_n == 0) block_n = moe_pick_block_n(shape->T, shape->n_experts, shape->top_k);
   if (!valid_block_n(block_n, false)) return MOE_ERR_SHAPE;
   const int T = shape->T, E = shape->n_experts, k = shape->top_k, d = shape->d_model,
@@ -395,7 +414,7 @@ int moe_forward(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* sh
   if (rc != MOE_OK) return rc;
   if (T > 0 && (!x || !out)) return MOE_ERR_NULL;
   if (!aligned(x, 16) || !aligned(out, 16)) return MOE_ERR_ALIGN;
-  const FwdWs fw = forward_ws(ws, shape, block_n);
+  const FwdWs fw = forward_ws(ws, shape, block_n, flags);
   if (!ws || !aligned(ws, kAlign) || ws_bytes < fw.bytes) return MOE_ERR_WORKSPACE;
   if ((rc = check_device()) != MOE_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -479,8 +498,11 @@ int moe_forward(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* sh
   g.ldc = f;
   g.status = v.status;
   if ((rc = cuda_status(moe::gemm_w4_launch(g, s))) != MOE_OK) return rc;
-  // 4. down grouped GEMM, weighted combine into the fp32 accumulator
-  if ((rc = cuda_status(cudaMemsetAsync(v.out_acc, 0, (size_t)T * d * 4, s))) != MOE_OK) return rc;
+  // 4. down grouped GEMM, weighted combine into the fp32 accumulator (or, in
+  // deterministic mode, every row's output stored for a fixed-order sum)
+  const bool det = v.y != nullptr;
+  if (!det && (rc = cuda_status(cudaMemsetAsync(v.out_acc, 0, (size_t)T * d * 4, s))) != MOE_OK)
+    return rc;
   moe::GemmParams g2 = g;
   g2.A = v.h;
   g2.A_rows = rows;
@@ -501,8 +523,18 @@ int moe_forward(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* sh
   g2.C = v.out_acc;
   g2.C_rows = T;
   g2.ldc = d;
+  if (det) {
+    g2.epilogue = MOE_EPI_NONE;
+    g2.row_scale = nullptr;
+    g2.out_row = nullptr;
+    g2.C = v.y;
+    g2.C_rows = rows;
+  }
   if ((rc = cuda_status(moe::gemm_w4_launch(g2, s))) != MOE_OK) return rc;
   // 5. bf16 output
+  if (det)
+    return cuda_status(moe::combine_rows_launch(v.y, v.inv_perm, v.row_weight, T, k, d, shared,
+                                                v.out_acc, out, v.status, s));
   return cuda_status(moe::f32_to_bf16_launch(v.out_acc, out, (int64_t)T * d, s));
 }
 

@@ -55,7 +55,8 @@ class ForwardViews(ctypes.Structure):
         "row_token", "row_weight", "block_map", "num_tiles", "x16", "h", "out_acc", "status")] + [
         ("max_tiles", ctypes.c_int32), ("block_n", ctypes.c_int32),
         ("down_block_map", ctypes.c_void_p), ("down_num_tiles", ctypes.c_void_p),
-        ("down_max_tiles", ctypes.c_int32), ("down_block_n", ctypes.c_int32)]
+        ("down_max_tiles", ctypes.c_int32), ("down_block_n", ctypes.c_int32),
+        ("y", ctypes.c_void_p)]
 
 
 class DecodeViews(ctypes.Structure):
@@ -90,6 +91,10 @@ def lib():
         L.moe_workspace_bytes.argtypes = [vp, i32]
         L.moe_forward_views.argtypes = [vp, sz, vp, i32, vp]
         L.moe_forward.argtypes = [vp, vp, vp, i32, vp, vp, sz, vp]
+        L.moe_workspace_bytes_ex.restype = sz
+        L.moe_workspace_bytes_ex.argtypes = [vp, i32, i32]
+        L.moe_forward_views_ex.argtypes = [vp, sz, vp, i32, i32, vp]
+        L.moe_forward_ex.argtypes = [vp, vp, vp, i32, i32, vp, vp, sz, vp]
         L.moe_decode_workspace_bytes.restype = sz
         L.moe_decode_workspace_bytes.argtypes = [vp]
         L.moe_decode_views.argtypes = [vp, sz, vp, vp]
@@ -250,31 +255,37 @@ def grouped_gemm_w4a16(A, W, n_groups, N, block_map, num_tiles, max_tiles_, bloc
     return C, ws
 
 
-class Forward:
-    """moe_forward with a reusable workspace for one (shape, T, block_n)."""
+FWD_DETERMINISTIC = 1
 
-    def __init__(self, layer: DeviceLayer, T: int, block_n: int = 0, device="cuda"):
+
+class Forward:
+    """moe_forward_ex with a reusable workspace for one (shape, T, block_n, flags);
+    deterministic=True sets MOE_FWD_DETERMINISTIC (fixed-order combine)."""
+
+    def __init__(self, layer: DeviceLayer, T: int, block_n: int = 0, device="cuda",
+                 deterministic: bool = False):
         self.layer = layer
         self.T = T
         self.shape = Shape.of(layer.shape, T)
         self.block_n = block_n or pick_block_n(T, layer.shape.n_experts, layer.shape.top_k)
-        nbytes = lib().moe_workspace_bytes(ctypes.byref(self.shape), self.block_n)
+        self.flags = FWD_DETERMINISTIC if deterministic else 0
+        nbytes = lib().moe_workspace_bytes_ex(ctypes.byref(self.shape), self.block_n, self.flags)
         if nbytes == 0:
-            raise MoeError("moe_workspace_bytes", -3)
+            raise MoeError("moe_workspace_bytes_ex", -3)
         self.ws = workspace(nbytes, device)
         self.views = ForwardViews()
-        _check("moe_forward_views", lib().moe_forward_views(
-            _p(self.ws), self.ws.numel(), ctypes.byref(self.shape), self.block_n,
+        _check("moe_forward_views_ex", lib().moe_forward_views_ex(
+            _p(self.ws), self.ws.numel(), ctypes.byref(self.shape), self.block_n, self.flags,
             ctypes.byref(self.views)))
 
     def __call__(self, x: torch.Tensor, out: torch.Tensor | None = None, stream=None):
         if out is None:
             out = torch.empty(self.T, self.layer.shape.d_model, dtype=torch.bfloat16,
                               device=x.device)
-        rc = lib().moe_forward(_p(x), ctypes.byref(self.layer.weights), ctypes.byref(self.shape),
-                               self.block_n, _p(out), _p(self.ws), self.ws.numel(),
-                               _stream(stream))
-        _check("moe_forward", rc)
+        rc = lib().moe_forward_ex(_p(x), ctypes.byref(self.layer.weights),
+                                  ctypes.byref(self.shape), self.block_n, self.flags, _p(out),
+                                  _p(self.ws), self.ws.numel(), _stream(stream))
+        _check("moe_forward_ex", rc)
         return out
 
     def view(self, name: str, shape, dtype) -> torch.Tensor:

@@ -211,6 +211,26 @@ size_t moe_workspace_bytes(const moe_shape_t* shape, int block_n);
 int moe_forward(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* shape, int block_n,
                 uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * moe_forward_ex: moe_forward with option flags; flags 0 is moe_forward.
+ * MOE_FWD_DETERMINISTIC makes the output reproducible bit for bit from run
+ * to run: the down grouped GEMM stores every row's (unweighted) output, fp32
+ * [T*top_k + T][d_model] in the workspace, instead of adding it into the
+ * token's accumulator at L2 (whose order of fp32 additions varies between
+ * runs), and one more kernel sums each token's rows in slot order (routed
+ * slots 0..top_k-1 by descending logit, then the shared expert), one fp32
+ * fused multiply-add per row, and rounds the sum to bf16. It costs the y
+ * rows' bytes in the workspace (2.4 GB at T = 32768, d_model 2048) and one
+ * write and one read of them per call. Other flag bits return MOE_ERR_SHAPE.
+ * moe_workspace_bytes_ex / moe_forward_views_ex take the same flags (the
+ * views' y is set only with MOE_FWD_DETERMINISTIC).
+ */
+#define MOE_FWD_DETERMINISTIC 1
+size_t moe_workspace_bytes_ex(const moe_shape_t* shape, int block_n, int flags);
+int moe_forward_ex(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* shape,
+                   int block_n, int flags, uint16_t* out, void* ws, size_t ws_bytes,
+                   void* stream);
+
 /* Device pointers of moe_forward's intermediates inside its workspace. */
 typedef struct {
   float* logits;       /* [T][E] router logits (without router_bias) */
@@ -238,9 +258,15 @@ typedef struct {
   int32_t* down_num_tiles;
   int32_t down_max_tiles;
   int32_t down_block_n;
+  /* MOE_FWD_DETERMINISTIC only (else NULL): fp32 [T*k + T][d_model], row r =
+     h row r . W_down^T of its expert, unweighted; out_acc then holds the
+     fixed-order weighted sum. */
+  float* y;
 } moe_forward_views_t;
 int moe_forward_views(void* ws, size_t ws_bytes, const moe_shape_t* shape, int block_n,
                       moe_forward_views_t* views);
+int moe_forward_views_ex(void* ws, size_t ws_bytes, const moe_shape_t* shape, int block_n,
+                         int flags, moe_forward_views_t* views);
 
 /*
  * moe_decode_gemv_w4: one token (shape->T == 1) through the layer with

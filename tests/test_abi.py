@@ -74,6 +74,12 @@ def test_workspace_sizes(L):
         if ok:  # logits, gate, ids, weights, h of every token
             assert n >= T * (256 * 4 + 4 + 8 * 4 + 9 * 4 + 9 * 512 * 4)
     assert L.moe_route_workspace_bytes(32768, 256) >= 256 * 256 * 4
+    # the deterministic mode adds the down projection's rows, fp32 [9T][d]
+    n_det = L.moe_workspace_bytes_ex(ctypes.byref(sh), 128, 1)
+    assert n_det >= L.moe_workspace_bytes(ctypes.byref(sh), 128) + (T * k + T) * d * 4
+    assert L.moe_workspace_bytes_ex(ctypes.byref(sh), 128, 0) == L.moe_workspace_bytes(
+        ctypes.byref(sh), 128)
+    assert L.moe_workspace_bytes_ex(ctypes.byref(sh), 128, 2) == 0  # unknown flag
 
 
 def test_forward_views_pick_the_down_tile_map(L):
@@ -92,7 +98,7 @@ def test_forward_views_pick_the_down_tile_map(L):
         v = ops.ForwardViews()
         assert L.moe_forward_views(ctypes.c_void_p(base), n, ctypes.byref(sh), bn,
                                    ctypes.byref(v)) == 0
-        assert v.block_n == bn
+        assert v.block_n == bn and not v.y
         if separate:
             assert v.down_block_n == 256 and v.down_block_map != v.block_map
             assert v.down_max_tiles == L.moe_max_tiles(T, 256, 8, 256, 1)
@@ -100,6 +106,29 @@ def test_forward_views_pick_the_down_tile_map(L):
         else:
             assert (v.down_block_n, v.down_max_tiles) == (bn, v.max_tiles)
             assert (v.down_block_map, v.down_num_tiles) == (v.block_map, v.num_tiles)
+
+
+def test_deterministic_views(L):
+    """The deterministic workspace keeps every other intermediate where moe_forward
+    puts it and adds y [T*k + T][d] fp32 at its end."""
+    from bit_moe_expert_route_gb300 import ops
+    from bit_moe_expert_route_gb300.synth import LayerShape
+    T, k, d = 512, 8, 2048
+    sh = ops.Shape.of(LayerShape(), T)
+    n = L.moe_workspace_bytes_ex(ctypes.byref(sh), 0, 1)
+    buf = ctypes.create_string_buffer(n + 256)
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    v0, v1 = ops.ForwardViews(), ops.ForwardViews()
+    assert L.moe_forward_views_ex(ctypes.c_void_p(base), n, ctypes.byref(sh), 0, 0,
+                                  ctypes.byref(v0)) == 0
+    assert L.moe_forward_views_ex(ctypes.c_void_p(base), n, ctypes.byref(sh), 0, 1,
+                                  ctypes.byref(v1)) == 0
+    for name in ("logits", "h", "out_acc", "block_map", "inv_perm", "row_weight"):
+        assert getattr(v0, name) == getattr(v1, name), name
+    assert not v0.y and v1.y >= v1.out_acc + T * d * 4
+    assert v1.y + (T * k + T) * d * 4 <= base + n
+    assert L.moe_forward_views_ex(ctypes.c_void_p(base), n - 256, ctypes.byref(sh), 0, 1,
+                                  ctypes.byref(v1)) == -4  # too small for y
 
 
 def test_bad_arguments_are_rejected_on_the_host(L):

@@ -42,10 +42,10 @@ def sample_tokens(T, n=48, seed=0):
     return np.unique(np.concatenate([[0, 1, T - 1], rng]))
 
 
-def run_layer(orc, host_layer, dev_layers, T, zipf, block_n=0):
+def run_layer(orc, host_layer, dev_layers, T, zipf, block_n=0, deterministic=False):
     from bit_moe_expert_route_gb300 import ops
     host = dict(host_layer, router_bias=synth.zipf_router_bias(FULL.n_experts) if zipf else None)
-    fwd = ops.Forward(dev_layers[zipf], T, block_n)
+    fwd = ops.Forward(dev_layers[zipf], T, block_n, deterministic=deterministic)
     x = synth.tokens(FULL, T, seed=0)
     out = fwd(torch.from_numpy(x.view(np.int16)).cuda())
     torch.cuda.synchronize()
@@ -178,3 +178,40 @@ def test_forward_repeatable(dev_layers, T, bn):
     assert ops.device_status(fwd.ws) == 0
     for h in hs[1:]:
         assert torch.equal(h, hs[0])
+
+
+@pytest.mark.parametrize("T,zipf,bn", [(64, False, 0), (512, False, 0), (4096, False, 0),
+                                       (4096, False, 64), (32768, True, 0)])
+def test_forward_deterministic(orc, host_layer, dev_layers, T, zipf, bn):
+    """MOE_FWD_DETERMINISTIC: the same parity bar, on the fixed-order fp32 sum
+    (out_acc) and on its bf16 rounding."""
+    run_layer(orc, host_layer, dev_layers, T, zipf, bn, deterministic=True)
+
+
+def test_forward_deterministic_is_bit_reproducible(dev_layers):
+    """Run to run, the deterministic output and its fp32 sum are identical bit for
+    bit; so they are across row-tile heights (64, 128 and the 256-row down map at
+    T = 8192), since each output element is the same MMA accumulation over K and
+    the same fixed-order sum. The default mode's fp32 adds at L2 agree only within
+    rounding."""
+    from bit_moe_expert_route_gb300 import ops
+    T = 8192
+    x = torch.from_numpy(synth.tokens(FULL, T, seed=5).view(np.int16)).cuda()
+    outs, accs = [], []
+    for bn in (128, 128, 64):
+        fwd = ops.Forward(dev_layers[False], T, bn, deterministic=True)
+        if bn == 128:
+            assert fwd.views.down_block_n == 256  # the taller down tiles at this size
+        outs.append(fwd(x).view(torch.int16).clone())
+        torch.cuda.synchronize()
+        assert ops.device_status(fwd.ws) == 0
+        accs.append(fwd.view("out_acc", (T, FULL.d_model), torch.int32).clone())
+        del fwd
+    for o, a in zip(outs[1:], accs[1:]):
+        assert torch.equal(o, outs[0])
+        assert torch.equal(a, accs[0])
+    fast = ops.Forward(dev_layers[False], T)(x)
+    torch.cuda.synchronize()
+    det = outs[0].view(torch.bfloat16).float()
+    assert (fast.float() - det).abs().max().item() <= 1e-2 * det.abs().max().item()
+
