@@ -32,8 +32,8 @@ int cuda_status(cudaError_t e) {
   return MOE_ERR_CUDA;
 }
 
-bool valid_block_n(int bn, bool route) {
-  return bn == 16 || bn == 32 || bn == 64 || bn == 128 || (route && bn == 256);
+bool valid_block_n(int bn) {
+  return bn == 16 || bn == 32 || bn == 64 || bn == 128 || bn == 256;
 }
 
 // Sequential workspace carve-out.
@@ -258,7 +258,7 @@ int moe_route(const float* logits, const float* logit_bias, int T, int n_experts
               float* row_weight, int32_t* block_map, int32_t* num_tiles, int max_tiles, void* ws,
               size_t ws_bytes, void* stream) {
   if (T < 0 || n_experts < 1 || n_experts > 1024 || top_k < 1 || top_k > 32 ||
-      top_k > n_experts || !valid_block_n(block_n, true) || (int64_t)T * (top_k + 1) >= (1 << 30))
+      top_k > n_experts || !valid_block_n(block_n) || (int64_t)T * (top_k + 1) >= (1 << 30))
     return MOE_ERR_SHAPE;
   if (!counts || !offsets || !num_tiles) return MOE_ERR_NULL;
   if (T > 0 && (!logits || !topk_ids || !topk_w || !perm || !inv_perm || !row_token || !block_map))
@@ -316,7 +316,7 @@ int moe_grouped_gemm_w4a16(const uint16_t* A, int64_t A_rows, int K, const int32
       max_tiles < 0 || ldc < N || C_rows < 0)
     return MOE_ERR_SHAPE;
   // 256-row tiles hold two 256-column accumulators: one weight matrix only
-  if (!valid_block_n(block_n, false) && !(block_n == 256 && epilogue != MOE_EPI_SWIGLU))
+  if (!valid_block_n(block_n) || (block_n == 256 && epilogue == MOE_EPI_SWIGLU))
     return MOE_ERR_SHAPE;
   if (epilogue != MOE_EPI_COMBINE && C_rows < n_rows) return MOE_ERR_SHAPE;
   // SWIGLU and COMBINE write 16-byte token-row segments (bulk copies)
@@ -372,7 +372,7 @@ int moe_grouped_gemm_w4a16(const uint16_t* A, int64_t A_rows, int K, const int32
 size_t moe_workspace_bytes_ex(const moe_shape_t* shape, int block_n, int flags) {
   if (!shape_ok(shape, false) || !flags_ok(flags)) return 0;
   if (block_n == 0) block_n = moe_pick_block_n(shape->T, shape->n_experts, shape->top_k);
-  if (!valid_block_n(block_n, false)) return 0;
+  if (!valid_block_n(block_n) || block_n == 256) return 0;  // gate/up: 128 rows at most
   return forward_ws(nullptr, shape, block_n, flags).bytes;
 }
 
@@ -384,7 +384,7 @@ int moe_forward_views_ex(void* ws, size_t ws_bytes, const moe_shape_t* shape, in
                          int flags, moe_forward_views_t* views) {
   if (!shape_ok(shape, false) || !flags_ok(flags)) return MOE_ERR_SHAPE;
   if (block_n == 0) block_n = moe_pick_block_n(shape->T, shape->n_experts, shape->top_k);
-  if (!valid_block_n(block_n, false)) return MOE_ERR_SHAPE;
+  if (!valid_block_n(block_n) || block_n == 256) return MOE_ERR_SHAPE;
   if (!views) return MOE_ERR_NULL;
   const FwdWs fw = forward_ws(ws, shape, block_n, flags);
   if (!ws || !aligned(ws, kAlign) || ws_bytes < fw.bytes) return MOE_ERR_WORKSPACE;
@@ -407,7 +407,7 @@ int moe_forward_ex(const uint16_t* x, const moe_weights_t* w, const moe_shape_t*
                    void* stream) {
   if (!shape_ok(shape, false) || !flags_ok(flags)) return MOE_ERR_SHAPE;
   if (block_n == 0) block_n = moe_pick_block_n(shape->T, shape->n_experts, shape->top_k);
-  if (!valid_block_n(block_n, false)) return MOE_ERR_SHAPE;
+  if (!valid_block_n(block_n) || block_n == 256) return MOE_ERR_SHAPE;
   const int T = shape->T, E = shape->n_experts, k = shape->top_k, d = shape->d_model,
             f = shape->d_ff;
   int rc = check_weights(w, shape);

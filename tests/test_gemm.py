@@ -122,11 +122,15 @@ def test_one_hot_reads_back_dequantised_weights(orc, fmt):
         assert np.array_equal(got[g].T, deq(orc, (q, s, b), g, fmt).astype(np.float32)), g
 
 
-@pytest.mark.parametrize("fmt,bn", [("f16", 16), ("f16", 128), ("bf16", 64)])
-def test_swiglu_epilogue_with_shared_group(orc, bn, fmt):
+@pytest.mark.parametrize("fmt,bn,T,E,k,K", [
+    ("f16", 16, 333, 16, 4, 1024), ("f16", 128, 333, 16, 4, 1024), ("bf16", 64, 333, 16, 4, 1024),
+    # experts with 2-3 tiles and ragged last tiles (the MMA's N follows the
+    # tile's rows); K/64 not a multiple of 4 (one k-block per packed-code stage)
+    ("f16", 128, 700, 8, 3, 1024), ("f16", 128, 333, 16, 4, 320)])
+def test_swiglu_epilogue_with_shared_group(orc, bn, fmt, T, E, k, K):
     from bit_moe_expert_route_gb300 import ops
-    shape = LayerShape(d_model=1024, n_experts=16, top_k=4, d_ff=256, d_ff_shared=256)
-    T, E, k, K, N = 333, 16, 4, 1024, 256
+    shape = LayerShape(d_model=K, n_experts=16, top_k=4, d_ff=256, d_ff_shared=256)
+    N = 256
     w = synth.layer_weights(shape, seed=9)
     X = round_fmt(synth.bf16_to_f32(synth.tokens(shape, T, seed=9)), fmt)
     ids, m = routing(orc, T, E, k, bn, seed=9 + bn)
