@@ -46,9 +46,10 @@ def parse():
                     help="skip the small-batch decode lines (T = 2, 4, 8 tokens per layer)")
     ap.add_argument("--prefill-iters", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["decode", "prefill", "decode-batch"],
+    ap.add_argument("--profile", choices=["decode", "prefill", "prefill-det", "decode-batch"],
                     help="no measurement: run one layer repeatedly (decode: 20 + 200 calls; prefill: "
-                         "3 forwards at --profile-T tokens; decode-batch: 8 calls at each of "
+                         "3 forwards at --profile-T tokens; prefill-det: the same with "
+                         "MOE_FWD_DETERMINISTIC; decode-batch: 8 calls at each of "
                          "T = 2, 4, 8) for a profiler to attach to")
     ap.add_argument("--profile-T", type=int, default=4096)
     return ap.parse_args()
@@ -535,7 +536,7 @@ def profile_run(args):
                 dec(x)
     else:
         T = args.profile_T
-        fwd = ops.Forward(dl, T)
+        fwd = ops.Forward(dl, T, deterministic=args.profile == "prefill-det")
         x = torch.from_numpy(synth.tokens(shape, T, seed=0).view(np.int16)).cuda()
         for _ in range(3):
             fwd(x)
