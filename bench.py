@@ -46,6 +46,7 @@ def parse():
                     help="skip the small-batch decode lines (T = 2, 4, 8 tokens per layer)")
     ap.add_argument("--prefill-iters", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-gdn", action="store_true", help="skip the Gated DeltaNet scan lines")
     ap.add_argument("--profile", choices=["decode", "prefill", "prefill-det", "decode-batch"],
                     help="no measurement: run one layer repeatedly (decode: 20 + 200 calls; prefill: "
                          "3 forwards at --profile-T tokens; prefill-det: the same with "
@@ -149,9 +150,10 @@ def measured_peaks():
             m = json.load(f)
         return dict(hbm_gbs=float(m["hbm_gbs"]), bf16=float(m["bf16_tflops"]),
                     bf16_sustained=float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
-                    source="measured")
+                    sm_max_mhz=float(m.get("sm_max_mhz", 2070.0)), source="measured")
     except (OSError, KeyError, ValueError):
-        return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+        return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sustained=1700.0, sm_max_mhz=2070.0,
+                    source="fallback")
 
 
 # ------------------------------------------------------------------ helpers
@@ -295,6 +297,80 @@ def run_decode(args, world, peaks):
     del layers
     torch.cuda.empty_cache()
     return res
+
+
+# Gated DeltaNet layer shape (a reading: the pages give no sizes; 16 key/query heads
+# and 32 value heads of 128, as in the public Qwen3-Next-style configuration with
+# d_model 2048); the model has 30 such layers.
+GDN_SHAPE = dict(Hk=16, Hv=32, dk=128, dv=128)
+GDN_LAYERS = 30
+
+
+def run_gdn(args, peaks):
+    """moe_gdn_scan on seeded synthetic inputs (unit-norm bf16 q and k, N(0,1) bf16 v,
+    alpha in [0.8, 1), beta in [0, 1), fp32 state): prefill, one scan over T = 4096
+    tokens; decode, one token through each of 30 layers (distinct states) captured in one
+    CUDA graph. L2 flushed before every timed replay."""
+    import torch
+    from bit_moe_expert_route_gb300 import ops
+    Hk, Hv, dk, dv = (GDN_SHAPE[n] for n in ("Hk", "Hv", "dk", "dv"))
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    stream = torch.cuda.Stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+
+    def make(T):
+        def unit(*shape):
+            a = torch.randn(*shape, device="cuda", generator=gen)
+            return (a / a.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+        q, k = unit(T, Hk, dk), unit(T, Hk, dk)
+        v = torch.randn(T, Hv, dv, device="cuda", generator=gen).to(torch.bfloat16)
+        al = 0.8 + 0.2 * torch.rand(T, Hv, device="cuda", generator=gen)
+        be = torch.rand(T, Hv, device="cuda", generator=gen)
+        S = 0.1 * torch.randn(Hv, dv, dk, device="cuda", generator=gen)
+        return q, k, v, al, be, S, torch.empty(T, Hv, dv, device="cuda")
+
+    T = 4096
+    q, k, v, al, be, S, out = make(T)
+    g = gpu_graph(lambda: ops.gdn_scan(q, k, v, al, be, S, out=out), stream)
+    for _ in range(3):
+        g.replay()
+    t_pre = statistics.median(timed_replays(g, stream, args.prefill_iters, flush))
+    flop = 6 * T * Hv * dv * dk  # three multiply-adds per state entry per token
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    fp32_peak = sms * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+    state_bytes = Hv * dv * dk * 4
+    layers = [make(1) for _ in range(GDN_LAYERS)]
+
+    def step():
+        for lq, lk, lv, la, lb, lS, lo in layers:
+            ops.gdn_scan(lq, lk, lv, la, lb, lS, out=lo)
+    gd = gpu_graph(step, stream)
+    for _ in range(3):
+        gd.replay()
+    t_dec = statistics.median(timed_replays(gd, stream, args.prefill_iters, flush)) / GDN_LAYERS
+    dec_gbs = 2 * state_bytes / t_dec / 1e9
+    del g, gd, layers, flush
+    torch.cuda.empty_cache()
+    return dict(
+        shape=dict(GDN_SHAPE, layers=GDN_LAYERS),
+        prefill=dict(T=T, ms=round(t_pre * 1e3, 4), tokens_per_s=round(T / t_pre, 1),
+                     roofline=dict(bound="alu", achieved=round(flop / t_pre / 1e12, 2),
+                                   peak=round(fp32_peak, 1), unit="TFLOP/s",
+                                   frac=round(flop / t_pre / 1e12 / fp32_peak, 4),
+                                   flop_per_token=6 * Hv * dv * dk,
+                                   kernel="gdn_scan_kernel: one warp per state row, the row in "
+                                          "registers for all T tokens",
+                                   peak_source="SM count x 128 fp32 lanes x 2 x max SM clock")),
+        decode=dict(us_per_layer=round(t_dec * 1e6, 3),
+                    tokens_per_s_30_layers=round(1 / (t_dec * GDN_LAYERS), 1),
+                    roofline=dict(bound="hbm", achieved=round(dec_gbs, 1), peak=peaks["hbm_gbs"],
+                                  unit="GB/s", frac=round(dec_gbs / peaks["hbm_gbs"], 4),
+                                  bytes_per_layer=2 * state_bytes,
+                                  kernel="gdn_scan_kernel at T = 1: the state read and written "
+                                         "once per layer")),
+        gpu_launches_per_decode_step=GDN_LAYERS,
+        l2="flushed (512 MB write) before every timed replay",
+    )
 
 
 EXPERT_BYTES = 1_769_472       # one expert's packed codes, scales and biases (3 projections)
@@ -569,6 +645,7 @@ def main():
         host0 = synth.layer_weights(synth.LayerShape(), seed=0, layer=0)
         for T, zipf in ((512, False), (4096, False), (32768, True)):
             prefill.append(run_prefill(T, zipf, host0, args, peaks))
+    gdn = None if args.no_gdn else run_gdn(args, peaks)
     line = {
         "metric": BASELINE_METRIC, "value": round(res["value"], 2), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -584,6 +661,8 @@ def main():
         line["decode_batch"] = res["decode_batch"]
     if prefill:
         line["prefill"] = prefill
+    if gdn:
+        line["gdn_scan"] = gdn
     if rank == 0:
         print(json.dumps(line), flush=True)
     barrier(world)

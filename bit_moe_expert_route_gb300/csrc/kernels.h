@@ -120,6 +120,21 @@ cudaError_t gemm_w4_launch(const GemmParams& p, cudaStream_t s);
 // ---------------------------------------------------------------- elementwise
 cudaError_t f32_to_bf16_launch(const float* in, uint16_t* out, int64_t n, cudaStream_t s);
 
+// Gated DeltaNet scan (gdn.cu): bf16 q, k [T][Hk][dk], v [T][Hv][dv]; fp32
+// alpha, beta [T][Hv]; fp32 state [Hv][dv][dk] in/out; fp32 out [T][Hv][dv].
+struct GdnParams {
+  const uint16_t* q;
+  const uint16_t* k;
+  const uint16_t* v;
+  const float* alpha;
+  const float* beta;
+  int T, Hk, Hv, dk, dv;
+  float* state;
+  float* out;
+};
+bool gdn_shape_supported(int dk, int dv, int Hk, int Hv);
+cudaError_t gdn_scan_launch(const GdnParams& p, cudaStream_t s);
+
 // Deterministic combine: acc[t] = sum, in slot order (routed slots, then the
 // shared row when `shared`), of row_weight[row] * y[row], fp32 fused
 // multiply-adds; out = bf16 RNE of acc. y [T*k (+T)][d] fp32, d % 4 == 0.

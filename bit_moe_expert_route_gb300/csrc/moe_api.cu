@@ -6,6 +6,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "gdn.h"
 
 namespace {
 
@@ -650,3 +651,33 @@ int moe_get_device_status(const void* ws, void* stream, int32_t* device_status) 
 }
 
 }  // extern "C"
+
+int moe_gdn_scan(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* alpha,
+                 const float* beta, int T, int n_k_heads, int n_v_heads, int d_k, int d_v,
+                 float* state, float* out, void* stream) {
+  if (T < 0 || !moe::gdn_shape_supported(d_k, d_v, n_k_heads, n_v_heads)) return MOE_ERR_SHAPE;
+  if ((int64_t)T * n_v_heads * d_v >= (int64_t)1 << 40) return MOE_ERR_SHAPE;
+  if (!state) return MOE_ERR_NULL;
+  if (T > 0 && (!q || !k || !v || !alpha || !beta || !out)) return MOE_ERR_NULL;
+  const size_t kq_align = d_k == 128 ? 8 : 4, state_align = d_k == 128 ? 16 : 8;
+  if (!aligned(q, kq_align) || !aligned(k, kq_align) || !aligned(state, state_align))
+    return MOE_ERR_ALIGN;
+  if (T == 0) return MOE_OK;
+  int rc = check_device();
+  if (rc != MOE_OK) return rc;
+  moe::GdnParams p;
+  memset(&p, 0, sizeof p);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.alpha = alpha;
+  p.beta = beta;
+  p.T = T;
+  p.Hk = n_k_heads;
+  p.Hv = n_v_heads;
+  p.dk = d_k;
+  p.dv = d_v;
+  p.state = state;
+  p.out = out;
+  return cuda_status(moe::gdn_scan_launch(p, static_cast<cudaStream_t>(stream)));
+}

@@ -1,6 +1,7 @@
 """The C ABI without a GPU: the library loads, exports every function that
-include/moe.h declares, and rejects bad arguments before touching a device."""
+include/*.h declares, and rejects bad arguments before touching a device."""
 import ctypes
+import glob
 import os
 import re
 
@@ -20,7 +21,7 @@ def L():
 
 
 def declared_functions():
-    src = open(HEADER).read()
+    src = "".join(open(h).read() for h in sorted(glob.glob(os.path.join(os.path.dirname(HEADER), "*.h"))))
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(moe_[a-z0-9_]+)\s*\(",
                        src, flags=re.M)
@@ -129,6 +130,25 @@ def test_deterministic_views(L):
     assert v1.y + (T * k + T) * d * 4 <= base + n
     assert L.moe_forward_views_ex(ctypes.c_void_p(base), n - 256, ctypes.byref(sh), 0, 1,
                                   ctypes.byref(v1)) == -4  # too small for y
+
+
+def test_gdn_scan_arguments_are_checked_on_the_host(L):
+    vp = ctypes.c_void_p
+    buf = ctypes.create_string_buffer(1 << 16)
+    a = (ctypes.addressof(buf) + 255) // 256 * 256
+    ok = dict(q=a, k=a, v=a, al=a, be=a, T=4, Hk=2, Hv=4, dk=128, dv=128, st=a, out=a)
+
+    def call(**kw):
+        c = dict(ok, **kw)
+        return L.moe_gdn_scan(vp(c["q"]), vp(c["k"]), vp(c["v"]), vp(c["al"]), vp(c["be"]),
+                              c["T"], c["Hk"], c["Hv"], c["dk"], c["dv"], vp(c["st"]),
+                              vp(c["out"]), None)
+    assert call(T=-1) == -3
+    assert call(dk=96) == -3 and call(dv=12) == -3 and call(Hv=3) == -3 and call(Hk=0) == -3
+    assert call(st=None) == -1 and call(q=None) == -1 and call(out=None) == -1
+    assert call(q=a + 4) == -2 and call(st=a + 8) == -2
+    assert call(dk=64, q=a + 4, st=a + 8) != -2  # 4- and 8-byte alignment suffice at d_k 64
+    assert call(T=0, q=None, k=None, v=None, al=None, be=None, out=None) == 0  # no work
 
 
 def test_bad_arguments_are_rejected_on_the_host(L):
