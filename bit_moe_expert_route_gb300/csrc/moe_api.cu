@@ -659,8 +659,9 @@ int moe_gdn_scan(const uint16_t* q, const uint16_t* k, const uint16_t* v, const 
   if ((int64_t)T * n_v_heads * d_v >= (int64_t)1 << 40) return MOE_ERR_SHAPE;
   if (!state) return MOE_ERR_NULL;
   if (T > 0 && (!q || !k || !v || !alpha || !beta || !out)) return MOE_ERR_NULL;
-  const size_t kq_align = d_k == 128 ? 8 : 4, state_align = d_k == 128 ? 16 : 8;
-  if (!aligned(q, kq_align) || !aligned(k, kq_align) || !aligned(state, state_align))
+  const size_t state_align = d_k == 128 ? 16 : 8;  // q, k, v are staged in 16-byte pieces
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(alpha, 4) ||
+      !aligned(beta, 4) || !aligned(state, state_align))
     return MOE_ERR_ALIGN;
   if (T == 0) return MOE_OK;
   int rc = check_device();

@@ -29,9 +29,8 @@ extern "C" {
  * moe_gdn_scan: the recurrence over T tokens for every value head, from the
  * state in `state` to the state after token T-1 (written back in place).
  *   q, k   bf16 [T][n_k_heads][d_k] device (used as given: any normalisation or
- *          scaling happens before the call); 8-byte aligned for d_k 128,
- *          4-byte for d_k 64
- *   v      bf16 [T][n_v_heads][d_v] device
+ *          scaling happens before the call); 16-byte aligned
+ *   v      bf16 [T][n_v_heads][d_v] device; 16-byte aligned
  *   alpha  fp32 [T][n_v_heads] device, decay per token and value head
  *   beta   fp32 [T][n_v_heads] device, write strength per token and value head
  *   state  fp32 [n_v_heads][d_v][d_k] device, in/out; 16-byte aligned for d_k
@@ -42,7 +41,8 @@ extern "C" {
  * MOE_ERR_SHAPE. NULL pointers: MOE_ERR_NULL; misaligned ones: MOE_ERR_ALIGN.
  * One launch of one 8-warp block per 8 state rows; every warp carries its row
  * through all T tokens in registers (state traffic: one read and one write of
- * the state per call). fp32 arithmetic throughout.
+ * the state per call), the block staging 32 tokens of inputs at a time in
+ * shared memory. fp32 arithmetic throughout.
  */
 int moe_gdn_scan(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* alpha,
                  const float* beta, int T, int n_k_heads, int n_v_heads, int d_k, int d_v,

@@ -146,8 +146,8 @@ def test_gdn_scan_arguments_are_checked_on_the_host(L):
     assert call(T=-1) == -3
     assert call(dk=96) == -3 and call(dv=12) == -3 and call(Hv=3) == -3 and call(Hk=0) == -3
     assert call(st=None) == -1 and call(q=None) == -1 and call(out=None) == -1
-    assert call(q=a + 4) == -2 and call(st=a + 8) == -2
-    assert call(dk=64, q=a + 4, st=a + 8) != -2  # 4- and 8-byte alignment suffice at d_k 64
+    assert call(q=a + 8) == -2 and call(v=a + 8) == -2 and call(st=a + 8) == -2
+    assert call(dk=64, st=a + 8) != -2  # an 8-byte aligned state suffices at d_k 64
     assert call(T=0, q=None, k=None, v=None, al=None, be=None, out=None) == 0  # no work
 
 
