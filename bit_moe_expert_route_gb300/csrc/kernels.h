@@ -135,6 +135,26 @@ struct GdnParams {
 bool gdn_shape_supported(int dk, int dv, int Hk, int Hv);
 cudaError_t gdn_scan_launch(const GdnParams& p, cudaStream_t s);
 
+// Batch-1 decode attention with grouped KV heads (attn.cu): bf16 q [Hq][d],
+// K, V [L][Hkv][d]; fp32 partials (m, l [Hq][P], o [Hq][P][d], P = splits x 8
+// warps) in a workspace; fp32 out [Hq][d].
+struct AttnParams {
+  const uint16_t* q;
+  const uint16_t* K;
+  const uint16_t* V;
+  int L, Hq, Hkv, d;
+  float scale;
+  float* ws;      // attn_workspace_floats(...) floats; the launch carves the partials
+  float* part_m;  // set by attn_decode_launch
+  float* part_l;
+  float* part_o;
+  float* out;
+};
+bool attn_shape_supported(int L, int Hq, int Hkv, int d);
+int attn_splits(int L, int Hkv, int sms);
+size_t attn_workspace_floats(int L, int Hq, int Hkv, int d, int sms);
+cudaError_t attn_decode_launch(const AttnParams& p, int sms, cudaStream_t s);
+
 // Deterministic combine: acc[t] = sum, in slot order (routed slots, then the
 // shared row when `shared`), of row_weight[row] * y[row], fp32 fused
 // multiply-adds; out = bf16 RNE of acc. y [T*k (+T)][d] fp32, d % 4 == 0.

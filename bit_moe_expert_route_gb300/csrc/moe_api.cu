@@ -2,11 +2,13 @@
 // launch sequences of the routing, grouped-GEMM, whole-layer and decode
 // entry points declared in include/moe.h.
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 
 #include "common.cuh"
 #include "kernels.h"
 #include "gdn.h"
+#include "attn.h"
 
 namespace {
 
@@ -681,4 +683,41 @@ int moe_gdn_scan(const uint16_t* q, const uint16_t* k, const uint16_t* v, const 
   p.state = state;
   p.out = out;
   return cuda_status(moe::gdn_scan_launch(p, static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_decode_attention_workspace_bytes(int L, int n_q_heads, int n_kv_heads, int d) {
+  if (!moe::attn_shape_supported(L, n_q_heads, n_kv_heads, d)) return 0;
+  // the split count never exceeds one per 256 positions, whatever the SM count
+  return moe::attn_workspace_floats(L, n_q_heads, n_kv_heads, d, 1 << 20) * sizeof(float);
+}
+
+int moe_decode_attention(const uint16_t* q, const uint16_t* K, const uint16_t* V, int L,
+                         int n_q_heads, int n_kv_heads, int d, float scale, float* out, void* ws,
+                         size_t ws_bytes, void* stream) {
+  if (!moe::attn_shape_supported(L, n_q_heads, n_kv_heads, d)) return MOE_ERR_SHAPE;
+  if ((int64_t)L * n_kv_heads * d >= (int64_t)1 << 40) return MOE_ERR_SHAPE;
+  if (!q || !K || !V || !out) return MOE_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(out, 4))
+    return MOE_ERR_ALIGN;
+  if (!ws || !aligned(ws, 4) ||
+      ws_bytes < moe_decode_attention_workspace_bytes(L, n_q_heads, n_kv_heads, d))
+    return MOE_ERR_WORKSPACE;
+  int rc = check_device();
+  if (rc != MOE_OK) return rc;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  moe::AttnParams p;
+  memset(&p, 0, sizeof p);
+  p.q = q;
+  p.K = K;
+  p.V = V;
+  p.L = L;
+  p.Hq = n_q_heads;
+  p.Hkv = n_kv_heads;
+  p.d = d;
+  p.scale = scale > 0.f ? scale : 1.f / sqrtf((float)d);
+  p.ws = static_cast<float*>(ws);
+  p.out = out;
+  return cuda_status(moe::attn_decode_launch(p, sms, static_cast<cudaStream_t>(stream)));
 }

@@ -96,6 +96,10 @@ def lib():
         L.moe_forward_views_ex.argtypes = [vp, sz, vp, i32, i32, vp]
         L.moe_forward_ex.argtypes = [vp, vp, vp, i32, i32, vp, vp, sz, vp]
         L.moe_gdn_scan.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
+        L.moe_decode_attention_workspace_bytes.restype = sz
+        L.moe_decode_attention_workspace_bytes.argtypes = [i32, i32, i32, i32]
+        L.moe_decode_attention.argtypes = [vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, vp, vp,
+                                           sz, vp]
         L.moe_decode_workspace_bytes.restype = sz
         L.moe_decode_workspace_bytes.argtypes = [vp]
         L.moe_decode_views.argtypes = [vp, sz, vp, vp]
@@ -269,6 +273,26 @@ def gdn_scan(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Ten
     rc = lib().moe_gdn_scan(_p(q), _p(k), _p(v), _p(alpha), _p(beta), T, Hk, Hv, dk, dv,
                             _p(state), _p(out), _stream(stream))
     _check("moe_gdn_scan", rc)
+    return out
+
+
+def decode_attention(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scale: float = 0.0,
+                     out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """moe_decode_attention (include/attn.h): q bf16 [Hq, d]; K, V bf16 [L, Hkv, d];
+    scale <= 0 means 1/sqrt(d). Returns out fp32 [Hq, d]."""
+    Hq, d = q.shape
+    L, Hkv = K.shape[0], K.shape[1]
+    nbytes = lib().moe_decode_attention_workspace_bytes(L, Hq, Hkv, d)
+    if nbytes == 0:
+        raise MoeError("moe_decode_attention_workspace_bytes", -3)
+    if ws is None:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty(Hq, d, dtype=torch.float32, device=q.device)
+    rc = lib().moe_decode_attention(_p(q), _p(K), _p(V), L, Hq, Hkv, d, float(scale), _p(out),
+                                    _p(ws), ws.numel(), _stream(stream))
+    _check("moe_decode_attention", rc)
     return out
 
 

@@ -151,6 +151,28 @@ def test_gdn_scan_arguments_are_checked_on_the_host(L):
     assert call(T=0, q=None, k=None, v=None, al=None, be=None, out=None) == 0  # no work
 
 
+def test_decode_attention_arguments_are_checked_on_the_host(L):
+    vp = ctypes.c_void_p
+    ws_n = L.moe_decode_attention_workspace_bytes(4096, 16, 2, 256)
+    # partials: (m, l, 256 outputs) per query head, 8 per 256-position slice at most
+    assert ws_n == 16 * (4096 // 256) * 8 * (2 + 256) * 4
+    for args in ((0, 16, 2, 256), (10, 16, 2, 96), (10, 16, 3, 256), (10, 32, 2, 128)):
+        assert L.moe_decode_attention_workspace_bytes(*args) == 0, args  # 16 per KV head > 8
+    buf = ctypes.create_string_buffer(1 << 20)
+    a = (ctypes.addressof(buf) + 255) // 256 * 256
+    ok = dict(q=a, K=a, V=a, L=64, Hq=8, Hkv=1, d=128, out=a, ws=a, n=1 << 19)
+
+    def call(**kw):
+        c = dict(ok, **kw)
+        return L.moe_decode_attention(vp(c["q"]), vp(c["K"]), vp(c["V"]), c["L"], c["Hq"],
+                                      c["Hkv"], c["d"], ctypes.c_float(0.0), vp(c["out"]),
+                                      vp(c["ws"]), c["n"], None)
+    assert call(L=0) == -3 and call(d=48) == -3 and call(Hq=9) == -3
+    assert call(q=None) == -1 and call(V=None) == -1
+    assert call(K=a + 8) == -2 and call(q=a + 4) == -2
+    assert call(ws=None) == -4 and call(n=16) == -4
+
+
 def test_bad_arguments_are_rejected_on_the_host(L):
     vp = ctypes.c_void_p
     fake = vp(0x10000)  # never dereferenced: every call below fails validation first
