@@ -211,3 +211,22 @@ def test_bad_arguments_are_rejected_on_the_host(L):
     # decode requires T == 1
     sh2 = ops.Shape(2, 2048, 256, 8, 512, 512, 64)
     assert L.moe_decode_gemv_w4(fake, None, ctypes.byref(sh2), fake, fake, 1 << 20, None) == -3
+
+
+def test_max_tiles_bounds_every_routing(L, orc):
+    """The device block map is sized by moe_max_tiles before the routing is known:
+    the exact tile count the oracle builds for any routing must stay within it
+    (uniform, fully concentrated and round-robin routings, every tile height)."""
+    import numpy as np
+    rng = np.random.default_rng(0)
+    for T, E, k in ((1, 8, 1), (7, 8, 8), (64, 72, 4), (1000, 256, 8), (4096, 256, 8)):
+        routings = {
+            "uniform": np.argsort(rng.random((T, E)), axis=1)[:, :k],
+            "concentrated": np.tile(np.arange(k), (T, 1)),
+            "round-robin": (np.arange(T)[:, None] * k + np.arange(k)[None, :]) % E,
+        }
+        for name, ids in routings.items():
+            ids = ids.astype(np.int32)
+            for bn in (16, 32, 64, 128, 256):
+                m = orc.route_meta(ids, E, bn, True)
+                assert m["num_tiles"] <= L.moe_max_tiles(T, E, k, bn, 1), (T, E, k, name, bn)
