@@ -308,3 +308,24 @@ def test_planted_mistakes_are_caught(mutant):
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, f"planted mistake '{MUTANTS[mutant]}' passed every pin"
+
+
+def test_route_invariants_hold_for_random_shapes(orc):
+    """Property test of the routing invariants (counts, offsets, stable
+    permutation and its inverse, row tokens, block map covering every row once
+    with the exact tile count) over random token counts (including none),
+    expert counts, top-k, tile heights and with or without the shared rows."""
+    pytest.importorskip("hypothesis")
+    from hypothesis import given, settings, strategies as st
+
+    @settings(max_examples=80, deadline=None)
+    @given(T=st.integers(0, 300), E=st.sampled_from([8, 16, 72, 256]), k=st.integers(1, 8),
+           bn=st.sampled_from([16, 32, 64, 128, 256]), shared=st.booleans(),
+           seed=st.integers(0, 2 ** 31 - 1))
+    def prop(T, E, k, bn, shared, seed):
+        rng = np.random.default_rng(seed)
+        ids = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+        r = orc.route_meta(ids, E, bn, shared)
+        check_route_invariants(ids, E, bn, r, shared)
+
+    prop()
