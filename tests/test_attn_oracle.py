@@ -10,6 +10,7 @@ A4  grouped heads: query head h equals a one-head call on KV head
     h // (Hq / Hkv); heads of one group with the same query agree.
 A5  permuting the cache positions (keys and values together) changes nothing,
     and the output is linear in the values.
+A6  all-one values give an all-one output (the weights sum to one).
 Each planted mistake (the oracle's `mutant`) fails at least one pin.
 """
 import math
@@ -82,8 +83,15 @@ def pin_permutation_and_linearity(mutant=0):
                                                                        atol=1e-13)
 
 
+def pin_values_all_one(mutant=0):
+    """The output is a convex combination of value rows: all-one values give ones."""
+    q, K, _ = rand(23, 8, 2, 16, 8)
+    o = decode_attention(q, K, np.ones((23, 2, 16)), mutant=mutant)
+    return np.allclose(o, 1.0, rtol=0, atol=1e-13)
+
+
 PINS = [pin_single_position, pin_equal_keys, pin_aligned_key, pin_grouped_heads,
-        pin_permutation_and_linearity]
+        pin_permutation_and_linearity, pin_values_all_one]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -94,3 +102,27 @@ def test_pin_holds(pin):
 @pytest.mark.parametrize("mutant", [1, 2, 3, 4])
 def test_planted_mistake_is_caught(mutant):
     assert not all(pin(mutant) for pin in PINS), f"mutant {mutant} passed every pin"
+
+
+def test_pins_for_random_shapes():
+    """A4-A6 over random cache lengths, head counts, group sizes and head dims."""
+    pytest.importorskip("hypothesis")
+    from hypothesis import given, settings, strategies as st
+
+    @settings(max_examples=60, deadline=None)
+    @given(L=st.integers(1, 40), Hkv=st.integers(1, 3), group=st.integers(1, 8),
+           d=st.integers(1, 12), seed=st.integers(0, 2 ** 31 - 1))
+    def prop(L, Hkv, group, d, seed):
+        Hq = Hkv * group
+        q, K, V = rand(L, Hq, Hkv, d, seed)
+        o = decode_attention(q, K, V)
+        assert np.allclose(decode_attention(q, K, np.ones_like(V)), 1.0, rtol=0, atol=1e-12)
+        perm = np.random.default_rng(seed + 1).permutation(L)
+        assert np.allclose(decode_attention(q, K[perm], V[perm]), o, rtol=1e-12, atol=1e-13)
+        for h in range(Hq):
+            g = h // group
+            o1 = decode_attention(q[h:h + 1], K[:, g:g + 1], V[:, g:g + 1])
+            assert np.allclose(o[h], o1[0], rtol=1e-13, atol=1e-14)
+
+    prop()
+

@@ -110,3 +110,36 @@ def test_decay_only_state_matches_closed_form_over_long_scan():
     q, k, v, _, _, S0 = rand_inputs(200, 1, 1, 4, 4, 5)
     o, S = gdn_scan(q, k, v, np.full((200, 1), 0.99), np.zeros((200, 1)), S0)
     assert np.allclose(S, 0.99 ** 200 * S0, rtol=1e-12)
+
+
+def test_product_form_for_random_shapes():
+    """The product-form pin (G3) over random sequence lengths, head sizes, grouped
+    heads, decays and write strengths (including alpha = 1 and beta = 0 or 1)."""
+    pytest.importorskip("hypothesis")
+    from hypothesis import given, settings, strategies as st
+
+    @settings(max_examples=60, deadline=None)
+    @given(T=st.integers(1, 12), Hk=st.integers(1, 3), group=st.integers(1, 3),
+           dk=st.integers(1, 7), dv=st.integers(1, 5), seed=st.integers(0, 2 ** 31 - 1),
+           edge=st.sampled_from(["none", "alpha1", "beta0", "beta1"]))
+    def prop(T, Hk, group, dk, dv, seed, edge):
+        Hv = Hk * group
+        q, k, v, alpha, beta, S0 = rand_inputs(T, Hk, Hv, dk, dv, seed)
+        if edge == "alpha1":
+            alpha[:] = 1.0
+        elif edge == "beta0":
+            beta[:] = 0.0
+        elif edge == "beta1":
+            beta[:] = 1.0
+        o, S = gdn_scan(q, k, v, alpha, beta, S0)
+        for h in range(Hv):
+            hk = h // group
+            St = S0[h]
+            for t in range(T):
+                kt = k[t, hk][:, None]
+                A = alpha[t, h] * (np.eye(dk) - beta[t, h] * kt @ kt.T)
+                St = St @ A + beta[t, h] * v[t, h][:, None] @ kt.T
+                assert np.allclose(o[t, h], St @ q[t, hk], rtol=1e-10, atol=1e-12)
+            assert np.allclose(S[h], St, rtol=1e-10, atol=1e-12)
+
+    prop()
