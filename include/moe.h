@@ -15,6 +15,9 @@
  *     optimizations", second bullet);
  *   - batch-1 decode is a matrix-vector product over only the selected
  *     experts' weights ("Why prefill and decode get different treatment").
+ * The same library also exports the model's Gated DeltaNet scan (gdn.h) and
+ * batch-1 decode attention with grouped KV heads (attn.h), under the
+ * conventions below.
  *
  * Conventions shared by every call
  *   - bf16 values are passed as uint16_t bit patterns.
