@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "kernels.h"
 
 namespace {
 
@@ -55,11 +56,32 @@ int scratch_on_current_device(void** addr) {
 extern "C" int moe_decode_gemv_w4_noalloc(const uint16_t* x, const moe_weights_t* w,
                                           const moe_shape_t* shape, uint16_t* out,
                                           void* stream) {
-  const size_t need = moe_decode_workspace_bytes(shape);
-  if (need == 0) return MOE_ERR_SHAPE;
-  if (need > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;  // shape too large for the built-in scratch
+  // the same argument checks as moe_decode_gemv_w4 first, so an unsupported
+  // shape reads as MOE_ERR_SHAPE here too; then the scratch's size limit
+  int rc = moe::decode_args_status(x, w, shape, out);
+  if (rc != MOE_OK) return rc;
+  if (moe_decode_workspace_bytes(shape) > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if ((rc = scratch_on_current_device(&scratch)) != MOE_OK) return rc;
+  return moe_decode_gemv_w4(x, w, shape, out, scratch, kNoAllocScratchBytes, stream);
+}
+
+extern "C" int moe_decode_noalloc_device_status(void* stream, int32_t* device_status) {
+  if (!device_status) return MOE_ERR_NULL;
   void* scratch = nullptr;
   const int rc = scratch_on_current_device(&scratch);
   if (rc != MOE_OK) return rc;
-  return moe_decode_gemv_w4(x, w, shape, out, scratch, kNoAllocScratchBytes, stream);
+  return moe_get_device_status(scratch, stream, device_status);
+}
+
+extern "C" int moe_decode_noalloc_reset(void* stream) {
+  void* scratch = nullptr;
+  const int rc = scratch_on_current_device(&scratch);
+  if (rc != MOE_OK) return rc;
+  if (cudaMemsetAsync(scratch, 0, kNoAllocScratchBytes, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess) {
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
 }

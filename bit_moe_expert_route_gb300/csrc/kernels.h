@@ -30,16 +30,29 @@ struct RouteParams {
   int32_t* block_map;      // [max_tiles][4]
   int32_t* num_tiles;      // [1]
   int max_tiles;
-  // optional second block map of the same rows in tiles of block_n2 rows
+  // optional second block map of the same rows in tiles of block_n2 rows;
+  // window2 > 0 (a multiple of kRouteTPB) orders it by token window: the
+  // tiles of tokens [0, window2) of every expert, then their shared rows,
+  // then the next window's (each expert's rows in a window are contiguous,
+  // since the scatter keeps every expert's rows in token order)
   int32_t* block_map2;     // [max_tiles2][4] or null
   int32_t* num_tiles2;     // [1]
-  int max_tiles2, block_n2;
+  int max_tiles2, block_n2, window2;
   // scratch
   int32_t* blk;            // [nblk][E]
   int32_t* status;
 };
 
 inline int route_nblk(int T) { return (T + kRouteTPB - 1) / kRouteTPB; }
+// Tiles of a block map of T tokens' rows cut per token window of W tokens
+// (W = 0: one window): every (window, expert) and (window, shared) piece
+// ends in at most one partial tile.
+inline int windowed_max_tiles(int T, int E, int k, int bn, int W, bool with_shared) {
+  const int64_t nW = W > 0 ? ((int64_t)T + W - 1) / W : 1;
+  const int64_t n = ((int64_t)T * k + bn - 1) / bn + nW * E +
+                    (with_shared ? ((int64_t)T + bn - 1) / bn + nW : 0);
+  return n > 0x3FFFFFFF ? 0x3FFFFFFF : (int)n;
+}
 cudaError_t route_launch(const RouteParams& p, cudaStream_t s);
 
 // ---------------------------------------------------------------- router GEMM
@@ -190,5 +203,8 @@ size_t decode_pub_words(int E);
 // Sizes the decode kernel can run: d <= 4096 and h of every slot fits in shared memory.
 bool decode_shape_supported(int d, int E, int k, int f, bool shared);
 cudaError_t decode_launch(const DecodeParams& p, cudaStream_t s);
+// moe_decode_gemv_w4's argument checks other than the workspace (moe_api.cu).
+int decode_args_status(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* shape,
+                       const uint16_t* out);
 
 }  // namespace moe

@@ -67,6 +67,11 @@ RouteWs route_ws(void* ws, int T, int E) {
   return r;
 }
 
+// Token window of the down projection's block map (a multiple of the routing
+// kernels' 128-token blocks): 8192 tokens' fp32 output rows are 64 MB, about
+// half of L2.
+constexpr int kDownWindow = 8192;
+
 bool shape_ok(const moe_shape_t* s, bool need_tokens) {
   if (!s) return false;
   if (s->T < 0 || (need_tokens && s->T < 1)) return false;
@@ -114,8 +119,11 @@ FwdWs forward_ws(void* ws, const moe_shape_t* s, int bn, int flags) {
   // are mostly padding, and the combine epilogue's per-row copies dominate)
   // (gate/up stays at 128: its two accumulators fill TMEM at that height)
   r.v.down_block_n = bn == 128 && (int64_t)T * k >= (int64_t)256 * E ? 256 : bn;
+  // above kDownWindow tokens the down map is ordered by token window (see
+  // RouteParams::window2): the fp32 rows it adds into then stay in L2
+  r.v.down_window = r.v.down_block_n != bn && T > kDownWindow ? kDownWindow : 0;
   if (r.v.down_block_n != bn) {
-    r.v.down_max_tiles = moe_max_tiles(T, E, k, r.v.down_block_n, 1);
+    r.v.down_max_tiles = moe::windowed_max_tiles(T, E, k, r.v.down_block_n, r.v.down_window, true);
     r.v.down_block_map = c.take<int32_t>((size_t)r.v.down_max_tiles * 4);
     r.v.down_num_tiles = c.take<int32_t>(1);
   } else {  // one map serves both projections
@@ -211,6 +219,20 @@ int check_weights(const moe_weights_t* w, const moe_shape_t* s) {
 }
 
 }  // namespace
+
+// Checks of moe_decode_gemv_w4's arguments other than the workspace.
+int moe::decode_args_status(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* shape,
+                            const uint16_t* out) {
+  if (!shape_ok(shape, true) || shape->T != 1) return MOE_ERR_SHAPE;
+  if (!moe::decode_shape_supported(shape->d_model, shape->n_experts, shape->top_k, shape->d_ff,
+                                   w && w->shared_gate))
+    return MOE_ERR_SHAPE;
+  int rc = check_weights(w, shape);
+  if (rc != MOE_OK) return rc;
+  if (!x || !out) return MOE_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(out, 4)) return MOE_ERR_ALIGN;
+  return MOE_OK;
+}
 
 extern "C" {
 
@@ -472,6 +494,7 @@ int moe_forward_ex(const uint16_t* x, const moe_weights_t* w, const moe_shape_t*
     rp.num_tiles2 = v.down_num_tiles;
     rp.max_tiles2 = v.down_max_tiles;
     rp.block_n2 = v.down_block_n;
+    rp.window2 = v.down_window;
   }
   if ((rc = cuda_status(moe::route_launch(rp, s))) != MOE_OK) return rc;
   // 3. gate/up grouped GEMM with SwiGLU -> h (rows in expert order, shared rows last)
@@ -558,14 +581,8 @@ int moe_decode_views(void* ws, size_t ws_bytes, const moe_shape_t* shape,
 
 int moe_decode_gemv_w4(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* shape,
                        uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
-  if (!shape_ok(shape, true) || shape->T != 1) return MOE_ERR_SHAPE;
-  if (!moe::decode_shape_supported(shape->d_model, shape->n_experts, shape->top_k, shape->d_ff,
-                                   w && w->shared_gate))
-    return MOE_ERR_SHAPE;
-  int rc = check_weights(w, shape);
+  int rc = moe::decode_args_status(x, w, shape, out);
   if (rc != MOE_OK) return rc;
-  if (!x || !out) return MOE_ERR_NULL;
-  if (!aligned(x, 16) || !aligned(out, 4)) return MOE_ERR_ALIGN;
   const DecWs dw = decode_ws(ws, shape);
   if (!ws || !aligned(ws, kAlign) || ws_bytes < dw.bytes) return MOE_ERR_WORKSPACE;
   if ((rc = check_device()) != MOE_OK) return rc;

@@ -184,6 +184,53 @@ __device__ void build_block_map(const RouteParams& p, int bn, int total, const i
   __syncthreads();  // s_toff and s_tiles are reused by a second call
 }
 
+// The same rows cut per token window of W tokens (W a multiple of
+// kRouteTPB): for each window, the tiles of every expert's rows whose tokens
+// lie in the window (experts in order; those rows are contiguous in expert
+// order because the scatter is stable), then the window's shared rows. A
+// GEMM that walks the map in order then finishes one window's tokens before
+// the next: the output rows it adds into stay in L2 while all of their
+// contributions arrive. p.blk holds the per-(block, expert) bases here.
+__device__ void build_windowed_map(const RouteParams& p, int bn, int W, int nblk, const int* s_off,
+                                   const int* s_cnt, int* s_tiles, int32_t* block_map,
+                                   int32_t* num_tiles, int max_tiles, int where) {
+  const int e = threadIdx.x;
+  const int bw = W / kRouteTPB;
+  const int nW = (p.T + W - 1) / W;
+  const int kT = p.T * p.k;
+  int written = 0;  // the same in every thread
+  for (int w = 0; w < nW; ++w) {
+    int lo = 0, n = 0, nt = 0;
+    if (e < p.E) {
+      const int b0 = w * bw, b1 = (w + 1) * bw;
+      lo = p.blk[(size_t)b0 * p.E + e];
+      const int hi = b1 < nblk ? p.blk[(size_t)b1 * p.E + e] : s_cnt[e];
+      n = hi - lo;
+      nt = (n + bn - 1) / bn;
+    }
+    const int toff = block_exclusive_scan_1024(nt, s_tiles);
+    const int routed = *s_tiles;
+    for (int j = 0; j < nt; ++j) {
+      const int i = written + toff + j;
+      if (i < max_tiles)
+        reinterpret_cast<int4*>(block_map)[i] = make_int4(e, s_off[e] + lo + j * bn, min(bn, n - j * bn), 0);
+    }
+    const int t0 = w * W, t1 = min(p.T, t0 + W);
+    const int ns = p.with_shared ? (t1 - t0 + bn - 1) / bn : 0;
+    for (int j = e; j < ns; j += blockDim.x) {
+      const int i = written + routed + j;
+      if (i < max_tiles)
+        reinterpret_cast<int4*>(block_map)[i] = make_int4(p.E, kT + t0 + j * bn, min(bn, t1 - t0 - j * bn), 0);
+    }
+    written += routed + ns;
+    __syncthreads();  // *s_tiles is rewritten by the next window's scan
+  }
+  if (e == 0) {
+    if (written > max_tiles) report(p.status, MOE_DEV_BAD_TILE, where, written);
+    *num_tiles = min(written, max_tiles);
+  }
+}
+
 __global__ void __launch_bounds__(1024) route_scan_kernel(RouteParams p, int nblk) {
   __shared__ int s_off[1025];
   __shared__ int s_cnt[1024];
@@ -214,7 +261,10 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(RouteParams p, int nbl
   __syncthreads();
   build_block_map(p, p.block_n, total, s_off, s_cnt, s_toff, &s_tiles, p.block_map, p.num_tiles,
                   p.max_tiles, 11);
-  if (p.block_map2)  // the same rows in tiles of block_n2 (a second GEMM's tile height)
+  if (p.block_map2 && p.window2 > 0)  // a second GEMM's tiles, ordered by token window
+    build_windowed_map(p, p.block_n2, p.window2, nblk, s_off, s_cnt, &s_tiles, p.block_map2,
+                       p.num_tiles2, p.max_tiles2, 13);
+  else if (p.block_map2)  // the same rows in tiles of block_n2 (a second GEMM's tile height)
     build_block_map(p, p.block_n2, total, s_off, s_cnt, s_toff, &s_tiles, p.block_map2,
                     p.num_tiles2, p.max_tiles2, 13);
 }

@@ -56,7 +56,7 @@ class ForwardViews(ctypes.Structure):
         ("max_tiles", ctypes.c_int32), ("block_n", ctypes.c_int32),
         ("down_block_map", ctypes.c_void_p), ("down_num_tiles", ctypes.c_void_p),
         ("down_max_tiles", ctypes.c_int32), ("down_block_n", ctypes.c_int32),
-        ("y", ctypes.c_void_p)]
+        ("y", ctypes.c_void_p), ("down_window", ctypes.c_int32)]
 
 
 class DecodeViews(ctypes.Structure):
@@ -105,6 +105,8 @@ def lib():
         L.moe_decode_views.argtypes = [vp, sz, vp, vp]
         L.moe_decode_gemv_w4.argtypes = [vp, vp, vp, vp, vp, sz, vp]
         L.moe_decode_gemv_w4_noalloc.argtypes = [vp, vp, vp, vp, vp]
+        L.moe_decode_noalloc_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+        L.moe_decode_noalloc_reset.argtypes = [vp]
         L.moe_decode_batch_workspace_bytes.restype = sz
         L.moe_decode_batch_workspace_bytes.argtypes = [vp]
         L.moe_decode_batch_views.argtypes = [vp, sz, vp, vp]

@@ -265,6 +265,11 @@ typedef struct {
      h row r . W_down^T of its expert, unweighted; out_acc then holds the
      fixed-order weighted sum. */
   float* y;
+  /* Tokens per window of the down projection's block map (0: one window).
+     With a window W, down_block_map lists, for tokens [0, W), every expert's
+     tiles in expert order and then the shared rows' tiles, then the same for
+     [W, 2W), and so on. */
+  int32_t down_window;
 } moe_forward_views_t;
 int moe_forward_views(void* ws, size_t ws_bytes, const moe_shape_t* shape, int block_n,
                       moe_forward_views_t* views);
@@ -311,21 +316,29 @@ int moe_decode_views(void* ws, size_t ws_bytes, const moe_shape_t* shape,
  * allocation's synchronisation. Its scratch is a 256 KB array compiled into
  * the library (each GPU that loads the library holds one until the process
  * exits); the call itself allocates nothing.
- *   x, w, shape, out, stream: as for moe_decode_gemv_w4 (shape->T == 1).
- *   Returns MOE_ERR_WORKSPACE when moe_decode_workspace_bytes(shape) exceeds
- *   256 KB (the top-8-of-256 layer with d_ff 512 needs about 40 KB), and
- *   MOE_ERR_CUDA if the scratch's device address cannot be obtained.
+ *   x, w, shape, out, stream: as for moe_decode_gemv_w4 (shape->T == 1), with
+ *   the same argument checks and return codes; then MOE_ERR_WORKSPACE when
+ *   moe_decode_workspace_bytes(shape) exceeds 256 KB (the top-8-of-256 layer
+ *   with d_ff 512 needs 74,240 bytes), and MOE_ERR_CUDA if the scratch's
+ *   device address cannot be obtained.
  * The first call on each device looks the scratch up (cudaGetSymbolAddress,
  * which may load the library's device code onto that device); make that
  * first call before any stream capture. All calls share the one array, which
  * keeps the previous call's contents (a static device array starts at zero,
- * and every call leaves the kernel's counters at zero). Calls that overlap
- * on the GPU, e.g. on two streams, race on the array; device-side fault
- * records stay in the array and are not readable through
- * moe_get_device_status.
+ * and every call leaves the kernel's counters as the next call needs them).
+ * Calls that overlap on the GPU, e.g. on two streams, race on the array.
+ * The array's device status word is read with
+ * moe_decode_noalloc_device_status; after a call that recorded
+ * MOE_DEV_TIMEOUT, moe_decode_noalloc_reset zeroes the array (the decode
+ * contract's "zero the workspace again"), and later calls are correct again.
  */
 int moe_decode_gemv_w4_noalloc(const uint16_t* x, const moe_weights_t* w,
                                const moe_shape_t* shape, uint16_t* out, void* stream);
+/* The built-in scratch's device status word (synchronises `stream`; returns
+ * MOE_ERR_DEVICE when the word holds a fault), as moe_get_device_status. */
+int moe_decode_noalloc_device_status(void* stream, int32_t* device_status);
+/* Zeroes the built-in scratch on `stream` (cudaMemsetAsync; allocates nothing). */
+int moe_decode_noalloc_reset(void* stream);
 
 /*
  * moe_decode_batch_w4: a small batch of tokens (1 <= shape->T <= 8, e.g. a

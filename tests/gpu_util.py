@@ -24,25 +24,46 @@ def bf16_np(t):
     return synth.bf16_to_f32(to_np(t.view(__import__("torch").int16)).view(np.uint16))
 
 
-def bf16_half_ulp(v):
-    """Half the bf16 spacing at |v| (the most a round-to-nearest bf16 store can move v)."""
-    a = np.maximum(np.abs(np.asarray(v, np.float64)), 2.0 ** -126)
-    return 2.0 ** (np.floor(np.log2(a)) - 8)
-
-
-def tolerance_check(got, ref, bf16_output=False):
-    """Layer-output bar: max|err| <= 2e-2 * rms(ref) and ||err|| / ||ref|| <= 5e-3.
-
-    bf16_output: `got` went through a final round-to-nearest bf16 store; that
-    store alone may move an element by half a bf16 spacing (0.125 at |v| >= 32,
-    above the bar whenever rms(ref) < 6.25), so the per-element bound is the bar
-    plus half a bf16 spacing at that element. rel-L2 keeps the plain bar."""
+def tolerance_check(got, ref):
+    """Layer-output bar: max|err| <= 2e-2 * rms(ref) and ||err|| / ||ref|| <= 5e-3,
+    applied as stated to every element, including outputs that went through
+    a final bf16 store (a store moves |v| by at most |v| * 2^-9, within the bar
+    for every |v| <= 10.24 rms(ref))."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     err = got - ref
     rms = np.sqrt(np.mean(ref ** 2))
-    bound = 2e-2 * rms + (bf16_half_ulp(np.maximum(np.abs(got), np.abs(ref))) if bf16_output else 0.0)
-    worst = float(np.max(np.abs(err) - bound))
+    worst = float(np.max(np.abs(err)) - 2e-2 * rms)
     rel_l2 = float(np.linalg.norm(err) / np.linalg.norm(ref))
     return worst <= 0 and rel_l2 <= 5e-3, dict(max_err=float(np.max(np.abs(err))), rms=rms,
-                                              rel_l2=rel_l2, worst_over_bound=worst)
+                                              rel_l2=rel_l2, worst_over_bound=worst,
+                                              max_ref_over_rms=float(np.max(np.abs(ref)) / rms))
+
+
+# A bf16 store moves |v| by up to half a bf16 spacing, |v| * 2^-8 at the bottom
+# of a binade, so it can meet a max-error bar of 2e-2 rms on its own only for
+# |v| <= 0.02 * 256 rms = 5.12 rms. The layer's outputs are near-Gaussian and
+# larger ones occur at T >= 4096 (T = 4096: an element in [32, 64) at rms 4.90,
+# error 0.126 against a bar of 0.098, all of it the store's rounding).
+BF16_BAR_LIMIT = 5.12
+
+
+def bf16_output_check(got, ref):
+    """The layer bar on a bf16 output: every element with |ref| <= 5.12 rms(ref)
+    within 2e-2 rms(ref); above that, within 2e-2 rms(ref) plus the store's own
+    rounding (half the bf16 spacing at |ref|); rel-L2 <= 5e-3 over all. The info
+    lists how many elements were above 5.12 rms and their worst error."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = np.abs(got - ref)
+    rms = np.sqrt(np.mean(ref ** 2))
+    big = np.abs(ref) > BF16_BAR_LIMIT * rms
+    half_spacing = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -126))) - 8)
+    bound = 2e-2 * rms + np.where(big, half_spacing, 0.0)
+    worst = float(np.max(err - bound))
+    rel_l2 = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    return worst <= 0 and rel_l2 <= 5e-3, dict(
+        max_err=float(err.max()), rms=rms, rel_l2=rel_l2, worst_over_bound=worst,
+        n_above_limit=int(big.sum()),
+        max_err_above_limit=float(err[big].max()) if big.any() else 0.0,
+        max_err_within_limit=float(err[~big].max()) if (~big).any() else 0.0)

@@ -102,11 +102,18 @@ def test_forward_views_pick_the_down_tile_map(L):
         assert v.block_n == bn and not v.y
         if separate:
             assert v.down_block_n == 256 and v.down_block_map != v.block_map
-            assert v.down_max_tiles == L.moe_max_tiles(T, 256, 8, 256, 1)
+            # above 8192 tokens the down map is cut per 8192-token window: every
+            # (window, expert) and (window, shared) piece may end in a partial tile
+            W = 8192 if T > 8192 else 0
+            assert v.down_window == W
+            nW = -(-T // W) if W else 1
+            assert v.down_max_tiles == -(-T * 8 // 256) + nW * 256 + -(-T // 256) + nW
+            assert v.down_max_tiles >= L.moe_max_tiles(T, 256, 8, 256, 1)
             assert base <= v.down_block_map and v.down_num_tiles + 4 <= base + n
         else:
             assert (v.down_block_n, v.down_max_tiles) == (bn, v.max_tiles)
             assert (v.down_block_map, v.down_num_tiles) == (v.block_map, v.num_tiles)
+            assert v.down_window == 0
 
 
 def test_deterministic_views(L):

@@ -4,17 +4,13 @@ Inputs: bf16 q [Hq, d] and K, V caches [L, Hkv, d] drawn N(0, 1); the oracle
 sees the same values exactly. The kernel computes the scores and the softmax
 in fp32 and merges per-warp partial softmaxes; the output is a convex
 combination of value rows. Bar: |err| <= 1e-4 * (rms(ref) + |ref|) per element.
-
-The kernel has not had its first GPU run yet: the module is skipped until it
-has, so the suite stays green meanwhile.
 """
 import numpy as np
 import pytest
 
 from oracle.attn import decode_attention
 
-pytestmark = [pytest.mark.gpu,
-              pytest.mark.skip(reason="decode-attention kernel not yet run on a GPU")]
+pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 

@@ -3,8 +3,12 @@
 The GPU's fp32 router logits are checked against the oracle's (they differ
 only in summation order), then the oracle runs the layer on the GPU's logits
 so both sides take the same top-k decision; ids must match exactly and the
-bf16 output must satisfy max|err| <= 2e-2 rms(ref) (plus half a bf16 spacing
-for the final bf16 store), rel-L2 <= 5e-3."""
+bf16 output must satisfy max|err| <= 2e-2 rms(ref) and rel-L2 <= 5e-3.
+
+The chained test runs several layers as a model does: each layer's bf16
+output is the next layer's input, the layers captured in one CUDA graph with
+programmatic-dependent-launch edges (each layer's weight prefetch runs
+before its dependency wait, while the previous layer still runs)."""
 import numpy as np
 import pytest
 
@@ -36,7 +40,7 @@ def check_one(orc, host, dec, x):
     w = to_np(dec.view("topk_w", (1, FULL.top_k + 1), torch.float32))
     np.testing.assert_allclose(w[:, :FULL.top_k], ref["w"], rtol=2e-6)
     np.testing.assert_allclose(w[0, FULL.top_k], ref["gate"][0], rtol=2e-6)
-    ok, info = tolerance_check(bf16_np(out).reshape(1, -1), ref["out"], bf16_output=True)
+    ok, info = tolerance_check(bf16_np(out).reshape(1, -1), ref["out"])
     assert ok, info
 
 
@@ -83,5 +87,60 @@ def test_decode_without_shared_expert(orc):
     torch.cuda.synchronize()
     lg = to_np(dec.view("logits", (1, 32), torch.float32))
     ref = orc.moe_forward(x, host, shape, logits_in=lg)
-    ok, info = tolerance_check(bf16_np(out).reshape(1, -1), ref["out"], bf16_output=True)
+    ok, info = tolerance_check(bf16_np(out).reshape(1, -1), ref["out"])
     assert ok, info
+
+
+def test_decode_chain_in_graph_matches_oracle(orc):
+    """Layers of distinct weights chained through their outputs inside one
+    captured graph (the decode step's schedule): every layer's output is held
+    to the bar against the oracle run on that layer's own input (the previous
+    layer's bf16 output as the GPU produced it) and logits, and the graph's
+    outputs equal an eager run of the same chain bit for bit.
+
+    Bare MoE layers (no normalisation between them, unlike a model) map an
+    input of rms r to an output of rms about 4.4 r^2 with these weights, so a
+    chain of them grows or dies out within a few layers. The first input is
+    N(0,1) scaled by 0.1, which keeps the six outputs' rms between 0.006 and
+    44 (measured with the oracle), inside the 16-bit formats' normal range."""
+    from bit_moe_expert_route_gb300 import ops
+    NL = 6
+    hosts = [synth.layer_weights(FULL, seed=11, layer=l) for l in range(NL)]
+    decs = [ops.Decode(ops.DeviceLayer(h, FULL)) for h in hosts]
+    xs = synth.f32_to_bf16(0.1 * synth.bf16_to_f32(synth.tokens(FULL, 1, seed=11, tensor=synth.X_DECODE)))
+    x0 = torch.from_numpy(xs.view(np.int16)).cuda().view(-1)
+    outs = torch.zeros(NL, FULL.d_model, dtype=torch.bfloat16, device="cuda")
+
+    def chain():
+        for l in range(NL):
+            decs[l](x0 if l == 0 else outs[l - 1].view(torch.int16), outs[l])
+
+    chain()
+    torch.cuda.synchronize()
+    eager = outs.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        chain()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chain()
+    for _ in range(3):
+        outs.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    for d in decs:
+        assert ops.device_status(d.ws) == 0
+    assert torch.equal(outs.view(torch.int16), eager.view(torch.int16))
+    xin = to_np(x0.view(1, -1)).view(np.uint16)
+    for l in range(NL):
+        lg = to_np(decs[l].view("logits", (1, FULL.n_experts), torch.float32))
+        ref_free = orc.moe_forward(xin, hosts[l], FULL)
+        np.testing.assert_allclose(lg, ref_free["logits"], rtol=1e-5, atol=2e-5)
+        ref = orc.moe_forward(xin, hosts[l], FULL, logits_in=lg)
+        ids = to_np(decs[l].view("topk_ids", (1, FULL.top_k), torch.int32))
+        assert np.array_equal(ids, ref["ids"]), l
+        ok, info = tolerance_check(bf16_np(outs[l]).reshape(1, -1), ref["out"])
+        assert ok, (l, info)
+        xin = to_np(outs[l].view(torch.int16)).view(np.uint16).reshape(1, -1)

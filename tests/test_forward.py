@@ -6,18 +6,25 @@ Per configuration (T = 64, 512, 4096, 32768 with the Zipf router bias):
      against the oracle's routing of those same logits (all tokens);
   3. the layer result matches the oracle run on the GPU's logits (so both
      sides take the same top-k decision) within max|err| <= 2e-2 rms(ref) and
-     rel-L2 <= 5e-3 -- on every token at T <= 512, on a sample of tokens (the
-     first, last and a seeded spread, covering the ragged tails) above. The bar
-     is applied to the fp32 result before its final bf16 store (that store
-     alone can move an element by 0.125 when |v| >= 32, more than the bar
-     allows when rms < 6.25), and the bf16 output must be exactly the
-     round-to-nearest-even of that fp32 result.
+     rel-L2 <= 5e-3, on every token up to T = 4096. At T = 32768 the default
+     run checks 1536 tokens (the first and last 512, which hold the ragged
+     tails of the hottest experts' tiles, and a seeded spread); with
+     MOE_RUN_SLOW=1 the slow-marked test checks all 32768. The bar holds for
+     the fp32 result before its final store; the bf16 output must be exactly
+     the round-to-nearest-even of that fp32 result, and meets the bar itself
+     wherever a bf16 store can (see gpu_util.bf16_output_check).
+
+The oracle's output for one set of logits is cached, so the variants of one
+configuration (tile heights, deterministic combine) share one oracle run.
 """
+import hashlib
+import os
+
 import numpy as np
 import pytest
 
 from bit_moe_expert_route_gb300 import synth
-from gpu_util import FULL, bf16_np, to_np, tolerance_check
+from gpu_util import FULL, bf16_np, bf16_output_check, to_np, tolerance_check
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -35,14 +42,49 @@ def dev_layers(host_layer):
     return {False: ops.DeviceLayer(host_layer, FULL), True: ops.DeviceLayer(zipf, FULL)}
 
 
-def sample_tokens(T, n=48, seed=0):
-    if T <= 512:
+def sample_tokens(T, seed=0):
+    if T <= 4096:
         return np.arange(T)
-    rng = synth.uniform_int(synth.key(seed, 0, 500), n, T)
-    return np.unique(np.concatenate([[0, 1, T - 1], rng]))
+    rng = synth.uniform_int(synth.key(seed, 0, 500), 512, T)
+    return np.unique(np.concatenate([np.arange(512), np.arange(T - 512, T), rng]))
 
 
-def run_layer(orc, host_layer, dev_layers, T, zipf, block_n=0, deterministic=False):
+def windowed_block_map(m, T, E, k, bn, W):
+    """The block map cut per token window of W tokens, derived from the oracle's
+    routing (offsets, and row_token of each position in expert order): for each
+    window, every expert's rows whose tokens fall in it (contiguous, since the
+    oracle's scatter is stable) in tiles of bn, then the window's shared rows."""
+    off, rt = m["offsets"], m["row_token"]
+    tiles = []
+    for t0 in range(0, T, W):
+        t1 = min(T, t0 + W)
+        for e in range(E):
+            pos = np.arange(off[e], off[e + 1])
+            sel = pos[(rt[pos] >= t0) & (rt[pos] < t1)]
+            if len(sel):
+                assert np.array_equal(sel, np.arange(sel[0], sel[0] + len(sel)))
+            for j in range(0, len(sel), bn):
+                tiles.append([e, sel[0] + j, min(bn, len(sel) - j), 0])
+        for j in range(0, t1 - t0, bn):
+            tiles.append([E, T * k + t0 + j, min(bn, t1 - t0 - j), 0])
+    return np.array(tiles, np.int32).reshape(-1, 4)
+
+
+_ORACLE_CACHE = {}
+
+
+def oracle_layer(orc, x, host, lg):
+    """The oracle's layer output on the GPU's logits, cached by the inputs' bytes."""
+    h = hashlib.sha1()
+    for a in (x, lg, host["router_bias"] if host["router_bias"] is not None else np.zeros(1)):
+        h.update(np.ascontiguousarray(a).tobytes())
+    key = h.hexdigest()
+    if key not in _ORACLE_CACHE:
+        _ORACLE_CACHE[key] = orc.moe_forward(x, host, FULL, logits_in=lg)
+    return _ORACLE_CACHE[key]
+
+
+def run_layer(orc, host_layer, dev_layers, T, zipf, block_n=0, deterministic=False, all_tokens=False):
     from bit_moe_expert_route_gb300 import ops
     host = dict(host_layer, router_bias=synth.zipf_router_bias(FULL.n_experts) if zipf else None)
     fwd = ops.Forward(dev_layers[zipf], T, block_n, deterministic=deterministic)
@@ -52,7 +94,7 @@ def run_layer(orc, host_layer, dev_layers, T, zipf, block_n=0, deterministic=Fal
     assert ops.device_status(fwd.ws) == 0
     E, k = FULL.n_experts, FULL.top_k
     lg = to_np(fwd.view("logits", (T, E), torch.float32))
-    idx = sample_tokens(T)
+    idx = np.arange(T) if all_tokens else sample_tokens(T)
     # 1. router logits
     ref_lg, ref_gl = orc.router(x[idx], host["router"], host["shared_gate"])
     np.testing.assert_allclose(lg[idx], ref_lg, rtol=1e-5, atol=2e-5)
@@ -70,20 +112,22 @@ def run_layer(orc, host_layer, dev_layers, T, zipf, block_n=0, deterministic=Fal
     assert np.array_equal(to_np(fwd.view("block_map", (nt, 4), torch.int32)), m["block_map"])
     v = fwd.views
     if v.down_block_map != v.block_map:  # the down projection's own, taller tiles
-        m2 = orc.route_meta(ids, E, v.down_block_n, True)
+        if v.down_window:
+            want = windowed_block_map(m, T, E, k, v.down_block_n, v.down_window)
+        else:
+            want = orc.route_meta(ids, E, v.down_block_n, True)["block_map"]
         nt2 = int(to_np(fwd.view("down_num_tiles", (1,), torch.int32))[0])
-        assert nt2 == m2["num_tiles"] <= v.down_max_tiles
-        assert np.array_equal(to_np(fwd.view("down_block_map", (nt2, 4), torch.int32)),
-                              m2["block_map"])
+        assert nt2 == len(want) <= v.down_max_tiles
+        assert np.array_equal(to_np(fwd.view("down_block_map", (nt2, 4), torch.int32)), want)
     # 3. layer output
-    ref = orc.moe_forward(x[idx], host, FULL, logits_in=lg[idx])
+    ref = oracle_layer(orc, x[idx], host, lg[idx])
     assert np.array_equal(ref["ids"], ids[idx])
     acc = to_np(fwd.view("out_acc", (T, FULL.d_model), torch.float32))
     ok, info = tolerance_check(acc[idx], ref["out"])
     assert ok, info
     # the bf16 output is exactly RNE(fp32 result), every token
     assert np.array_equal(to_np(out.view(torch.int16)).view(np.uint16), synth.f32_to_bf16(acc))
-    ok, info_bf16 = tolerance_check(bf16_np(out)[idx], ref["out"], bf16_output=True)
+    ok, info_bf16 = bf16_output_check(bf16_np(out)[idx], ref["out"])
     assert ok, info_bf16
     return m, info
 
@@ -106,6 +150,14 @@ def test_forward_T32768_zipf(orc, host_layer, dev_layers):
     m, _ = run_layer(orc, host_layer, dev_layers, 32768, True)
     c = m["counts"]
     assert c.max() > 10 * c.mean() and (c == 0).sum() >= 2
+
+
+@pytest.mark.slow
+@pytest.mark.skipif(os.environ.get("MOE_RUN_SLOW") != "1",
+                    reason="every-token check at T = 32768 (minutes of oracle time): MOE_RUN_SLOW=1")
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_forward_T32768_zipf_every_token(orc, host_layer, dev_layers, deterministic):
+    run_layer(orc, host_layer, dev_layers, 32768, True, deterministic=deterministic, all_tokens=True)
 
 
 def test_forward_small_shapes(orc):
@@ -136,7 +188,7 @@ def test_forward_small_shapes(orc):
         acc = to_np(fwd.view("out_acc", (T, shape.d_model), torch.float32))
         ok, info = tolerance_check(acc, ref["out"])
         assert ok, (shape, T, info)
-        ok, info = tolerance_check(bf16_np(out), ref["out"], bf16_output=True)
+        ok, info = bf16_output_check(bf16_np(out), ref["out"])
         assert ok, (shape, T, info)
 
 
