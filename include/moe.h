@@ -162,8 +162,11 @@ int moe_route(const float* logits, const float* logit_bias, int T, int n_experts
 /*
  * moe_grouped_gemm_w4a16: grouped GEMM over row tiles with 4-bit weights
  * dequantised on chip ("Prefill optimizations", first bullet). Tensor-core
- * (tcgen05) kernel: packed tiles arrive by TMA, are unpacked to bf16 in
- * shared memory and multiplied with fp32 accumulation in tensor memory.
+ * (tcgen05) kernel: packed tiles arrive by TMA and are unpacked to the
+ * operand type (f16 or bf16, as operand_format says) into the MMA's A
+ * operand, in tensor memory where it fits beside two accumulator buffers
+ * (always for a single weight matrix, e.g. the down projection) and in
+ * shared memory otherwise; products accumulate in fp32 in tensor memory.
  *
  *   A           [A_rows][K] device, row-major (K contiguous), bf16 or f16 as
  *               operand_format says (moe_operand_format).
