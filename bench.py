@@ -47,6 +47,7 @@ def parse():
     ap.add_argument("--prefill-iters", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-gdn", action="store_true", help="skip the Gated DeltaNet scan lines")
+    ap.add_argument("--no-attn", action="store_true", help="skip the decode-attention lines")
     ap.add_argument("--profile", choices=["decode", "prefill", "prefill-det", "decode-batch"],
                     help="no measurement: run one layer repeatedly (decode: 20 + 200 calls; prefill: "
                          "3 forwards at --profile-T tokens; prefill-det: the same with "
@@ -379,6 +380,59 @@ def run_gdn(args, peaks):
     )
 
 
+# Decode attention with grouped KV heads (a reading: the pages give no sizes;
+# 16 query heads, 2 KV heads of 256, as in the public Qwen3-Next-style
+# configuration); the model has 10 such layers.
+ATTN_SHAPE = dict(Hq=16, Hkv=2, d=256)
+ATTN_LAYERS = 10
+
+
+def run_attn(args, peaks):
+    """moe_decode_attention on seeded bf16 q, K, V ~ N(0, 1): one new token over a
+    cache of L positions, L = 4096 and 32768; 10 layers (distinct caches) in one
+    CUDA graph, L2 flushed before every replay. Bound: HBM, for the K and V bytes
+    read once (2 * L * Hkv * d * 2 per layer)."""
+    import torch
+    from bit_moe_expert_route_gb300 import ops
+    Hq, Hkv, d = ATTN_SHAPE["Hq"], ATTN_SHAPE["Hkv"], ATTN_SHAPE["d"]
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    stream = torch.cuda.Stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    res = []
+    for L in (4096, 32768):
+        layers = []
+        for _ in range(ATTN_LAYERS):
+            q = torch.randn(Hq, d, device="cuda", generator=gen).to(torch.bfloat16)
+            K = torch.randn(L, Hkv, d, device="cuda", generator=gen).to(torch.bfloat16)
+            V = torch.randn(L, Hkv, d, device="cuda", generator=gen).to(torch.bfloat16)
+            out = torch.empty(Hq, d, dtype=torch.float32, device="cuda")
+            nbytes = ops.lib().moe_decode_attention_workspace_bytes(L, Hq, Hkv, d)
+            ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+            layers.append((q, K, V, out, ws))
+
+        def step():
+            for q, K, V, out, ws in layers:
+                ops.decode_attention(q, K, V, out=out, ws=ws)
+        g = gpu_graph(step, stream)
+        for _ in range(3):
+            g.replay()
+        t = statistics.median(timed_replays(g, stream, args.prefill_iters, flush)) / ATTN_LAYERS
+        kv = 2 * L * Hkv * d * 2
+        gbs = kv / t / 1e9
+        res.append(dict(L=L, us_per_layer=round(t * 1e6, 3),
+                        roofline=dict(bound="hbm", achieved=round(gbs, 1), peak=peaks["hbm_gbs"],
+                                      unit="GB/s", frac=round(gbs / peaks["hbm_gbs"], 4),
+                                      bytes_per_layer=kv,
+                                      kernel="attn_split_kernel + attn_combine_kernel: all query "
+                                             "heads of a KV head per block, each K/V row read once")))
+        del layers, g
+    del flush
+    torch.cuda.empty_cache()
+    return dict(shape=dict(ATTN_SHAPE, layers=ATTN_LAYERS), configs=res,
+                gpu_launches_per_step=2 * ATTN_LAYERS,
+                l2="flushed (512 MB write) before every timed replay")
+
+
 EXPERT_BYTES = 1_769_472       # one expert's packed codes, scales and biases (3 projections)
 ROUTER_BYTES = 2_105_344       # fp32 router [2048][256] and w_sg
 
@@ -708,6 +762,7 @@ def main():
         for T, zipf in ((64, False), (512, False), (4096, False), (32768, True)):
             prefill.append(run_prefill(T, zipf, host0, args, peaks))
     gdn = None if args.no_gdn else run_gdn(args, peaks)
+    attn = None if args.no_attn else run_attn(args, peaks)
     line = {
         "metric": BASELINE_METRIC, "value": round(res["value"], 2), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -725,6 +780,8 @@ def main():
         line["prefill"] = prefill
     if gdn:
         line["gdn_scan"] = gdn
+    if attn:
+        line["decode_attention"] = attn
     if rank == 0:
         print(json.dumps(line), flush=True)
     barrier(world)

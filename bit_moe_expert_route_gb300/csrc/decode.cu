@@ -8,26 +8,32 @@
 // One persistent launch per layer: G blocks (one per SM), 256 threads each.
 //   before the dependency wait (griddepcontrol.wait; nothing here depends on
 //     the previous kernel): TMA bulk copies of this block's shared-expert
-//     gate/up rows and shared-expert down rows into shared memory, and
-//     register loads of its slice of the router.
+//     gate/up rows and shared-expert down rows into shared memory, register
+//     loads of its slice of the router; every copy barrier is armed with its
+//     byte count (the counts do not depend on the routing).
 //   phase A  x into shared memory (one round trip); router partial logits
-//     over this block's (8 experts x d/KS rows) slice and the matching partial
-//     of the shared gate logit x . w_sg; h of its shared-expert rows.
-//   phase B  every block polls the KS partials of each logit (summed in a
-//     fixed order), selects the top k itself (two-level rank count,
-//     descending, ties to the lower id) and issues its bulk copies: the
-//     routed gate/up rows of its share of the k * d_ff row pairs and the
-//     routed down rows of its share of the d_model outputs; then h of its
-//     row pairs.
+//     over this block's (8 experts x d/KS rows) slice and the matching
+//     partial of the shared gate logit x . w_sg, published at once; then h of
+//     the block's shared-expert rows, while the partials travel.
+//   phase B  thread e polls the KS partials of expert e's logit (summed in a
+//     fixed order); each warp ranks its 32 logits by register shuffles, the
+//     warps' top-k candidates are ranked among themselves (descending, ties
+//     to the lower id), and the last warp issues the block's bulk copies of
+//     the selected experts' rows: its routed gate/up row pairs in two groups
+//     with a barrier each (rows land, and are computed, group by group), then
+//     its share of every slot's down rows. The other warps compute h of each
+//     routed row-pair group as it lands; the issuing warp computes the
+//     routing weights.
 //   phase C  every block polls h of every slot into shared memory and
 //     computes its outputs: every slot's down row, weighted, in slot order,
 //     rounded once to bf16.
 // Cross-block values are published as 64-bit {value, call epoch} words, so a
 // reader's poll is both the synchronisation and the load: one L2 round trip
-// per dependency. Block 0 stores the epoch for the next call at its end; no
-// counter needs resetting, so consecutive calls on one workspace stay one
-// chain of programmatic dependent launches, and the next layer's blocks
-// (two blocks fit per SM) fetch their weights while this layer runs.
+// per dependency. Block 0 stores the epoch
+// for the next call at its end; no counter needs resetting, so consecutive
+// calls on one workspace stay one chain of programmatic dependent launches,
+// and the next layer's blocks (two blocks fit per SM) fetch their weights
+// while this layer runs.
 //
 // Every block runs each phase once per launch, so the kernel's instruction
 // footprint, fetched cold from L2 on every SM, matters as much as its
@@ -44,6 +50,7 @@
 // f stays in [1, 2), so the fp32 sums cancel no more than a factor of a few.
 // x enters as its own bf16 values; h (the SwiGLU output) enters the down
 // projection rounded to f16, as in the prefill path.
+#include <algorithm>
 #include <climits>
 #include <mutex>
 
@@ -57,7 +64,10 @@ namespace {
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kIssueWarp = kDecWarps - 1;  // issues the routed copies, then the routing weights
 constexpr int kRouterPre = 2;  // router rows per thread loaded before the dependency wait
+constexpr int kYGroups = 2;    // routed row-pair groups, each with its own copy barrier
+static_assert(kDecodeMaxExperts == kDecThreads, "one expert per thread in the top-k");
 
 MOE_DEVINL void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 MOE_DEVINL void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
@@ -72,12 +82,12 @@ MOE_DEVINL void bulk_load(void* smem_dst, const void* src, uint32_t bytes, uint6
 }
 
 // Bounded wait on a shared-memory barrier phase (every thread).
-MOE_DEVINL void bar_wait(uint64_t* bar, uint32_t parity, int32_t* status, int where) {
+MOE_DEVINL void bar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns, int32_t* status, int where) {
   if (mbar_try_wait(bar, parity)) return;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return;
-    if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+    if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) {
       report(status, MOE_DEV_TIMEOUT, where, (int)threadIdx.x);
       return;
     }
@@ -92,10 +102,10 @@ MOE_DEVINL float2 affine_f(uint16_t sbits, uint16_t bbits) {
 }
 
 // ---------------------------------------------------------------- publishing
-// Values other blocks read (router partials, h) are published as 64-bit words
-// {value bits, call epoch}: a reader polls a word until its epoch is this
-// call's, so one L2 round trip both synchronises and delivers the value. The
-// epoch is one more than the last call's (kept in the workspace by block 0).
+// Values other blocks read are published as 64-bit words {payload, call
+// epoch}: a reader polls a word until its epoch is this call's, so one L2
+// round trip both synchronises and delivers the value. The epoch is one more
+// than the last call's (kept in the workspace by block 0).
 MOE_DEVINL void publish(unsigned long long* w, float v, uint32_t epoch) {
   const unsigned long long x = ((unsigned long long)epoch << 32) | __float_as_uint(v);
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(w), "l"(x) : "memory");
@@ -115,11 +125,11 @@ MOE_DEVINL float word_value(unsigned long long x) { return __uint_as_float((uint
 struct Poll {
   uint64_t t0 = 0;
   uint32_t i = 0;
-  MOE_DEVINL bool again(int32_t* status, int where) {
+  MOE_DEVINL bool again(uint64_t limit_ns, int32_t* status, int where) {
     if (++i == 32) t0 = globaltimer_ns();
     if (i > 32) {
       __nanosleep(32);
-      if ((i & 63) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+      if ((i & 63) == 0 && globaltimer_ns() - t0 > limit_ns) {
         report(status, MOE_DEV_TIMEOUT, where, (int)blockIdx.x);
         return false;
       }
@@ -136,58 +146,58 @@ struct Poll {
 //   X   down rows per slot s (S = k routed + shared): codes [capX][f/2],
 //       scale, bias [capX][f/64] each.
 //   Z   the shared expert's row pairs, laid out as in Y with capS rows.
-//   XP  x as bf16 pairs (see pair_slot) [d/32 chunks][4 words], then the x
+//   U   x as bf16 pairs (see pair_slot) [d/32 chunks][4 words], then the x
 //       chunk sums (fp32 [d/32]).
-//   K   the keys [E] and the top-k candidates.
-//   then the selection and reduction scratch and the two bulk-copy barriers.
+//   then the selection scratch and the bulk-copy barriers. The router's
+//   reduction scratch and the top-k candidates live at the start of Y,
+//   which receives no copy before the selection is complete (two blocks per
+//   SM need every byte).
 struct DecSmem {
   uint8_t* Y;
   uint8_t* X;
   uint8_t* Z;
   uint4* xp;        // [d/32 * 4]
   float* xsum;      // [d/32]
-  float* keys;      // [E]
   float* cand_key;  // [8 * kc]
   int* cand_id;     // [8 * kc]
   int* s_ids;       // [32]
   float* s_z;       // [32]
-  float* s_w;       // [33]: routing weights, then the shared gate
+  float* s_w;       // [34]: routing weights, then the shared gate
   float* red;       // [8][9]
   float* s_gp;      // [kDecodeMaxSplits] gate-logit partials
   uint32_t* s_epoch;
-  uint64_t* barY;
+  uint64_t* barY;   // [kYGroups]
   uint64_t* barX;
   uint64_t* barZ;
 };
+
+MOE_DEVINL int cand_per_warp(const DecodeParams& p) { return min(p.k, 32); }
 
 MOE_DEVINL DecSmem carve_dec_smem(uint8_t* base, const DecodeParams& p) {
   DecSmem m;
   m.Y = base;
   m.X = base + p.y_bytes;
   m.Z = m.X + p.x_bytes;
+  m.red = reinterpret_cast<float*>(base);  // aliases in Y (see above)
+  m.cand_key = m.red + 8 * 9;
+  m.cand_id = reinterpret_cast<int*>(m.cand_key + kDecWarps * cand_per_warp(p));
   uint8_t* u = m.Z + p.z_bytes;
   m.xp = reinterpret_cast<uint4*>(u);
   m.xsum = reinterpret_cast<float*>(u + (size_t)p.d * 2);
-  m.keys = m.xsum + ((p.d / 32 + 3) & ~3);
-  const int kc = min(p.k, p.E / 8);
-  m.cand_key = m.keys + p.E;
-  m.cand_id = reinterpret_cast<int*>(m.cand_key + 8 * kc);
   float* f = reinterpret_cast<float*>(u + p.u_bytes);
   m.s_ids = reinterpret_cast<int*>(f);
   f += 32;
   m.s_z = f;
   f += 32;
   m.s_w = f;
-  f += 40;
-  m.red = f;
-  f += 8 * 9;
+  f += 34;
   m.s_gp = f;
   f += kDecodeMaxSplits;
   m.s_epoch = reinterpret_cast<uint32_t*>(f);
   f += 2;
   m.barY = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(f) + 7) & ~uintptr_t(7));
-  m.barX = m.barY + 1;
-  m.barZ = m.barY + 2;
+  m.barX = m.barY + kYGroups;
+  m.barZ = m.barX + 1;
   return m;
 }
 
@@ -199,7 +209,7 @@ MOE_DEVINL int pair_slot(int c, int j) { return c * 4 + (j ^ ((c >> 1) & 3)); }
 // 16-bit element index of value i inside that layout.
 MOE_DEVINL int pair_elem(int i) { return pair_slot(i >> 5, (i >> 3) & 3) * 8 + (i & 3) * 2 + ((i >> 2) & 1); }
 
-// Row-pair views inside Y.
+// Row-pair views inside Y (or Z).
 struct RowPairSmem {
   const uint4* gq;
   const uint4* uq;
@@ -224,23 +234,21 @@ MOE_DEVINL uint32_t word_of(const uint4& q, int j) { return j == 0 ? q.x : j == 
 // v * 1/(1 + e^-v) with a correctly rounded reciprocal (no division slow path)
 MOE_DEVINL float silu(float v) { return v * __frcp_rn(1.f + expf(-v)); }
 
-// h of rows [0, n) of Y (row i = flattened row pair r0 + i), four rows per
-// warp per pass (rows i, i+8, i+16, i+24; those past n run as duplicates of
-// row i): h = silu(x . g) * (x . u), published and stored plainly for the
-// workspace view. Lanes take the 32-code chunks c = lane, lane + 32, ...;
-// 16 independent FMA chains each.
-constexpr int kRowsPerPass = 4;
+// h of rows [i0, i1) of a row-pair region (region row i = flattened row
+// pair r0 + i), by warps [w0, w0 + nw): two consecutive rows per warp per
+// pass (a row past i1 runs as a duplicate): h = silu(x . g) * (x . u),
+// stored plainly for the workspace view and published. Lanes take the
+// 32-code chunks c = lane, lane + 32, ...; 8 independent FMA chains each.
+constexpr int kRowsPerPass = 2;
 __device__ __noinline__ void rows_h(const DecodeParams& p, const uint8_t* Y, int cap, const uint4* xp,
-                                    const float* xsum, int n, int r0, uint32_t epoch) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, d = p.d, nch = d / 32;
+                                    const float* xsum, int i0, int i1, int r0, int w0, int nw,
+                                    uint32_t epoch) {
+  const int lane = threadIdx.x & 31, wr = (int)(threadIdx.x >> 5) - w0, d = p.d, nch = d / 32;
 #pragma unroll 1
-  for (int i = warp; i < n; i += kRowsPerPass * kDecWarps) {
+  for (int i = i0 + kRowsPerPass * wr; i < i1; i += kRowsPerPass * nw) {
     RowPairSmem r[kRowsPerPass];
 #pragma unroll
-    for (int t = 0; t < kRowsPerPass; ++t) {
-      const int it = i + t * kDecWarps;
-      r[t] = rowpair_smem(Y, cap, it < n ? it : i, d);
-    }
+    for (int t = 0; t < kRowsPerPass; ++t) r[t] = rowpair_smem(Y, cap, i + t < i1 ? i + t : i, d);
     float acc[2 * kRowsPerPass];  // gate, up of each row
 #pragma unroll
     for (int m = 0; m < 2 * kRowsPerPass; ++m) acc[m] = 0.f;
@@ -274,16 +282,16 @@ __device__ __noinline__ void rows_h(const DecodeParams& p, const uint8_t* Y, int
     for (int off = 16; off > 0; off >>= 1)
 #pragma unroll
       for (int m = 0; m < 2 * kRowsPerPass; ++m) acc[m] += __shfl_xor_sync(kFull, acc[m], off);
-    if (lane < kRowsPerPass && i + lane * kDecWarps < n) {
-      float g = acc[0], u = acc[1];
+    float g = acc[0], u = acc[1];
 #pragma unroll
-      for (int t = 1; t < kRowsPerPass; ++t)
-        if (lane == t) {
-          g = acc[2 * t];
-          u = acc[2 * t + 1];
-        }
-      const int row = r0 + i + lane * kDecWarps;
+    for (int t = 1; t < kRowsPerPass; ++t)
+      if (lane == t) {
+        g = acc[2 * t];
+        u = acc[2 * t + 1];
+      }
+    if (lane < kRowsPerPass && i + lane < i1) {
       const float v = silu(g) * u;
+      const int row = r0 + i + lane;
       p.h[row] = v;
       publish(p.pub_h + row, v, epoch);
     }
@@ -343,7 +351,8 @@ __device__ __noinline__ void down_cols(const DecodeParams& p, const uint8_t* X, 
 }
 
 // Bulk copies of row pairs [r0, r0 + n) of one expert's gate/up into Y slots
-// [i0, i0 + n).
+// [i0, i0 + n): codes of gate and up, then gate scale, gate bias, up scale,
+// up bias. `lane_of`/`lanes`: the calling lane's share of the six copies.
 __device__ __noinline__ void issue_rowpairs(uint8_t* Y, int capY, int i0, const moe_w4_t& G,
                                             const moe_w4_t& U, int64_t r0, int n, int d, uint64_t* bar) {
   const uint32_t half_row = d / 2, sbytes = d / 32;  // codes and scale bytes per row
@@ -372,83 +381,41 @@ __device__ __noinline__ void issue_down(uint8_t* X, int capX, int s, const moe_w
             reinterpret_cast<const uint8_t*>(D.bias) + r0 * sbytes, n * sbytes, bar);
 }
 
-// Routed row pairs [r0, r0 + n) of the flattened (slot, row) order into Y
-// slots [0, n), split where a slot (expert) ends.
-__device__ __noinline__ void issue_routed(const DecodeParams& p, uint8_t* Y, const int* ids, int r0,
-                                          int n, uint64_t* bar) {
-  for (int i = 0; i < n;) {
-    const int r = r0 + i, slot = r / p.f, row = r % p.f;
-    const int seg = min(n - i, p.f - row);
-    issue_rowpairs(Y, p.capY, i, p.w.gate, p.w.up, (int64_t)ids[slot] * p.f + row, seg, p.d, bar);
-    i += seg;
-  }
-}
-
-// Down rows [j0, j0 + n) of every slot (routed ones, then the shared one if
-// `with_shared`) into X.
-__device__ __noinline__ void issue_down_all(const DecodeParams& p, uint8_t* X, const int* ids, int j0,
-                                            int n, bool with_shared, uint64_t* bar) {
-  for (int s = 0; s < p.k; ++s) issue_down(X, p.capX, s, p.w.down, ids[s], j0, n, p.d, p.f, bar);
-  if (with_shared) issue_down(X, p.capX, p.k, p.w.sh_down, 0, j0, n, p.d, p.f, bar);
-}
-
-// The selected experts' first chunks, one bulk copy per lane (so a batch
-// goes out in a few warp instructions): routed gate/up rows [r0, r0 + n)
-// into Y (6 copies per segment of one expert: codes of gate and up, then
-// gate scale, gate bias, up scale, up bias), then down rows [j0, j0 + nj)
-// of each routed slot into X (codes, scale, bias). Called by a whole warp.
-__device__ __noinline__ void issue_selected(const DecodeParams& p, uint8_t* Y, uint8_t* X, const int* ids,
-                                            int r0, int n, int j0, int nj, uint64_t* barY, uint64_t* barX) {
-  const int lane = threadIdx.x & 31, d = p.d, f = p.f;
-  const uint32_t hq = d / 2, hs = d / 32;  // gate/up row: code bytes, scale bytes
-  const uint32_t dq = f / 2, ds = f / 32;  // down row
-  const int nseg = n > 0 ? (r0 + n - 1) / f - r0 / f + 1 : 0;
-  const int nq = 6 * nseg + (nj > 0 ? 3 * p.k : 0);
-  for (int q = lane; q < nq; q += 32) {
-    uint8_t* dst;
-    const uint8_t* src;
-    uint32_t bytes;
-    uint64_t* bar;
-    if (q < 6 * nseg) {
-      const int si = q / 6, kind = q % 6, slot = r0 / f + si;
-      const int lo = max(r0, slot * f), hi = min(r0 + n, (slot + 1) * f);
-      const int i0 = lo - r0, len = hi - lo;
-      const int64_t grow = (int64_t)ids[slot] * f + (lo - slot * f);
-      const moe_w4_t& W = (kind == 1 || kind >= 4) ? p.w.up : p.w.gate;
-      if (kind < 2) {
-        dst = Y + ((size_t)(kind ? p.capY : 0) + i0) * hq;
-        src = reinterpret_cast<const uint8_t*>(W.q) + grow * hq;
-        bytes = len * hq;
-      } else {
-        const int m = kind - 2;  // gate scale, gate bias, up scale, up bias
-        dst = Y + (size_t)p.capY * d + ((size_t)m * p.capY + i0) * hs;
-        src = reinterpret_cast<const uint8_t*>((m & 1) ? W.bias : W.scale) + grow * hs;
-        bytes = len * hs;
+// The block's routed region rows (flattened (slot, row) index y0 + i = slot
+// * f + row; group g holds region rows [gb[g], gb[g + 1])) cut at group and
+// slot boundaries, issued by lane 0 in order, group 0 first, so that the
+// groups land in that order; then the down rows [j0, j0 + nj) of every
+// routed slot (three copies, one lane per slot). Called by a whole warp.
+__device__ __noinline__ void issue_routed(const DecodeParams& p, uint8_t* Y, uint8_t* X, const int* ids,
+                                          int y0, const int* gb, int ng, int j0, int nj, uint64_t* barY,
+                                          uint64_t* barX) {
+  const int lane = threadIdx.x & 31, f = p.f;
+  if (lane == 0)
+    for (int g = 0; g < ng; ++g) {
+      for (int a = gb[g]; a < gb[g + 1];) {
+        const int r = y0 + a, slot = r / f, row = r % f;
+        const int len = min(gb[g + 1] - a, f - row);
+        issue_rowpairs(Y, p.capY, a, p.w.gate, p.w.up, (int64_t)ids[slot] * f + row, len, p.d, barY + g);
+        a += len;
       }
-      bar = barY;
-    } else {
-      const int qq = q - 6 * nseg, s = qq / 3, kind = qq % 3;
-      const int64_t r = (int64_t)ids[s] * d + j0;
-      uint8_t* base = X + (size_t)s * p.capX * (dq + 2 * ds);
-      if (kind == 0) {
-        dst = base;
-        src = reinterpret_cast<const uint8_t*>(p.w.down.q) + r * dq;
-        bytes = nj * dq;
-      } else {
-        dst = base + (size_t)p.capX * dq + (size_t)(kind - 1) * p.capX * ds;
-        src = reinterpret_cast<const uint8_t*>(kind == 1 ? p.w.down.scale : p.w.down.bias) + r * ds;
-        bytes = nj * ds;
-      }
-      bar = barX;
     }
-    bulk_load(dst, src, bytes, bar);
-  }
+  __syncwarp();
+  if (nj > 0)
+    for (int s = lane; s < p.k; s += 32) issue_down(X, p.capX, s, p.w.down, ids[s], j0, nj, p.d, f, barX);
 }
 
 // [lo, hi) of `units` work units for block b of G, scaled by `gran`.
 MOE_DEVINL int2 block_range(int units, int b, int G, int gran) {
   const int lo = (int)((int64_t)units * b / G), hi = (int)((int64_t)units * (b + 1) / G);
   return make_int2(lo * gran, hi * gran);
+}
+
+// The groups of region rows [0, n) (n a multiple of q, the rows a bulk copy
+// moves at least: a row's scales are d/32 bytes, a copy a multiple of 16):
+// kYGroups nearly equal parts, each a multiple of q rows.
+MOE_DEVINL void y_groups(int n, int q, int* gb) {
+  const int units = n / q, ng = units >= kYGroups ? kYGroups : 1;
+  for (int g = 0; g <= kYGroups; ++g) gb[g] = g >= ng ? n : (units * g / ng) * q;
 }
 
 // ---------------------------------------------------------------- kernel
@@ -466,27 +433,37 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_layer_kernel(const __gr
   const int2 sr = p.shared ? block_range(f / p.qrow, b, G, p.qrow) : make_int2(0, 0);  // shared row pairs
   const int2 orng = block_range(d / p.qout, b, G, p.qout);                          // outputs
   const int nj0 = min(orng.y - orng.x, p.capX);
+  const int nr0 = min(rr.y - rr.x, p.capY);
+  const int kc = cand_per_warp(p);
+  int gb[kYGroups + 1];
+  y_groups(nr0, p.qrow, gb);
 
   if (tid == 0) {
-    mbar_init(sm.barY, 1);
+    for (int g = 0; g < kYGroups; ++g) mbar_init(sm.barY + g, 1);
     mbar_init(sm.barZ, 1);
-    mbar_init(sm.barX, 2);  // each X chunk: shared-slot arrival + routed-slot arrival
+    mbar_init(sm.barX, 1);
     fence_mbar_init();
   }
+  for (int i = tid; i < kDecWarps * kc; i += kDecThreads) {
+    sm.cand_key[i] = -INFINITY;
+    sm.cand_id[i] = INT_MAX;
+  }
+  if (tid < 32) sm.s_ids[tid] = tid < k ? tid : 0;  // overwritten by the selection
   __syncthreads();
 
-  // ---- before the dependency wait: weights only (nothing the previous kernel writes)
+  // ---- before the dependency wait: weights only (nothing the previous
+  // kernel writes); every barrier armed with the bytes it will receive
   if (warp == 0) {
     const int ns0 = min(sr.y - sr.x, p.capS), njs = p.shared ? nj0 : 0;
     if (lane == 0) {
       mbar_arrive_expect_tx(sm.barZ, ns0 * rp_bytes);
-      mbar_arrive_expect_tx(sm.barX, njs * dn_bytes);
+      mbar_arrive_expect_tx(sm.barX, (njs + k * nj0) * dn_bytes);
+      for (int g = 0; g < kYGroups; ++g) mbar_arrive_expect_tx(sm.barY + g, (gb[g + 1] - gb[g]) * rp_bytes);
     }
     __syncwarp();
     if (lane == 0 && ns0 > 0) issue_rowpairs(sm.Z, p.capS, 0, p.w.sh_gate, p.w.sh_up, sr.x, ns0, d, sm.barZ);
     if (lane == 1 && njs > 0) issue_down(sm.X, p.capX, k, p.w.sh_down, 0, orng.x, njs, d, f, sm.barX);
   }
-  uint32_t y_phase = 0, z_phase = 1;
   // this block's first router item (8 experts x d/KS rows): kRouterPre rows per thread
   float4 wa[kRouterPre], wb[kRouterPre];
   float wg[kRouterPre];
@@ -573,7 +550,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_layer_kernel(const __gr
 #pragma unroll
       for (int i = 0; i < 9; ++i) sm.red[warp * 9 + i] = acc[i];
     __syncthreads();
-    if (tid < 9) {
+    if (tid < 9 && b != p.silent_block) {
       float v = 0.f;
       for (int w = 0; w < kDecWarps; ++w) v += sm.red[w * 9 + tid];
       if (tid < 8) publish(p.pub + (size_t)ks * E + cg * 8 + tid, v, epoch);
@@ -583,8 +560,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_layer_kernel(const __gr
   }
 
   // ---- phase B: logits (polled from the published partials), top k
-#pragma unroll 1
-  for (int e = tid; e < E; e += kDecThreads) {
+  float key = -INFINITY;
+  if (tid < E) {
     unsigned long long w[kDecodeMaxSplits];
     bool ready = false;
     Poll poll;
@@ -593,71 +570,50 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_layer_kernel(const __gr
 #pragma unroll
       for (int s = 0; s < kDecodeMaxSplits; ++s)
         if (s < p.KS) {
-          w[s] = ld_word(p.pub + (size_t)s * E + e);
+          w[s] = ld_word(p.pub + (size_t)s * E + tid);
           ready = ready && word_ready(w[s], epoch);
         }
-    } while (!ready && poll.again(p.status, 41));
+    } while (!ready && poll.again(p.wait_ns, p.status, 41));
     float z = 0.f;
 #pragma unroll
     for (int s = 0; s < kDecodeMaxSplits; ++s)
       if (s < p.KS) z += word_value(w[s]);
-    if (b == 0) p.logits[e] = z;
-    sm.keys[e] = p.w.router_bias ? z + p.w.router_bias[e] : z;
+    if (b == 0) p.logits[tid] = z;
+    key = p.w.router_bias ? z + p.w.router_bias[tid] : z;
   }
-  if (tid >= kDecThreads - 32 && tid - (kDecThreads - 32) < p.KS) {  // gate-logit partials
-    const int s = tid - (kDecThreads - 32);
+  if (tid < p.KS) {  // gate-logit partials
     unsigned long long w;
     Poll poll;
-    do w = ld_word(p.pub + (size_t)kDecodeMaxSplits * E + s);
-    while (!word_ready(w, epoch) && poll.again(p.status, 42));
-    sm.s_gp[s] = word_value(w);
+    do w = ld_word(p.pub + (size_t)kDecodeMaxSplits * E + tid);
+    while (!word_ready(w, epoch) && poll.again(p.wait_ns, p.status, 42));
+    sm.s_gp[tid] = word_value(w);
   }
-  __syncthreads();
-  // top k in two levels: each warp keeps the best kc of its E/8 keys (rank by
-  // counting), then the 8 * kc candidates are ranked among themselves. An
-  // expert in the overall top k is in its warp's top kc, and everything that
-  // outranks it is too, so its rank among the candidates is its overall rank.
-  // (Rank counts are branch-free so the compares and loads pipeline.)
-  const int EW = E / 8, kc = min(k, EW), n_cand = kDecWarps * kc;
-  if (EW <= 32) {  // one key per lane: the warp's keys come by register shuffles
-    const int base = warp * EW;
-    const float ke = lane < EW ? sm.keys[base + lane] : 0.f;
+  // rank of each key among its warp's 32 (register shuffles; descending,
+  // ties to the lower expert id); the best kc of each warp are candidates
+  {
     int rank = 0;
 #pragma unroll
     for (int o = 1; o < 32; ++o) {
       const int src = (lane + o) & 31;
-      const float kj = __shfl_sync(kFull, ke, src);
-      rank += (int)(src < EW) & ((int)(kj > ke) | ((int)(kj == ke) & (int)(src < lane)));
+      const float kj = __shfl_sync(kFull, key, src);
+      rank += (int)(kj > key) | ((int)(kj == key) & (int)(src < lane));
     }
-    if (lane < EW && rank < kc) {
-      sm.cand_key[warp * kc + rank] = ke;
-      sm.cand_id[warp * kc + rank] = base + lane;
-    }
-  } else {
-#pragma unroll 1
-    for (int m = lane; m < EW; m += 32) {
-      const int base = warp * EW;
-      const float ke = sm.keys[base + m];
-      int rank = 0;
-#pragma unroll 8
-      for (int j = 0; j < EW; ++j) {
-        const float kj = sm.keys[base + j];
-        rank += (int)(kj > ke) | ((int)(kj == ke) & (int)(j < m));
-      }
-      if (rank < kc) {
-        sm.cand_key[warp * kc + rank] = ke;
-        sm.cand_id[warp * kc + rank] = base + m;
-      }
+    if (tid < E && rank < kc) {
+      sm.cand_key[warp * kc + rank] = key;
+      sm.cand_id[warp * kc + rank] = tid;
     }
   }
   __syncthreads();
+  // a candidate's rank among all candidates is its overall rank (everything
+  // that outranks a top-k expert is a candidate too)
 #pragma unroll 1
-  for (int t = tid; t < n_cand; t += kDecThreads) {
+  for (int t = tid; t < kDecWarps * kc; t += kDecThreads) {
     const float kt = sm.cand_key[t];
     const int et = sm.cand_id[t];
+    if (et == INT_MAX) continue;
     int rank = 0;
 #pragma unroll 8
-    for (int j = 0; j < n_cand; ++j) {
+    for (int j = 0; j < kDecWarps * kc; ++j) {
       const float kj = sm.cand_key[j];
       rank += (int)(kj > kt) | ((int)(kj == kt) & (int)(sm.cand_id[j] < et));
     }
@@ -666,76 +622,81 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_layer_kernel(const __gr
       sm.s_z[rank] = kt;
     }
   }
+  fence_proxy_async_smem();  // the aliases in Y are done with before copies land there
   __syncthreads();
-  if (warp == 0) {  // the selected experts' rows, as early as possible
-    const int nr0 = min(rr.y - rr.x, p.capY);
-    if (lane == 0) {
-      mbar_arrive_expect_tx(sm.barY, nr0 * rp_bytes);
-      mbar_arrive_expect_tx(sm.barX, k * nj0 * dn_bytes);
-    }
-    __syncwarp();
-    issue_selected(p, sm.Y, sm.X, sm.s_ids, rr.x, nr0, orng.x, nj0, sm.barY, sm.barX);
-  }
-  ++y_phase;
-  if (warp == 0) {  // softmax over the selected biased logits; the shared gate
-    const float zmax = sm.s_z[0];
-    const float ex = lane < k ? expf(sm.s_z[lane] - zmax) : 0.f;
-    float sum = ex;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
-    const float wt = ex * __frcp_rn(sum);
-    if (lane < k) sm.s_w[lane] = wt;
-    float gl = 0.f;
-    for (int s = 0; s < p.KS; ++s) gl += sm.s_gp[s];
-    const float gate = p.shared ? __frcp_rn(1.f + expf(-gl)) : 0.f;
-    if (lane == 0) sm.s_w[k] = gate;
-    if (b == 0) {
-      if (lane < k) {
-        p.ids[lane] = sm.s_ids[lane];
-        p.wts[lane] = wt;
-      }
-      if (lane == 0) {
-        p.gate_logit[0] = gl;
-        p.wts[k] = gate;
-      }
-    }
-  }
 
-  // ---- h of the shared expert's rows: off the critical path here, while
-  // the routed rows are in flight (their copies went out above)
-#pragma unroll 1
-  for (int c0 = sr.x; c0 < sr.y; c0 += p.capS) {
-    const int n = min(p.capS, sr.y - c0);
-    if (c0 != sr.x) {
-      __syncthreads();  // the previous chunk's rows are consumed
-      if (tid == 0) {
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(sm.barZ, n * rp_bytes);
-        issue_rowpairs(sm.Z, p.capS, 0, p.w.sh_gate, p.w.sh_up, c0, n, d, sm.barZ);
-      }
-      ++z_phase;
-    }
-    bar_wait(sm.barZ, (z_phase - 1) & 1, p.status, 40);
-    rows_h(p, sm.Z, p.capS, sm.xp, sm.xsum, n, k * f + c0, epoch);
-  }
-
-  // ---- phase B: h of the routed row pairs
+  // ---- the routed rows: the issuing warp sends the copies (gate/up row
+  // pairs group by group, then the down rows) and computes the routing
+  // weights; the other warps compute each row-pair group as it lands
+  uint32_t y_phase = 0;
 #pragma unroll 1
   for (int c0 = rr.x; c0 < rr.y; c0 += p.capY) {
     const int n = min(p.capY, rr.y - c0);
-    if (c0 != rr.x) {
-      __syncthreads();
-      if (tid == 0) {
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(sm.barY, n * rp_bytes);
-        issue_routed(p, sm.Y, sm.s_ids, c0, n, sm.barY);
+    y_groups(n, p.qrow, gb);
+    if (c0 != rr.x) __syncthreads();  // the previous chunk's rows are consumed
+    if (warp == kIssueWarp) {
+      if (c0 != rr.x) {
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          for (int g = 0; g < kYGroups; ++g) mbar_arrive_expect_tx(sm.barY + g, (gb[g + 1] - gb[g]) * rp_bytes);
+        }
+        __syncwarp();
       }
-      ++y_phase;
+      issue_routed(p, sm.Y, sm.X, sm.s_ids, c0, gb, kYGroups, orng.x, c0 == rr.x ? nj0 : 0, sm.barY, sm.barX);
+      if (c0 == rr.x) {  // the routing weights: softmax over the selected biased logits; the shared gate
+        const float zmax = sm.s_z[0];
+        const float ex = lane < k ? expf(sm.s_z[lane] - zmax) : 0.f;
+        float sum = ex;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+        const float wt = ex * __frcp_rn(sum);
+        if (lane < k) sm.s_w[lane] = wt;
+        float gl = 0.f;
+        for (int s = 0; s < p.KS; ++s) gl += sm.s_gp[s];
+        const float gate = p.shared ? __frcp_rn(1.f + expf(-gl)) : 0.f;
+        if (lane == 0) sm.s_w[k] = gate;
+        if (b == 0) {
+          if (lane < k) {
+            p.ids[lane] = sm.s_ids[lane];
+            p.wts[lane] = wt;
+          }
+          if (lane == 0) {
+            p.gate_logit[0] = gl;
+            p.wts[k] = gate;
+          }
+        }
+      }
+    } else {
+      if (c0 == rr.x && warp >= kIssueWarp - 2) {
+        // the shared expert's rows (prefetched before the dependency wait) on
+        // two warps, while the routed rows are in flight
+        uint32_t z_phase = 0;
+#pragma unroll 1
+        for (int s0 = sr.x; s0 < sr.y; s0 += p.capS) {
+          const int n = min(p.capS, sr.y - s0);
+          if (s0 != sr.x) {
+            named_bar_sync(2, 64);  // both warps are done with the previous chunk
+            if (warp == kIssueWarp - 2 && lane == 0) {
+              fence_proxy_async_smem();
+              mbar_arrive_expect_tx(sm.barZ, n * rp_bytes);
+              issue_rowpairs(sm.Z, p.capS, 0, p.w.sh_gate, p.w.sh_up, s0, n, d, sm.barZ);
+            }
+          }
+          bar_wait(sm.barZ, z_phase & 1, p.wait_ns, p.status, 40);
+          ++z_phase;
+          rows_h(p, sm.Z, p.capS, sm.xp, sm.xsum, 0, n, k * f + s0, kIssueWarp - 2, 2, epoch);
+        }
+      }
+#pragma unroll 1
+      for (int g = 0; g < kYGroups; ++g) {
+        if (gb[g + 1] == gb[g]) continue;
+        bar_wait(sm.barY + g, y_phase & 1, p.wait_ns, p.status, 43);
+        rows_h(p, sm.Y, p.capY, sm.xp, sm.xsum, gb[g], gb[g + 1], c0, 0, kIssueWarp, epoch);
+      }
     }
-    bar_wait(sm.barY, (y_phase - 1) & 1, p.status, 43);
-    rows_h(p, sm.Y, p.capY, sm.xp, sm.xsum, n, c0, epoch);  // flattened (slot, row) = slot * f + row
+    ++y_phase;
   }
-  __syncthreads();  // Y is consumed: it holds h from here on
+  __syncthreads();  // Y is consumed: it holds h from here on; s_w is complete
 
   // ---- phase C: h of every slot (polled; as f16 pairs), then the block's outputs
   const int total = S * (f / 32);
@@ -768,7 +729,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_layer_kernel(const __gr
           }
           pending &= ~(1u << m);
         }
-    } while (pending && poll.again(p.status, 44));
+    } while (pending && poll.again(p.wait_ns, p.status, 44));
   }
   __syncthreads();
 #pragma unroll 1
@@ -795,11 +756,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_layer_kernel(const __gr
       if (tid == 0) {
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(sm.barX, S * nj * dn_bytes);
-        issue_down_all(p, sm.X, sm.s_ids, j0, nj, p.shared, sm.barX);
-        mbar_arrive(sm.barX);
+        for (int s = 0; s < k; ++s) issue_down(sm.X, p.capX, s, p.w.down, sm.s_ids[s], j0, nj, d, f, sm.barX);
+        if (p.shared) issue_down(sm.X, p.capX, k, p.w.sh_down, 0, j0, nj, d, f, sm.barX);
       }
     }
-    bar_wait(sm.barX, x_phase & 1, p.status, 45);
+    bar_wait(sm.barX, x_phase & 1, p.wait_ns, p.status, 45);
     ++x_phase;
     down_cols(p, sm.X, hp, hsum, sm.s_w, total, j0, nj);
   }
@@ -811,8 +772,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_layer_kernel(const __gr
 
 // ---------------------------------------------------------------- launch
 // Two blocks per SM (this layer's and the next layer's, which prefetches):
-// 228 KB of shared memory per SM, less 1 KB reserved per block, halved.
-constexpr size_t kDecSmemLimit = (228 * 1024 - 2 * 1024) / 2;
+// 227 KB of shared memory usable by the blocks of one SM, less 1 KB
+// reserved per block, halved.
+constexpr size_t kDecSmemLimit = (227 * 1024 - 2 * 1024) / 2;
 
 int gcd_int(int a, int b) { return b == 0 ? a : gcd_int(b, a % b); }
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -831,22 +793,26 @@ int sm_count() {
   return n;
 }
 
-uint32_t u_bytes(const DecodeParams& p) {  // x pairs, x chunk sums, keys and candidates
-  const int kc = std::min(p.k, p.E / 8);
-  return (uint32_t)round_up((size_t)p.d * 2 + (size_t)((p.d / 32 + 3) & ~3) * 4 + (size_t)(p.E + 16 * kc) * 4, 16);
+uint32_t u_bytes(const DecodeParams& p) {  // x pairs, x chunk sums
+  return (uint32_t)round_up((size_t)p.d * 2 + (size_t)((p.d / 32 + 3) & ~3) * 4, 16);
 }
 
 size_t scratch_bytes(const DecodeParams& p) {
-  return u_bytes(p) + (size_t)(32 + 32 + 40 + 72 + kDecodeMaxSplits + 2) * 4 + 8 + 24;
+  return u_bytes(p) + (size_t)(32 + 32 + 34 + kDecodeMaxSplits + 2) * 4 + 8 + 8 * (kYGroups + 2);
+}
+
+// What the aliases at the start of Y need.
+size_t y_alias_bytes(const DecodeParams& p) {
+  return (size_t)(72 + 2 * kDecWarps * std::min(p.k, 32)) * 4;
 }
 
 void size_buffers(DecodeParams& p) {
   const int S = p.k + (p.shared ? 1 : 0);
   const size_t rp = (size_t)p.d + p.d / 8, dn = (size_t)p.f / 2 + p.f / 16;
   const size_t h_bytes = (size_t)S * p.f * 2 + (size_t)S * (p.f / 32) * 4;  // f16 h, chunk sums
-  p.y_bytes = (uint32_t)round_up(std::max((size_t)p.capY * rp, h_bytes), 128);
-  p.x_bytes = (uint32_t)round_up((size_t)p.capX * S * dn, 128);
-  p.z_bytes = (uint32_t)round_up((size_t)p.capS * rp, 128);
+  p.y_bytes = (uint32_t)round_up(std::max({(size_t)p.capY * rp, h_bytes, y_alias_bytes(p)}), 128);
+  p.x_bytes = (uint32_t)round_up((size_t)p.capX * S * dn, 16);
+  p.z_bytes = (uint32_t)round_up((size_t)p.capS * rp, 16);
   p.u_bytes = u_bytes(p);
 }
 
@@ -880,20 +846,25 @@ cudaError_t launch_decode(const DecodeParams& p, int G, size_t smem, cudaStream_
   return launch_pdl(decode_layer_kernel, dim3(G), smem, s, p);
 }
 
+// Row granularity of the block ranges: bulk copies move whole 16-byte units
+// (d/32 scale bytes per gate/up row, f/32 per down row).
+int qrow_of(int d) { return 16 / gcd_int(16, d / 32); }
+int qout_of(int f) { return 16 / gcd_int(16, f / 32); }
+
 }  // namespace
 
 size_t decode_pub_words(int E) { return (size_t)kDecodeMaxSplits * E + kDecodeMaxSplits; }
 
 bool decode_shape_supported(int d, int E, int k, int f, bool shared) {
-  if (d > 4096 || E % 8) return false;
+  if (d > 4096 || E % 8 || E > kDecodeMaxExperts || k > 32) return false;
   DecodeParams p = {};
   p.d = d;
   p.E = E;
   p.k = k;
   p.f = f;
   p.shared = shared;
-  p.capY = 16 / gcd_int(16, d / 32);  // smallest chunks the kernel can loop over
-  p.capX = 16 / gcd_int(16, f / 32);
+  p.capY = qrow_of(d);  // smallest chunks the kernel can loop over
+  p.capX = qout_of(f);
   p.capS = shared ? p.capY : 0;
   size_buffers(p);
   return (size_t)p.y_bytes + p.x_bytes + p.z_bytes + scratch_bytes(p) <= kDecSmemLimit;
@@ -901,10 +872,8 @@ bool decode_shape_supported(int d, int E, int k, int f, bool shared) {
 
 cudaError_t decode_launch(const DecodeParams& p0, cudaStream_t s) {
   DecodeParams p = p0;
-  // Bulk copies move whole 16-byte units: row ranges start and end on
-  // multiples of qrow (gate/up, d/32 scale bytes per row) and qout (down).
-  p.qrow = 16 / gcd_int(16, p.d / 32);
-  p.qout = 16 / gcd_int(16, p.f / 32);
+  p.qrow = qrow_of(p.d);
+  p.qout = qout_of(p.f);
   // One block per SM, but no more blocks than routed row-pair units: every
   // block then publishes some h, which block 0 waits for before it moves the
   // epoch on (so no block can read the epoch after it changed).

@@ -50,7 +50,7 @@ inline int route_nblk(int T) { return (T + kRouteTPB - 1) / kRouteTPB; }
 inline int windowed_max_tiles(int T, int E, int k, int bn, int W, bool with_shared) {
   const int64_t nW = W > 0 ? ((int64_t)T + W - 1) / W : 1;
   const int64_t n = ((int64_t)T * k + bn - 1) / bn + nW * E +
-                    (with_shared ? ((int64_t)T + bn - 1) / bn + nW : 0);
+                    (with_shared ? ((int64_t)T + bn - 1) / bn + nW - 1 : 0);
   return n > 0x3FFFFFFF ? 0x3FFFFFFF : (int)n;
 }
 cudaError_t route_launch(const RouteParams& p, cudaStream_t s);
@@ -194,11 +194,16 @@ struct DecodeParams {
   unsigned long long* pub;
   unsigned long long* pub_h;
   uint32_t* sync;           // [0]: epoch of the last call (zero before the first call)
+  // bounded waits give up after wait_ns; silent_block >= 0 (tests of the
+  // timeout path only): that block publishes no router partial sums
+  uint64_t wait_ns;
+  int silent_block;
   // set by decode_launch
   int KS, qrow, qout, capY, capX, capS;
   uint32_t y_bytes, x_bytes, z_bytes, u_bytes;
 };
 constexpr int kDecodeMaxSplits = 8;  // router K splits
+constexpr int kDecodeMaxExperts = 256;  // one expert per thread in the top-k
 size_t decode_pub_words(int E);
 // Sizes the decode kernel can run: d <= 4096 and h of every slot fits in shared memory.
 bool decode_shape_supported(int d, int E, int k, int f, bool shared);

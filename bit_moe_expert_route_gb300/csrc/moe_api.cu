@@ -1,6 +1,7 @@
 // C ABI of libmoe_gb300: argument validation, workspace layouts and the
 // launch sequences of the routing, grouped-GEMM, whole-layer and decode
 // entry points declared in include/moe.h.
+#include <atomic>
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -67,10 +68,14 @@ RouteWs route_ws(void* ws, int T, int E) {
   return r;
 }
 
-// Token window of the down projection's block map (a multiple of the routing
-// kernels' 128-token blocks): 8192 tokens' fp32 output rows are 64 MB, about
-// half of L2.
+// Token window of the down projection's block map under MOE_FWD_DOWN_WINDOWS
+// (a multiple of the routing kernels' 128-token blocks): 8192 tokens' fp32
+// output rows are 64 MB, about half of L2.
 constexpr int kDownWindow = 8192;
+
+// moe_debug_decode_fault's settings (process-wide; tests of the timeout path)
+std::atomic<uint64_t> g_decode_wait_ns{0};
+std::atomic<int> g_decode_silent_block{-1};
 
 bool shape_ok(const moe_shape_t* s, bool need_tokens) {
   if (!s) return false;
@@ -119,9 +124,10 @@ FwdWs forward_ws(void* ws, const moe_shape_t* s, int bn, int flags) {
   // are mostly padding, and the combine epilogue's per-row copies dominate)
   // (gate/up stays at 128: its two accumulators fill TMEM at that height)
   r.v.down_block_n = bn == 128 && (int64_t)T * k >= (int64_t)256 * E ? 256 : bn;
-  // above kDownWindow tokens the down map is ordered by token window (see
-  // RouteParams::window2): the fp32 rows it adds into then stay in L2
-  r.v.down_window = r.v.down_block_n != bn && T > kDownWindow ? kDownWindow : 0;
+  // MOE_FWD_DOWN_WINDOWS, above kDownWindow tokens: the down map ordered by
+  // token window (see RouteParams::window2)
+  r.v.down_window =
+      (flags & MOE_FWD_DOWN_WINDOWS) && r.v.down_block_n != bn && T > kDownWindow ? kDownWindow : 0;
   if (r.v.down_block_n != bn) {
     r.v.down_max_tiles = moe::windowed_max_tiles(T, E, k, r.v.down_block_n, r.v.down_window, true);
     r.v.down_block_map = c.take<int32_t>((size_t)r.v.down_max_tiles * 4);
@@ -140,7 +146,7 @@ FwdWs forward_ws(void* ws, const moe_shape_t* s, int bn, int flags) {
   return r;
 }
 
-bool flags_ok(int flags) { return (flags & ~MOE_FWD_DETERMINISTIC) == 0; }
+bool flags_ok(int flags) { return (flags & ~(MOE_FWD_DETERMINISTIC | MOE_FWD_DOWN_WINDOWS)) == 0; }
 
 struct DecWs {
   moe_decode_views_t v;
@@ -609,6 +615,9 @@ int moe_decode_gemv_w4(const uint16_t* x, const moe_weights_t* w, const moe_shap
   p.pub = dw.pub;
   p.pub_h = dw.pub_h;
   p.sync = dw.sync;
+  const uint64_t limit = g_decode_wait_ns.load(std::memory_order_relaxed);
+  p.wait_ns = limit ? limit : moe::kWaitLimitNs;
+  p.silent_block = g_decode_silent_block.load(std::memory_order_relaxed);
   return cuda_status(moe::decode_launch(p, s));
 }
 
@@ -656,6 +665,12 @@ int moe_decode_batch_w4(const uint16_t* x, const moe_weights_t* w, const moe_sha
   p.out = out;
   p.status = bw.v.status;
   return cuda_status(moe::decode_batch_launch(p, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_debug_decode_fault(uint64_t wait_limit_ns, int silent_block) {
+  g_decode_wait_ns.store(wait_limit_ns, std::memory_order_relaxed);
+  g_decode_silent_block.store(silent_block < 0 ? -1 : silent_block, std::memory_order_relaxed);
+  return MOE_OK;
 }
 
 int moe_get_device_status(const void* ws, void* stream, int32_t* device_status) {

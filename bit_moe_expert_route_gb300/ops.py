@@ -112,6 +112,7 @@ def lib():
         L.moe_decode_batch_views.argtypes = [vp, sz, vp, vp]
         L.moe_decode_batch_w4.argtypes = [vp, vp, vp, vp, vp, sz, vp]
         L.moe_get_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
+        L.moe_debug_decode_fault.argtypes = [ctypes.c_uint64, i32]
         _lib = L
     return _lib
 
@@ -299,19 +300,21 @@ def decode_attention(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scale: f
 
 
 FWD_DETERMINISTIC = 1
+FWD_DOWN_WINDOWS = 2
 
 
 class Forward:
     """moe_forward_ex with a reusable workspace for one (shape, T, block_n, flags);
-    deterministic=True sets MOE_FWD_DETERMINISTIC (fixed-order combine)."""
+    deterministic=True sets MOE_FWD_DETERMINISTIC (fixed-order combine),
+    down_windows=True MOE_FWD_DOWN_WINDOWS (down tiles ordered by token window)."""
 
     def __init__(self, layer: DeviceLayer, T: int, block_n: int = 0, device="cuda",
-                 deterministic: bool = False):
+                 deterministic: bool = False, down_windows: bool = False):
         self.layer = layer
         self.T = T
         self.shape = Shape.of(layer.shape, T)
         self.block_n = block_n or pick_block_n(T, layer.shape.n_experts, layer.shape.top_k)
-        self.flags = FWD_DETERMINISTIC if deterministic else 0
+        self.flags = (FWD_DETERMINISTIC if deterministic else 0) | (FWD_DOWN_WINDOWS if down_windows else 0)
         nbytes = lib().moe_workspace_bytes_ex(ctypes.byref(self.shape), self.block_n, self.flags)
         if nbytes == 0:
             raise MoeError("moe_workspace_bytes_ex", -3)

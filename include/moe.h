@@ -227,11 +227,18 @@ int moe_forward(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* sh
  * slots 0..top_k-1 by descending logit, then the shared expert), one fp32
  * fused multiply-add per row, and rounds the sum to bf16. It costs the y
  * rows' bytes in the workspace (2.4 GB at T = 32768, d_model 2048) and one
- * write and one read of them per call. Other flag bits return MOE_ERR_SHAPE.
+ * write and one read of them per call.
+ * MOE_FWD_DOWN_WINDOWS orders the down projection's tiles by token window
+ * (8192 tokens) when it runs on its own 256-row map (T * top_k >= 256 *
+ * n_experts with 128-row gate/up tiles) and T > 8192: every expert's rows of
+ * one window, then the next window's, so the fp32 rows the combine adds into
+ * stay in L2 while their contributions arrive. Each (window, expert) piece
+ * may end in a partial tile. Other flag bits return MOE_ERR_SHAPE.
  * moe_workspace_bytes_ex / moe_forward_views_ex take the same flags (the
  * views' y is set only with MOE_FWD_DETERMINISTIC).
  */
 #define MOE_FWD_DETERMINISTIC 1
+#define MOE_FWD_DOWN_WINDOWS 2
 size_t moe_workspace_bytes_ex(const moe_shape_t* shape, int block_n, int flags);
 int moe_forward_ex(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* shape,
                    int block_n, int flags, uint16_t* out, void* ws, size_t ws_bytes,
@@ -287,9 +294,9 @@ int moe_forward_views_ex(void* ws, size_t ws_bytes, const moe_shape_t* shape, in
  * blocks synchronise through counters in the workspace, so the call needs
  * the whole GPU to itself while it runs (other work on the GPU only delays
  * it; a wait that exceeds 2 s records MOE_DEV_TIMEOUT).
- *   x bf16 [d_model] device; out bf16 [d_model] device; d_model <= 4096 and
- *   (top_k + 1) * d_ff <= about 24000 (h of every slot is staged on chip);
- *   other sizes return MOE_ERR_SHAPE.
+ *   x bf16 [d_model] device; out bf16 [d_model] device; d_model <= 4096,
+ *   n_experts <= 256, top_k <= 32 and (top_k + 1) * d_ff <= about 24000 (h
+ *   of every slot is staged on chip); other sizes return MOE_ERR_SHAPE.
  *   ws 256-byte aligned, >= moe_decode_workspace_bytes(shape) bytes, and
  *   zero-filled before its first use (cudaMemset); every call leaves its
  *   counters at zero for the next one. Zero it again after a call whose
@@ -370,6 +377,19 @@ int moe_decode_batch_w4(const uint16_t* x, const moe_weights_t* w, const moe_sha
  * gate last), h fp32 [T][k + 1][d_ff]. */
 int moe_decode_batch_views(void* ws, size_t ws_bytes, const moe_shape_t* shape,
                            moe_decode_views_t* views);
+
+/*
+ * moe_debug_decode_fault: a test hook for the decode path's failure
+ * detection (no counterpart on the pages). Later moe_decode_gemv_w4 calls
+ * (and moe_decode_gemv_w4_noalloc) give up a cross-block wait after
+ * wait_limit_ns instead of 2 s (0 restores 2 s), and, when silent_block >= 0,
+ * that block of each call publishes no router partial sums, so every other
+ * block's wait for them runs out: the call then records MOE_DEV_TIMEOUT in
+ * the workspace's status word and runs to its end with a wrong output. The
+ * settings are process-wide and apply to calls enqueued after this one
+ * (CUDA graphs keep the settings they were captured with). Returns MOE_OK.
+ */
+int moe_debug_decode_fault(uint64_t wait_limit_ns, int silent_block);
 
 /*
  * Reads the device status word of a workspace (synchronises `stream`).

@@ -80,7 +80,7 @@ def test_workspace_sizes(L):
     assert n_det >= L.moe_workspace_bytes(ctypes.byref(sh), 128) + (T * k + T) * d * 4
     assert L.moe_workspace_bytes_ex(ctypes.byref(sh), 128, 0) == L.moe_workspace_bytes(
         ctypes.byref(sh), 128)
-    assert L.moe_workspace_bytes_ex(ctypes.byref(sh), 128, 2) == 0  # unknown flag
+    assert L.moe_workspace_bytes_ex(ctypes.byref(sh), 128, 4) == 0  # unknown flag
 
 
 def test_forward_views_pick_the_down_tile_map(L):
@@ -102,14 +102,23 @@ def test_forward_views_pick_the_down_tile_map(L):
         assert v.block_n == bn and not v.y
         if separate:
             assert v.down_block_n == 256 and v.down_block_map != v.block_map
-            # above 8192 tokens the down map is cut per 8192-token window: every
-            # (window, expert) and (window, shared) piece may end in a partial tile
-            W = 8192 if T > 8192 else 0
-            assert v.down_window == W
-            nW = -(-T // W) if W else 1
-            assert v.down_max_tiles == -(-T * 8 // 256) + nW * 256 + -(-T // 256) + nW
-            assert v.down_max_tiles >= L.moe_max_tiles(T, 256, 8, 256, 1)
+            assert v.down_window == 0
+            assert v.down_max_tiles == L.moe_max_tiles(T, 256, 8, 256, 1)
             assert base <= v.down_block_map and v.down_num_tiles + 4 <= base + n
+            # with MOE_FWD_DOWN_WINDOWS, above 8192 tokens the down map is cut per
+            # 8192-token window: every (window, expert) and (window, shared) piece
+            # may end in a partial tile
+            nw = L.moe_workspace_bytes_ex(ctypes.byref(sh), bn, 2)
+            bufw = ctypes.create_string_buffer(nw + 256)
+            basew = (ctypes.addressof(bufw) + 255) // 256 * 256
+            vw = ops.ForwardViews()
+            assert L.moe_forward_views_ex(ctypes.c_void_p(basew), nw, ctypes.byref(sh), bn, 2,
+                                          ctypes.byref(vw)) == 0
+            W = 8192 if T > 8192 else 0
+            assert vw.down_window == W
+            nW = -(-T // W) if W else 1
+            assert vw.down_max_tiles == -(-T * 8 // 256) + nW * 256 + -(-T // 256) + nW - 1
+            assert vw.down_max_tiles >= v.down_max_tiles
         else:
             assert (v.down_block_n, v.down_max_tiles) == (bn, v.max_tiles)
             assert (v.down_block_map, v.down_num_tiles) == (v.block_map, v.num_tiles)

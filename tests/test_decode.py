@@ -78,7 +78,7 @@ def test_decode_graph_replay_matches_eager(layer):
 def test_decode_without_shared_expert(orc):
     from bit_moe_expert_route_gb300 import ops
     from bit_moe_expert_route_gb300.synth import LayerShape
-    shape = LayerShape(d_model=256, n_experts=32, top_k=4, d_ff=128, d_ff_shared=128)
+    shape = LayerShape(d_model=256, n_experts=32, top_k=4, d_ff=256, d_ff_shared=256)
     host = synth.layer_weights(shape, seed=5, shared=False)
     dl = ops.DeviceLayer(host, shape)
     dec = ops.Decode(dl)
@@ -144,3 +144,29 @@ def test_decode_chain_in_graph_matches_oracle(orc):
         ok, info = tolerance_check(bf16_np(outs[l]).reshape(1, -1), ref["out"])
         assert ok, (l, info)
         xin = to_np(outs[l].view(torch.int16)).view(np.uint16).reshape(1, -1)
+
+
+def test_decode_timeout_is_reported_and_recovers(orc, layer):
+    """Failure detection without a GPU fault: with a 1 ms wait limit and one
+    block withholding its router partial sums (moe_debug_decode_fault), every
+    other block's bounded poll runs out, the call records MOE_DEV_TIMEOUT in
+    the workspace status word and still ends; after the documented recovery
+    (the workspace zeroed) the next call matches the oracle again."""
+    from bit_moe_expert_route_gb300 import ops
+    host, dl = layer
+    dec = ops.Decode(dl)
+    L = ops.lib()
+    x = synth.tokens(FULL, 1, seed=0, layer=0, off=9, tensor=synth.X_DECODE)
+    xt = torch.from_numpy(x.view(np.int16)).cuda().view(-1)
+    dec(xt)
+    torch.cuda.synchronize()
+    assert ops.device_status(dec.ws) == ops.DEV_OK
+    try:
+        assert L.moe_debug_decode_fault(1_000_000, 3) == 0
+        dec(xt)
+        torch.cuda.synchronize()
+        assert ops.device_status(dec.ws) == ops.DEV_TIMEOUT
+    finally:
+        L.moe_debug_decode_fault(0, -1)
+    dec.ws.zero_()
+    check_one(orc, host, dec, x)

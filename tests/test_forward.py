@@ -84,10 +84,13 @@ def oracle_layer(orc, x, host, lg):
     return _ORACLE_CACHE[key]
 
 
-def run_layer(orc, host_layer, dev_layers, T, zipf, block_n=0, deterministic=False, all_tokens=False):
+def run_layer(orc, host_layer, dev_layers, T, zipf, block_n=0, deterministic=False, all_tokens=False,
+              down_windows=False):
     from bit_moe_expert_route_gb300 import ops
     host = dict(host_layer, router_bias=synth.zipf_router_bias(FULL.n_experts) if zipf else None)
-    fwd = ops.Forward(dev_layers[zipf], T, block_n, deterministic=deterministic)
+    fwd = ops.Forward(dev_layers[zipf], T, block_n, deterministic=deterministic,
+                      down_windows=down_windows)
+    assert bool(fwd.views.down_window) == (down_windows and T > 8192)
     x = synth.tokens(FULL, T, seed=0)
     out = fwd(torch.from_numpy(x.view(np.int16)).cuda())
     torch.cuda.synchronize()
@@ -150,6 +153,14 @@ def test_forward_T32768_zipf(orc, host_layer, dev_layers):
     m, _ = run_layer(orc, host_layer, dev_layers, 32768, True)
     c = m["counts"]
     assert c.max() > 10 * c.mean() and (c == 0).sum() >= 2
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_forward_T32768_zipf_down_windows(orc, host_layer, dev_layers, deterministic):
+    """MOE_FWD_DOWN_WINDOWS: the down tiles in four 8192-token windows (the map
+    derived from the oracle's routing), the same parity bar."""
+    run_layer(orc, host_layer, dev_layers, 32768, True, deterministic=deterministic,
+              down_windows=True)
 
 
 @pytest.mark.slow

@@ -78,7 +78,7 @@ def test_noalloc_refuses_shapes_beyond_its_scratch():
     s = ops._stream()
     # a shape the decode kernel runs whose workspace is above 256 KB: refused
     # before anything is read (the weights above are never dereferenced)
-    big = ops.Shape(1, 2048, 256, 8, 2560, 2560, 64)
+    big = ops.Shape(1, 2048, 256, 16, 2048, 2048, 64)
     assert L.moe_decode_workspace_bytes(ctypes.byref(big)) > 256 * 1024
     assert L.moe_decode_gemv_w4_noalloc(_ptr(x), ctypes.byref(layer.weights), ctypes.byref(big),
                                         _ptr(out), s) == -4
@@ -87,3 +87,32 @@ def test_noalloc_refuses_shapes_beyond_its_scratch():
                 ops.Shape(1, 2048, 64, 32, 2048, 2048, 64)):
         assert L.moe_decode_gemv_w4_noalloc(_ptr(x), ctypes.byref(layer.weights),
                                             ctypes.byref(bad), _ptr(out), s) == -3
+
+
+def test_noalloc_timeout_status_and_reset():
+    """A call on the built-in scratch whose bounded waits run out (one block
+    withholds its router partials under moe_debug_decode_fault) is visible
+    through moe_decode_noalloc_device_status; after moe_decode_noalloc_reset
+    the next call equals moe_decode_gemv_w4's output bit for bit."""
+    from bit_moe_expert_route_gb300 import ops
+    host = synth.layer_weights(FULL, seed=7, layer=3)
+    layer = ops.DeviceLayer(host, FULL)
+    dec = ops.Decode(layer)
+    shape = ops.Shape.of(FULL, 1)
+    L = ops.lib()
+    xs = synth.tokens(FULL, 1, seed=7, layer=3, off=5, tensor=synth.X_DECODE)
+    x = torch.from_numpy(xs.view(np.int16)).cuda().view(-1)
+    out = torch.empty(FULL.d_model, dtype=torch.bfloat16, device="cuda")
+    try:
+        assert L.moe_debug_decode_fault(1_000_000, 5) == 0
+        _noalloc(L, x, layer, shape, out)
+        torch.cuda.synchronize()
+        assert _noalloc_status(L) == ops.DEV_TIMEOUT
+    finally:
+        L.moe_debug_decode_fault(0, -1)
+    assert L.moe_decode_noalloc_reset(ops._stream()) == 0
+    ref = dec(x)
+    _noalloc(L, x, layer, shape, out)
+    torch.cuda.synchronize()
+    assert _noalloc_status(L) == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
