@@ -602,6 +602,13 @@ def run_prefill(T, zipf, host0, args, peaks):
         gd.replay()
     t_det = statistics.median(timed_replays(gd, stream, args.prefill_iters, flush))
     del gd, fwd_det
+    # the fused chain (MOE_FWD_FUSED: gate/up, SwiGLU and down per 64-row tile, h on chip)
+    fwd_fused = ops.Forward(dl, T, fused=True)
+    gf = gpu_graph(lambda: fwd_fused(x, out), stream)
+    for _ in range(3):
+        gf.replay()
+    t_fused = statistics.median(timed_replays(gf, stream, args.prefill_iters, flush))
+    del gf, fwd_fused
     f1 = 2 * 2 * d * f * rows
     f2 = 2 * f * d * rows
     achieved = (f1 + f2) / (t1 + t2) / 1e12
@@ -611,6 +618,8 @@ def run_prefill(T, zipf, host0, args, peaks):
         T=T, router_bias="zipf 1.5*ln(1/rank)" if zipf else None, block_n=bn,
         tokens_per_s=round(T / t_layer, 1), ms=round(t_layer * 1e3, 4),
         deterministic_ms=round(t_det * 1e3, 4),
+        fused_chain_ms=round(t_fused * 1e3, 4),
+        fused_chain_frac_of_bf16_peak=round(FLOP_PER_TOKEN * T / t_fused / 1e12 / peaks["bf16"], 4),
         layer_tflops=round(FLOP_PER_TOKEN * T / t_layer / 1e12, 2),
         layer_frac_of_bf16_peak=round(FLOP_PER_TOKEN * T / t_layer / 1e12 / peaks["bf16"], 4),
         weights_hbm_frac=round(weight_bytes / t_layer / 1e9 / peaks["hbm_gbs"], 4),

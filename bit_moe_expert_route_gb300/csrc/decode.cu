@@ -837,12 +837,23 @@ cudaError_t launch_decode(const DecodeParams& p, int G, size_t smem, cudaStream_
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!attr_set) {
-      const cudaError_t err = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)kDecSmemLimit);
+      cudaError_t err = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kDecSmemLimit);
+      if (err != cudaSuccess) return err;
+      // all of the SM's configurable memory as shared memory (two blocks' worth)
+      err = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
       if (err != cudaSuccess) return err;
       attr_set = true;
     }
   }
+  // The blocks wait on one another, so all G must be resident at once (one
+  // per SM here), and the next layer's blocks should fit beside them: the
+  // occupancy query must allow two blocks per SM, else the launch is refused.
+  int per_sm = 0;
+  const cudaError_t err =
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel, kDecThreads, smem);
+  if (err != cudaSuccess) return err;
+  if (per_sm < 2 || G > per_sm * sm_count()) return cudaErrorInvalidConfiguration;
   return launch_pdl(decode_layer_kernel, dim3(G), smem, s, p);
 }
 

@@ -130,6 +130,32 @@ struct GemmParams {
 
 cudaError_t gemm_w4_launch(const GemmParams& p, cudaStream_t s);
 
+// Fused gate/up -> SwiGLU -> down -> weighted combine over tiles of
+// kFusedBlockN rows (gemm_fused.cu): h of a tile stays in shared memory.
+// f16 operands; W[0..2] = gate, up, down of the routed stack (n_groups
+// experts), X[0..2] the shared expert (group n_groups; q == null if absent).
+constexpr int kFusedBlockN = 64;
+constexpr int kFusedMaxDff = 512;
+struct FusedParams {
+  const uint16_t* A;        // x16 [A_rows][d] f16
+  int64_t A_rows;
+  int d, f;
+  const int32_t* row_index; // [n_rows]: token of row r
+  int64_t n_rows;
+  GemmW4 W[3];
+  GemmW4 X[3];
+  int n_groups;
+  const int32_t* block_map; // tiles of at most kFusedBlockN rows
+  const int32_t* num_tiles;
+  int max_tiles;
+  const float* row_scale;   // [n_rows] combine weights
+  float* C;                 // [C_rows][d] fp32, added into
+  int64_t C_rows;
+  int32_t* status;
+};
+bool fused_shape_supported(int d, int f);
+cudaError_t gemm_fused_launch(const FusedParams& p, cudaStream_t s);
+
 // ---------------------------------------------------------------- elementwise
 cudaError_t f32_to_bf16_launch(const float* in, uint16_t* out, int64_t n, cudaStream_t s);
 

@@ -146,7 +146,21 @@ FwdWs forward_ws(void* ws, const moe_shape_t* s, int bn, int flags) {
   return r;
 }
 
-bool flags_ok(int flags) { return (flags & ~(MOE_FWD_DETERMINISTIC | MOE_FWD_DOWN_WINDOWS)) == 0; }
+bool flags_ok(int flags) {
+  if (flags & ~(MOE_FWD_DETERMINISTIC | MOE_FWD_DOWN_WINDOWS | MOE_FWD_FUSED)) return false;
+  return !((flags & MOE_FWD_FUSED) && (flags & (MOE_FWD_DETERMINISTIC | MOE_FWD_DOWN_WINDOWS)));
+}
+
+// The row-tile height moe_forward_ex uses: the caller's, else the fused
+// chain's own, else the one moe_pick_block_n picks; 0 if unsupported.
+int forward_block_n(const moe_shape_t* s, int block_n, int flags) {
+  if (flags & MOE_FWD_FUSED) {
+    if (block_n == 0) block_n = moe::kFusedBlockN;
+    return block_n == moe::kFusedBlockN && moe::fused_shape_supported(s->d_model, s->d_ff) ? block_n : 0;
+  }
+  if (block_n == 0) block_n = moe_pick_block_n(s->T, s->n_experts, s->top_k);
+  return valid_block_n(block_n) && block_n != 256 ? block_n : 0;  // gate/up: 128 rows at most
+}
 
 struct DecWs {
   moe_decode_views_t v;
@@ -402,8 +416,7 @@ int moe_grouped_gemm_w4a16(const uint16_t* A, int64_t A_rows, int K, const int32
 
 size_t moe_workspace_bytes_ex(const moe_shape_t* shape, int block_n, int flags) {
   if (!shape_ok(shape, false) || !flags_ok(flags)) return 0;
-  if (block_n == 0) block_n = moe_pick_block_n(shape->T, shape->n_experts, shape->top_k);
-  if (!valid_block_n(block_n) || block_n == 256) return 0;  // gate/up: 128 rows at most
+  if ((block_n = forward_block_n(shape, block_n, flags)) == 0) return 0;
   return forward_ws(nullptr, shape, block_n, flags).bytes;
 }
 
@@ -414,8 +427,7 @@ size_t moe_workspace_bytes(const moe_shape_t* shape, int block_n) {
 int moe_forward_views_ex(void* ws, size_t ws_bytes, const moe_shape_t* shape, int block_n,
                          int flags, moe_forward_views_t* views) {
   if (!shape_ok(shape, false) || !flags_ok(flags)) return MOE_ERR_SHAPE;
-  if (block_n == 0) block_n = moe_pick_block_n(shape->T, shape->n_experts, shape->top_k);
-  if (!valid_block_n(block_n) || block_n == 256) return MOE_ERR_SHAPE;
+  if ((block_n = forward_block_n(shape, block_n, flags)) == 0) return MOE_ERR_SHAPE;
   if (!views) return MOE_ERR_NULL;
   const FwdWs fw = forward_ws(ws, shape, block_n, flags);
   if (!ws || !aligned(ws, kAlign) || ws_bytes < fw.bytes) return MOE_ERR_WORKSPACE;
@@ -437,8 +449,7 @@ int moe_forward_ex(const uint16_t* x, const moe_weights_t* w, const moe_shape_t*
                    int block_n, int flags, uint16_t* out, void* ws, size_t ws_bytes,
                    void* stream) {
   if (!shape_ok(shape, false) || !flags_ok(flags)) return MOE_ERR_SHAPE;
-  if (block_n == 0) block_n = moe_pick_block_n(shape->T, shape->n_experts, shape->top_k);
-  if (!valid_block_n(block_n) || block_n == 256) return MOE_ERR_SHAPE;
+  if ((block_n = forward_block_n(shape, block_n, flags)) == 0) return MOE_ERR_SHAPE;
   const int T = shape->T, E = shape->n_experts, k = shape->top_k, d = shape->d_model,
             f = shape->d_ff;
   int rc = check_weights(w, shape);
@@ -503,6 +514,37 @@ int moe_forward_ex(const uint16_t* x, const moe_weights_t* w, const moe_shape_t*
     rp.window2 = v.down_window;
   }
   if ((rc = cuda_status(moe::route_launch(rp, s))) != MOE_OK) return rc;
+  if (flags & MOE_FWD_FUSED) {
+    // 3-4. the fused chain: per 64-row tile, gate/up + SwiGLU into shared
+    // memory, then down + weighted combine into the fp32 accumulator
+    if ((rc = cuda_status(cudaMemsetAsync(v.out_acc, 0, (size_t)T * d * 4, s))) != MOE_OK) return rc;
+    moe::FusedParams fp;
+    memset(&fp, 0, sizeof fp);
+    fp.A = v.x16;
+    fp.A_rows = T;
+    fp.d = d;
+    fp.f = f;
+    fp.row_index = v.row_token;
+    fp.n_rows = rows;
+    fp.W[0] = {w->gate.q, w->gate.scale, w->gate.bias};
+    fp.W[1] = {w->up.q, w->up.scale, w->up.bias};
+    fp.W[2] = {w->down.q, w->down.scale, w->down.bias};
+    if (shared) {
+      fp.X[0] = {w->sh_gate.q, w->sh_gate.scale, w->sh_gate.bias};
+      fp.X[1] = {w->sh_up.q, w->sh_up.scale, w->sh_up.bias};
+      fp.X[2] = {w->sh_down.q, w->sh_down.scale, w->sh_down.bias};
+    }
+    fp.n_groups = E;
+    fp.block_map = v.block_map;
+    fp.num_tiles = v.num_tiles;
+    fp.max_tiles = v.max_tiles;
+    fp.row_scale = v.row_weight;
+    fp.C = v.out_acc;
+    fp.C_rows = T;
+    fp.status = v.status;
+    if ((rc = cuda_status(moe::gemm_fused_launch(fp, s))) != MOE_OK) return rc;
+    return cuda_status(moe::f32_to_bf16_launch(v.out_acc, out, (int64_t)T * d, s));
+  }
   // 3. gate/up grouped GEMM with SwiGLU -> h (rows in expert order, shared rows last)
   moe::GemmParams g;
   memset(&g, 0, sizeof g);

@@ -301,20 +301,23 @@ def decode_attention(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scale: f
 
 FWD_DETERMINISTIC = 1
 FWD_DOWN_WINDOWS = 2
+FWD_FUSED = 4
 
 
 class Forward:
     """moe_forward_ex with a reusable workspace for one (shape, T, block_n, flags);
     deterministic=True sets MOE_FWD_DETERMINISTIC (fixed-order combine),
-    down_windows=True MOE_FWD_DOWN_WINDOWS (down tiles ordered by token window)."""
+    down_windows=True MOE_FWD_DOWN_WINDOWS (down tiles ordered by token window),
+    fused=True MOE_FWD_FUSED (gate/up, SwiGLU and down per 64-row tile in one kernel)."""
 
     def __init__(self, layer: DeviceLayer, T: int, block_n: int = 0, device="cuda",
-                 deterministic: bool = False, down_windows: bool = False):
+                 deterministic: bool = False, down_windows: bool = False, fused: bool = False):
         self.layer = layer
         self.T = T
         self.shape = Shape.of(layer.shape, T)
-        self.block_n = block_n or pick_block_n(T, layer.shape.n_experts, layer.shape.top_k)
-        self.flags = (FWD_DETERMINISTIC if deterministic else 0) | (FWD_DOWN_WINDOWS if down_windows else 0)
+        self.flags = ((FWD_DETERMINISTIC if deterministic else 0) | (FWD_DOWN_WINDOWS if down_windows else 0)
+                      | (FWD_FUSED if fused else 0))
+        self.block_n = block_n or (64 if fused else pick_block_n(T, layer.shape.n_experts, layer.shape.top_k))
         nbytes = lib().moe_workspace_bytes_ex(ctypes.byref(self.shape), self.block_n, self.flags)
         if nbytes == 0:
             raise MoeError("moe_workspace_bytes_ex", -3)

@@ -233,12 +233,20 @@ int moe_forward(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* sh
  * n_experts with 128-row gate/up tiles) and T > 8192: every expert's rows of
  * one window, then the next window's, so the fp32 rows the combine adds into
  * stay in L2 while their contributions arrive. Each (window, expert) piece
- * may end in a partial tile. Other flag bits return MOE_ERR_SHAPE.
+ * may end in a partial tile.
+ * MOE_FWD_FUSED runs the two projections as one kernel over 64-row tiles
+ * (block_n 0 or 64): per tile, the gate/up products and SwiGLU go into
+ * shared memory (h is not written to the workspace; its view stays
+ * unwritten), then the down products of that h are weighted and added into
+ * the fp32 accumulator. Needs d_model and d_ff multiples of 512, d_ff <= 512;
+ * not combinable with the other flags. Other flag bits, or those cases,
+ * return MOE_ERR_SHAPE.
  * moe_workspace_bytes_ex / moe_forward_views_ex take the same flags (the
  * views' y is set only with MOE_FWD_DETERMINISTIC).
  */
 #define MOE_FWD_DETERMINISTIC 1
 #define MOE_FWD_DOWN_WINDOWS 2
+#define MOE_FWD_FUSED 4
 size_t moe_workspace_bytes_ex(const moe_shape_t* shape, int block_n, int flags);
 int moe_forward_ex(const uint16_t* x, const moe_weights_t* w, const moe_shape_t* shape,
                    int block_n, int flags, uint16_t* out, void* ws, size_t ws_bytes,

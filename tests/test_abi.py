@@ -80,7 +80,13 @@ def test_workspace_sizes(L):
     assert n_det >= L.moe_workspace_bytes(ctypes.byref(sh), 128) + (T * k + T) * d * 4
     assert L.moe_workspace_bytes_ex(ctypes.byref(sh), 128, 0) == L.moe_workspace_bytes(
         ctypes.byref(sh), 128)
-    assert L.moe_workspace_bytes_ex(ctypes.byref(sh), 128, 4) == 0  # unknown flag
+    assert L.moe_workspace_bytes_ex(ctypes.byref(sh), 128, 8) == 0  # unknown flag
+    # the fused chain: 64-row tiles only, not with the other flags, d/f multiples of 512
+    assert L.moe_workspace_bytes_ex(ctypes.byref(sh), 0, 4) == L.moe_workspace_bytes(ctypes.byref(sh), 64)
+    assert L.moe_workspace_bytes_ex(ctypes.byref(sh), 128, 4) == 0
+    assert L.moe_workspace_bytes_ex(ctypes.byref(sh), 0, 4 | 1) == 0
+    small = ops.Shape(64, 256, 32, 4, 256, 256, 64)
+    assert L.moe_workspace_bytes_ex(ctypes.byref(small), 0, 4) == 0
 
 
 def test_forward_views_pick_the_down_tile_map(L):

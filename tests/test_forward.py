@@ -85,11 +85,11 @@ def oracle_layer(orc, x, host, lg):
 
 
 def run_layer(orc, host_layer, dev_layers, T, zipf, block_n=0, deterministic=False, all_tokens=False,
-              down_windows=False):
+              down_windows=False, fused=False):
     from bit_moe_expert_route_gb300 import ops
     host = dict(host_layer, router_bias=synth.zipf_router_bias(FULL.n_experts) if zipf else None)
     fwd = ops.Forward(dev_layers[zipf], T, block_n, deterministic=deterministic,
-                      down_windows=down_windows)
+                      down_windows=down_windows, fused=fused)
     assert bool(fwd.views.down_window) == (down_windows and T > 8192)
     x = synth.tokens(FULL, T, seed=0)
     out = fwd(torch.from_numpy(x.view(np.int16)).cuda())
@@ -153,6 +153,27 @@ def test_forward_T32768_zipf(orc, host_layer, dev_layers):
     m, _ = run_layer(orc, host_layer, dev_layers, 32768, True)
     c = m["counts"]
     assert c.max() > 10 * c.mean() and (c == 0).sum() >= 2
+
+
+@pytest.mark.parametrize("T,zipf", [(64, False), (512, False), (4096, False), (32768, True)])
+def test_forward_fused_chain(orc, host_layer, dev_layers, T, zipf):
+    """MOE_FWD_FUSED: gate/up, SwiGLU and down per 64-row tile in one kernel, h
+    never leaving shared memory; the same routing checks (64-row tile map) and
+    the same parity bar on the fp32 result and its bf16 rounding."""
+    run_layer(orc, host_layer, dev_layers, T, zipf, fused=True)
+
+
+def test_forward_fused_matches_two_kernel_path(dev_layers):
+    """The fused chain computes what the two grouped GEMMs at 64-row tiles
+    compute (same h rounding, same MMA order per element); only the order of
+    the fp32 additions into each output row differs."""
+    from bit_moe_expert_route_gb300 import ops
+    T = 4096
+    x = torch.from_numpy(synth.tokens(FULL, T, seed=9).view(np.int16)).cuda()
+    a = ops.Forward(dev_layers[False], T, 64)(x).float()
+    b = ops.Forward(dev_layers[False], T, fused=True)(x).float()
+    torch.cuda.synchronize()
+    assert (a - b).abs().max().item() <= 1e-2 * a.abs().max().item()
 
 
 @pytest.mark.parametrize("deterministic", [False, True])
