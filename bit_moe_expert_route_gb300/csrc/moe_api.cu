@@ -277,11 +277,15 @@ const char* moe_status_string(int status) {
 
 int moe_version(void) { return 100; }
 
+// Measured on GB300 (d_model 2048, 256 experts, top-8, layer times with L2
+// flushed): 64-row tiles beat 16- and 32-row tiles from about 8 rows per
+// expert on (T = 512: 0.453 -> 0.338 ms; T = 1024: 0.461 -> 0.364 ms), since
+// a tile's fixed costs (block-map entry, gathers, accumulator hand-offs)
+// outweigh its padding; 128-row tiles win once experts average more than 64.
 int moe_pick_block_n(int T, int n_experts, int top_k) {
   if (T <= 0 || n_experts <= 0) return 16;
   const double per_expert = (double)T * top_k / n_experts;
-  if (per_expert <= 16) return 16;
-  if (per_expert <= 32) return 32;
+  if (per_expert <= 4) return 16;
   if (per_expert <= 64) return 64;
   return 128;
 }

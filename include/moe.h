@@ -118,7 +118,8 @@ const char* moe_status_string(int status);
 /* Library ABI version (major * 100 + minor). */
 int moe_version(void);
 
-/* Row-tile height used by moe_forward when block_n == 0 (16, 32, 64 or 128). */
+/* Row-tile height used by moe_forward when block_n == 0: 16 up to 4 rows per
+ * expert on average (T * top_k / n_experts), 64 up to 64, else 128. */
 int moe_pick_block_n(int T, int n_experts, int top_k);
 
 /* Upper bound on block-map entries: ceil(T*k/bn) + E + (with_shared ? ceil(T/bn) : 0). */

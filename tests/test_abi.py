@@ -50,7 +50,9 @@ def test_status_strings(L):
 def test_block_n_and_tile_bounds(L):
     from bit_moe_expert_route_gb300 import ops
     assert ops.pick_block_n(64, 256, 8) == 16
-    assert ops.pick_block_n(512, 256, 8) == 16
+    assert ops.pick_block_n(512, 256, 8) == 64
+    assert ops.pick_block_n(128, 256, 8) == 16
+    assert ops.pick_block_n(2048, 256, 8) == 64
     assert ops.pick_block_n(4096, 256, 8) == 128
     assert ops.pick_block_n(32768, 256, 8) == 128
     assert ops.max_tiles(3, 4, 2, 2, True) == 3 + 4 + 2
