@@ -48,11 +48,13 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-gdn", action="store_true", help="skip the Gated DeltaNet scan lines")
     ap.add_argument("--no-attn", action="store_true", help="skip the decode-attention lines")
-    ap.add_argument("--profile", choices=["decode", "prefill", "prefill-det", "decode-batch"],
+    ap.add_argument("--profile", choices=["decode", "prefill", "prefill-det", "prefill-fused",
+                                          "decode-batch", "attn"],
                     help="no measurement: run one layer repeatedly (decode: 20 + 200 calls; prefill: "
-                         "3 forwards at --profile-T tokens; prefill-det: the same with "
-                         "MOE_FWD_DETERMINISTIC; decode-batch: 8 calls at each of "
-                         "T = 2, 4, 8) for a profiler to attach to")
+                         "3 forwards at --profile-T tokens; prefill-det / prefill-fused: the same "
+                         "with MOE_FWD_DETERMINISTIC / MOE_FWD_FUSED; decode-batch: 8 calls at each "
+                         "of T = 2, 4, 8; attn: 4 decode-attention calls over 32768 cached "
+                         "positions) for a profiler to attach to")
     ap.add_argument("--profile-T", type=int, default=4096)
     return ap.parse_args()
 
@@ -729,6 +731,15 @@ def profile_run(args):
         out = torch.empty(shape.d_model, dtype=torch.bfloat16, device="cuda")
         for _ in range(220):
             dec(x, out)
+    elif args.profile == "attn":
+        Hq, Hkv, d = ATTN_SHAPE["Hq"], ATTN_SHAPE["Hkv"], ATTN_SHAPE["d"]
+        gen = torch.Generator(device="cuda").manual_seed(0)
+        L = 32768
+        q = torch.randn(Hq, d, device="cuda", generator=gen).to(torch.bfloat16)
+        K = torch.randn(L, Hkv, d, device="cuda", generator=gen).to(torch.bfloat16)
+        V = torch.randn(L, Hkv, d, device="cuda", generator=gen).to(torch.bfloat16)
+        for _ in range(4):
+            ops.decode_attention(q, K, V)
     elif args.profile == "decode-batch":
         for T in (2, 4, 8):
             dec = ops.DecodeBatch(dl, T)
@@ -737,7 +748,8 @@ def profile_run(args):
                 dec(x)
     else:
         T = args.profile_T
-        fwd = ops.Forward(dl, T, deterministic=args.profile == "prefill-det")
+        fwd = ops.Forward(dl, T, deterministic=args.profile == "prefill-det",
+                          fused=args.profile == "prefill-fused")
         x = torch.from_numpy(synth.tokens(shape, T, seed=0).view(np.int16)).cuda()
         for _ in range(3):
             fwd(x)

@@ -16,8 +16,9 @@
 // scores (E-term partial dots, butterfly warp sums), then the online softmax
 // update per head (running max m, running sum l, output rescaled when the max
 // grows). Each warp writes its (m, l, unnormalised output) per head as one
-// partial. Combine kernel: per query head, all partials merged with weights
-// exp(m_part - max m) and divided by the merged sum.
+// partial. Combine kernel: per query head and 64 output elements, all
+// partials merged with weights exp(m_part - max m) and divided by the merged
+// sum (block-wide reductions in a fixed order).
 #include <algorithm>
 #include <cmath>
 
@@ -48,6 +49,40 @@ MOE_DEVINL void load_row(const uint16_t* p, float (&f)[E]) {
     f[3] = __uint_as_float(w.y & 0xFFFF0000u);
   } else {
     const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(p));
+    f[0] = __uint_as_float(w << 16);
+    f[1] = __uint_as_float(w & 0xFFFF0000u);
+  }
+}
+
+constexpr int kRing = 8;  // positions in flight per warp
+
+// 16-, 8- or 4-byte cp.async global -> shared (the lane's own elements of a row)
+template <int B>
+MOE_DEVINL void cp_async_bytes(uint32_t dst, const void* src) {
+  if constexpr (B == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(dst), "l"(src), "n"(B) : "memory");
+}
+
+template <int E>
+MOE_DEVINL void load_row_smem(const uint8_t* p, float (&f)[E]) {
+  if constexpr (E == 8) {
+    const uint4 w = *reinterpret_cast<const uint4*>(p);
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(u[i] << 16);
+      f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+    }
+  } else if constexpr (E == 4) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    f[0] = __uint_as_float(w.x << 16);
+    f[1] = __uint_as_float(w.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(w.y << 16);
+    f[3] = __uint_as_float(w.y & 0xFFFF0000u);
+  } else {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
     f[0] = __uint_as_float(w << 16);
     f[1] = __uint_as_float(w & 0xFFFF0000u);
   }
@@ -84,12 +119,31 @@ __global__ void __launch_bounds__(32 * kAttnWarps, 1) attn_split_kernel(const At
     m[h] = -INFINITY;
     l[h] = 0.f;
   }
+  // K and V rows of the warp's next kRing positions in flight: each lane
+  // copies (cp.async) exactly the E elements of each row it later reads, into
+  // its own slots of a per-warp shared-memory ring, so the ring needs no
+  // synchronisation beyond the lane's own wait_group
+  extern __shared__ __align__(16) uint8_t attn_ring[];
+  uint8_t* ring = attn_ring + (size_t)warp * kRing * 2 * (32 * E * 2);
+  auto slot = [&](int r, int kv) { return smem_u32(ring + ((size_t)(r * 2 + kv) * 32 + lane) * (E * 2)); };
+  auto issue = [&](int j, int r) {
+    if (j < j1) {
+      const int64_t row = ((int64_t)j * p.Hkv + g) * d + lane * E;
+      cp_async_bytes<E * 2>(slot(r, 0), p.K + row);
+      cp_async_bytes<E * 2>(slot(r, 1), p.V + row);
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int r = 0; r < kRing; ++r) issue(j0 + warp + r * kAttnWarps, r);
+  int r = 0;
 #pragma unroll 1
-  for (int j = j0 + warp; j < j1; j += kAttnWarps) {
+  for (int j = j0 + warp; j < j1; j += kAttnWarps, r = (r + 1) % kRing) {
+    cp_async_wait<kRing - 1>();
     float k[E], v[E];
-    const int64_t row = ((int64_t)j * p.Hkv + g) * d + lane * E;
-    load_row<E>(p.K + row, k);
-    load_row<E>(p.V + row, v);
+    load_row_smem<E>(ring + ((size_t)(r * 2 + 0) * 32 + lane) * (E * 2), k);
+    load_row_smem<E>(ring + ((size_t)(r * 2 + 1) * 32 + lane) * (E * 2), v);
+    issue(j + kRing * kAttnWarps, r);  // the slot is read: refill it
 #pragma unroll
     for (int h = 0; h < kAttnMaxGroup; ++h) {
       if (h >= G) break;
@@ -122,23 +176,58 @@ __global__ void __launch_bounds__(32 * kAttnWarps, 1) attn_split_kernel(const At
   }
 }
 
-// One block per query head; thread t merges element t of every partial.
-__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p, int P) {
-  const int qh = blockIdx.x, d = p.d;
+// Merge of the partials: one block per (query head, 64 output elements).
+// The merged max over the P partials and the weights w_i = exp(m_i - max)
+// come from block-wide reductions in a fixed order (each thread's share in
+// index order, then the warps' butterfly, then warps in order), so the result
+// does not depend on timing; then each output element is summed over the
+// partials by 4 threads (quarters of the index range, added in order).
+constexpr int kCombThreads = 256;
+MOE_DEVINL float block_reduce(float v, bool is_max, float* red) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float o = __shfl_xor_sync(0xffffffffu, v, off);
+    v = is_max ? fmaxf(v, o) : v + o;
+  }
+  __syncthreads();  // red is free
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int w = 1; w < kCombThreads / 32; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
+  return r;
+}
+
+__global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const AttnParams p, int P) {
+  extern __shared__ float s_w[];  // [P] merge weights, then [4][64] quarter sums, then [8] reduction slots
+  float* quart = s_w + P;
+  float* red = quart + 4 * 64;
+  const int qh = blockIdx.x, e0 = blockIdx.y * 64, d = p.d;
   const float* pm = p.part_m + (int64_t)qh * P;
   const float* pl = p.part_l + (int64_t)qh * P;
-  float M = -INFINITY;
-  for (int i = 0; i < P; ++i) M = fmaxf(M, pm[i]);
-  float L = 0.f;
-  for (int i = 0; i < P; ++i)
-    if (pm[i] > -INFINITY) L = fmaf(pl[i], __expf(pm[i] - M), L);
-  const float inv = 1.f / L;
-  for (int t = threadIdx.x; t < d; t += blockDim.x) {
-    float o = 0.f;
-    for (int i = 0; i < P; ++i)
-      if (pm[i] > -INFINITY) o = fmaf(p.part_o[((int64_t)qh * P + i) * d + t], __expf(pm[i] - M), o);
-    p.out[(int64_t)qh * d + t] = o * inv;
+  float m = -INFINITY;
+  for (int i = threadIdx.x; i < P; i += kCombThreads) m = fmaxf(m, pm[i]);
+  const float M = block_reduce(m, true, red);
+  float l = 0.f;
+  for (int i = threadIdx.x; i < P; i += kCombThreads) {
+    const float mi = pm[i];
+    const float w = mi > -INFINITY ? __expf(mi - M) : 0.f;
+    s_w[i] = w;
+    l = fmaf(pl[i], w, l);
   }
+  const float inv = 1.f / block_reduce(l, false, red);  // also orders the s_w writes before the reads
+  const int t = threadIdx.x & 63, q = threadIdx.x >> 6;  // element, quarter of the partials
+  const int i0 = P * q / 4, i1 = P * (q + 1) / 4;
+  float o = 0.f;
+  if (e0 + t < d) {
+    const float* po = p.part_o + ((int64_t)qh * P) * d + e0 + t;
+#pragma unroll 4
+    for (int i = i0; i < i1; ++i) o = fmaf(po[(int64_t)i * d], s_w[i], o);
+  }
+  quart[q * 64 + t] = o;
+  __syncthreads();
+  if (threadIdx.x < 64 && e0 + t < d)
+    p.out[(int64_t)qh * d + e0 + t] = (((quart[t] + quart[64 + t]) + quart[128 + t]) + quart[192 + t]) * inv;
 }
 
 }  // namespace
@@ -149,7 +238,7 @@ bool attn_shape_supported(int L, int Hq, int Hkv, int d) {
 }
 
 int attn_splits(int L, int Hkv, int sms) {
-  const int by_len = (L + 255) / 256;           // at least 32 positions per warp
+  const int by_len = (L + 63) / 64;             // at least 8 positions per warp
   const int by_grid = std::max(1, 2 * sms / Hkv);  // about two blocks per SM
   return std::max(1, std::min(by_len, by_grid));
 }
@@ -168,15 +257,28 @@ cudaError_t attn_decode_launch(const AttnParams& pin, int sms, cudaStream_t s) {
   p.part_l = p.ws + (size_t)p.Hq * P;
   p.part_o = p.ws + 2 * (size_t)p.Hq * P;
   const dim3 grid(p.Hkv, splits);
-  if (p.d == 256)
-    attn_split_kernel<8><<<grid, 32 * kAttnWarps, 0, s>>>(p);
-  else if (p.d == 128)
-    attn_split_kernel<4><<<grid, 32 * kAttnWarps, 0, s>>>(p);
-  else
-    attn_split_kernel<2><<<grid, 32 * kAttnWarps, 0, s>>>(p);
-  cudaError_t err = cudaGetLastError();
+  const size_t ring = (size_t)kAttnWarps * kRing * 2 * p.d * 2;  // bf16 K and V rows per warp slot
+  cudaError_t err = cudaSuccess;
+  if (p.d == 256) {
+    err = cudaFuncSetAttribute(attn_split_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
+    if (err == cudaSuccess) attn_split_kernel<8><<<grid, 32 * kAttnWarps, ring, s>>>(p);
+  } else if (p.d == 128) {
+    err = cudaFuncSetAttribute(attn_split_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
+    if (err == cudaSuccess) attn_split_kernel<4><<<grid, 32 * kAttnWarps, ring, s>>>(p);
+  } else {
+    err = cudaFuncSetAttribute(attn_split_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
+    if (err == cudaSuccess) attn_split_kernel<2><<<grid, 32 * kAttnWarps, ring, s>>>(p);
+  }
   if (err != cudaSuccess) return err;
-  attn_combine_kernel<<<p.Hq, 256, 0, s>>>(p, splits * kAttnWarps);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const int P2 = splits * kAttnWarps;
+  const size_t comb_smem = ((size_t)P2 + 4 * 64 + kCombThreads / 32) * sizeof(float);
+  if (comb_smem > 48 * 1024) {
+    err = cudaFuncSetAttribute(attn_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)comb_smem);
+    if (err != cudaSuccess) return err;
+  }
+  attn_combine_kernel<<<dim3(p.Hq, (p.d + 63) / 64), kCombThreads, comb_smem, s>>>(p, P2);
   return cudaGetLastError();
 }
 
