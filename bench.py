@@ -585,13 +585,16 @@ def run_prefill(T, zipf, host0, args, peaks):
     rw = fwd.view("row_weight", (rows,), torch.float32)
     acc = fwd.view("out_acc", (T, d), torch.float32)
     t = dl.t
-    g1 = gpu_graph(lambda: ops.grouped_gemm_w4a16(
-        x16, [t["gate"], t["up"]], E, f, bm, nt, mt, bn, ops.EPI_SWIGLU, row_index=rt, n_rows=rows,
-        W_extra=[t["sh_gate"], t["sh_up"]], C=h), stream)
-    # the down projection runs on its own (taller) tile map at large T
+    # the down projection runs on its own (taller) tile map at large T, and
+    # gate/up joins it from 512 rows per expert (as the forward does)
     mt2, bn2 = fwd.views.down_max_tiles, fwd.views.down_block_n
     bm2 = fwd.view("down_block_map", (mt2, 4), torch.int32)
     nt2 = fwd.view("down_num_tiles", (1,), torch.int32)
+    tall = bn2 == 256 and T * k >= 512 * E
+    gu = (bm2, nt2, mt2, bn2) if tall else (bm, nt, mt, bn)
+    g1 = gpu_graph(lambda: ops.grouped_gemm_w4a16(
+        x16, [t["gate"], t["up"]], E, f, gu[0], gu[1], gu[2], gu[3], ops.EPI_SWIGLU, row_index=rt,
+        n_rows=rows, W_extra=[t["sh_gate"], t["sh_up"]], C=h), stream)
     g2 = gpu_graph(lambda: ops.grouped_gemm_w4a16(
         h, [t["down"]], E, d, bm2, nt2, mt2, bn2, ops.EPI_COMBINE, n_rows=rows,
         W_extra=[t["sh_down"]], row_scale=rw, out_row=rt, C=acc), stream)
@@ -617,7 +620,8 @@ def run_prefill(T, zipf, host0, args, peaks):
     counts = fwd.view("counts", (E,), torch.int32).cpu().numpy()
     weight_bytes = 257 * 1_769_472
     res = dict(
-        T=T, router_bias="zipf 1.5*ln(1/rank)" if zipf else None, block_n=bn,
+        T=T, router_bias="zipf 1.5*ln(1/rank)" if zipf else None, block_n=bn, gateup_block_n=gu[3],
+        down_block_n=bn2,
         tokens_per_s=round(T / t_layer, 1), ms=round(t_layer * 1e3, 4),
         deterministic_ms=round(t_det * 1e3, 4),
         fused_chain_ms=round(t_fused * 1e3, 4),

@@ -82,10 +82,20 @@ struct Cfg {
   static constexpr int kAStage = kATmem ? 0 : NMAT * kABytes;
   static constexpr int kBBytes = BN * kKB * 2;
   static constexpr int kQRing = kSQ * NMAT * kQStage;
-  static constexpr int kAccBufs = 2;
+  // Two accumulator buffers where they fit (the epilogue of one tile then
+  // overlaps the MMAs of the next); 256-row tiles of gate and up fill TMEM
+  // with one.
+  static constexpr int kAccBufs = 2 * NMAT * BN <= 512 ? 2 : 1;
   static constexpr int kACol = kAccBufs * NMAT * BN;  // first TMEM column of the A stages
-  static constexpr int kSB0 =
+  static constexpr int kSB0a =
       (kSmemBudget - kQRing - kEpiBytes - kRowInfoBytes - kSA * kAStage) / kBBytes;
+  // a tile too wide for three token stages within the budget takes what is
+  // left of the CTA's shared memory (barriers and alignment slack reserved)
+  static constexpr int kSB0 =
+      kSB0a >= 3 ? kSB0a
+                 : (232448 - 1024 - 8 * (2 * kSQ + 2 * kSA + 2 * 8 + 5) - 16 - kQRing - kEpiBytes -
+                    kRowInfoBytes - kSA * kAStage) /
+                       kBBytes;
   static constexpr int kSB = kSB0 > 8 ? 8 : kSB0;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kSA * kAStage;
@@ -749,9 +759,7 @@ cudaError_t launch_bn(const KParams& kp, cudaStream_t s) {
     case 32: return launch_t<32, NMAT, EPI, F16, QK>(kp, s);
     case 64: return launch_t<64, NMAT, EPI, F16, QK>(kp, s);
     case 128: return launch_t<128, NMAT, EPI, F16, QK>(kp, s);
-    case 256:  // one weight matrix only: two 256-column accumulators fill TMEM
-      if constexpr (NMAT == 1) return launch_t<256, NMAT, EPI, F16, QK>(kp, s);
-      return cudaErrorInvalidValue;
+    case 256: return launch_t<256, NMAT, EPI, F16, QK>(kp, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -121,8 +121,8 @@ FwdWs forward_ws(void* ws, const moe_shape_t* s, int bn, int flags) {
   r.wsplit = c.take<uint16_t>((size_t)3 * moe::router_split_rows(E, true) * s->d_model);
   // 256-row tiles pay off once the experts average 256 rows or more: each
   // tile's weights are dequantised once for twice the rows (below that they
-  // are mostly padding, and the combine epilogue's per-row copies dominate)
-  // (gate/up stays at 128: its two accumulators fill TMEM at that height)
+  // are mostly padding, and the combine epilogue's per-row copies dominate);
+  // gate/up joins at 512 rows per expert (see moe_forward)
   r.v.down_block_n = bn == 128 && (int64_t)T * k >= (int64_t)256 * E ? 256 : bn;
   // MOE_FWD_DOWN_WINDOWS, above kDownWindow tokens: the down map ordered by
   // token window (see RouteParams::window2)
@@ -364,9 +364,7 @@ int moe_grouped_gemm_w4a16(const uint16_t* A, int64_t A_rows, int K, const int32
   if (K < 64 || K % 64 || N < 128 || N % 128 || n_groups < 1 || A_rows < 0 || n_rows < 0 ||
       max_tiles < 0 || ldc < N || C_rows < 0)
     return MOE_ERR_SHAPE;
-  // 256-row tiles hold two 256-column accumulators: one weight matrix only
-  if (!valid_block_n(block_n) || (block_n == 256 && epilogue == MOE_EPI_SWIGLU))
-    return MOE_ERR_SHAPE;
+  if (!valid_block_n(block_n)) return MOE_ERR_SHAPE;
   if (epilogue != MOE_EPI_COMBINE && C_rows < n_rows) return MOE_ERR_SHAPE;
   // SWIGLU and COMBINE write 16-byte token-row segments (bulk copies)
   if (epilogue == MOE_EPI_SWIGLU && ldc % 8) return MOE_ERR_SHAPE;
@@ -565,10 +563,14 @@ int moe_forward_ex(const uint16_t* x, const moe_weights_t* w, const moe_shape_t*
   }
   g.n_groups = E;
   g.N = f;
-  g.block_map = v.block_map;
-  g.num_tiles = v.num_tiles;
-  g.max_tiles = v.max_tiles;
-  g.block_n = block_n;
+  // From 512 rows per expert on average, gate/up also runs on the down
+  // projection's 256-row map (one accumulator buffer then fills TMEM); at
+  // 256-511 rows per expert the 128-row tiles measured faster.
+  const bool tall = v.down_block_n == 256 && v.down_window == 0 && (int64_t)T * k >= (int64_t)512 * E;
+  g.block_map = tall ? v.down_block_map : v.block_map;
+  g.num_tiles = tall ? v.down_num_tiles : v.num_tiles;
+  g.max_tiles = tall ? v.down_max_tiles : v.max_tiles;
+  g.block_n = tall ? 256 : block_n;
   g.epilogue = MOE_EPI_SWIGLU;
   g.operand_f16 = 1;
   g.C = v.h;
@@ -765,7 +767,7 @@ int moe_gdn_scan(const uint16_t* q, const uint16_t* k, const uint16_t* v, const 
 
 size_t moe_decode_attention_workspace_bytes(int L, int n_q_heads, int n_kv_heads, int d) {
   if (!moe::attn_shape_supported(L, n_q_heads, n_kv_heads, d)) return 0;
-  // the split count never exceeds one per 256 positions, whatever the SM count
+  // the split count never exceeds one per 64 positions, whatever the SM count
   return moe::attn_workspace_floats(L, n_q_heads, n_kv_heads, d, 1 << 20) * sizeof(float);
 }
 

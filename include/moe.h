@@ -188,7 +188,9 @@ int moe_route(const float* logits, const float* logit_bias, int T, int n_experts
  *               SWIGLU needs ldc % 8 == 0, COMBINE ldc % 4 == 0.
  *   N           output columns (multiple of 128); K multiple of 64.
  *   ws          256-byte aligned, >= moe_gemm_workspace_bytes() bytes.
- * block_n in {16, 32, 64, 128}, or 256 for NONE and COMBINE (one weight matrix).
+ * block_n in {16, 32, 64, 128, 256}. At 256 with SWIGLU the two 256-column
+ * accumulators fill tensor memory, so a tile's epilogue no longer overlaps
+ * the next tile's products.
  */
 size_t moe_gemm_workspace_bytes(void);
 int moe_grouped_gemm_w4a16(const uint16_t* A, int64_t A_rows, int K, const int32_t* row_index,
@@ -275,7 +277,8 @@ typedef struct {
   int32_t block_n;     /* gate/up row-tile height */
   /* The down projection's block map. Equal to block_map/num_tiles/max_tiles
      unless block_n is 128 and T*top_k >= 256*n_experts: the down projection
-     (one weight matrix) then runs on 256-row tiles of a second map. */
+     then runs on 256-row tiles of a second map, and from T*top_k >=
+     512*n_experts (without MOE_FWD_DOWN_WINDOWS) so does gate/up. */
   int32_t* down_block_map;
   int32_t* down_num_tiles;
   int32_t down_max_tiles;

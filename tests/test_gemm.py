@@ -126,7 +126,9 @@ def test_one_hot_reads_back_dequantised_weights(orc, fmt):
     ("f16", 16, 333, 16, 4, 1024), ("f16", 128, 333, 16, 4, 1024), ("bf16", 64, 333, 16, 4, 1024),
     # experts with 2-3 tiles and ragged last tiles (the MMA's N follows the
     # tile's rows); K/64 not a multiple of 4 (one k-block per packed-code stage)
-    ("f16", 128, 700, 8, 3, 1024), ("f16", 128, 333, 16, 4, 320)])
+    ("f16", 128, 700, 8, 3, 1024), ("f16", 128, 333, 16, 4, 320),
+    # 256-row tiles: both accumulators fill tensor memory (one buffer)
+    ("f16", 256, 700, 8, 3, 1024), ("bf16", 256, 333, 16, 4, 320)])
 def test_swiglu_epilogue_with_shared_group(orc, bn, fmt, T, E, k, K):
     from bit_moe_expert_route_gb300 import ops
     shape = LayerShape(d_model=K, n_experts=16, top_k=4, d_ff=256, d_ff_shared=256)
@@ -154,6 +156,26 @@ def test_swiglu_epilogue_with_shared_group(orc, bn, fmt, T, E, k, K):
     tol = 1e-3 if fmt == "f16" else 4e-3  # rounding of h to the operand format dominates
     assert np.linalg.norm(err) / np.linalg.norm(ref) < tol
     assert np.max(np.abs(err) / (np.abs(ref) + 1e-2 * np.sqrt(np.mean(ref ** 2)))) < 5 * tol
+
+
+@pytest.mark.parametrize("K", [1024, 320])
+def test_swiglu_tile_height_leaves_h_unchanged(orc, K):
+    """Each output row is the same sum over K whatever tile it sits in: the
+    gate/up products on 256-row tiles equal those on 128-row tiles bit for bit."""
+    from bit_moe_expert_route_gb300 import ops
+    T, E, k, N = 1500, 8, 3, 256
+    shape = LayerShape(d_model=K, n_experts=16, top_k=4, d_ff=256, d_ff_shared=256)
+    w = synth.layer_weights(shape, seed=11)
+    X = round_fmt(synth.bf16_to_f32(synth.tokens(shape, T, seed=11)), "f16")
+    outs = []
+    for bn in (128, 256):
+        ids, m = routing(orc, T, E, k, bn, seed=11)
+        rt = torch.from_numpy(m["row_token"]).cuda()
+        C, ws = gemm_call(dev(to_fmt(X, "f16")), [w["gate"], w["up"]], E, N, m, bn, ops.EPI_SWIGLU,
+                          "f16", row_index=rt, extra=[w["sh_gate"], w["sh_up"]])
+        assert ops.device_status(ws) == 0
+        outs.append(C.view(torch.int16).cpu().numpy())
+    assert np.array_equal(outs[0], outs[1])
 
 
 @pytest.mark.parametrize("fmt,bn", [("f16", 32), ("bf16", 64), ("f16", 256)])
