@@ -59,6 +59,22 @@ MOE_DEVINL float group_fdot(const uint32_t (&w)[8], const uint16_t* v, int g) {
   return a0 + a1;
 }
 
+// Sum of the 64 bf16 values of one group (any order of the values inside
+// it): the 32 words start at a lane-dependent word, so that the lanes of a
+// warp, each summing its own group, read 32 different banks.
+MOE_DEVINL float group_sum64(const uint16_t* v) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(v);
+  const int r = threadIdx.x & 31;
+  float a = 0.f, b = 0.f;
+#pragma unroll 8
+  for (int j = 0; j < 32; ++j) {
+    const uint32_t u = w[(j + r) & 31];
+    a += __uint_as_float(u << 16);
+    b += __uint_as_float(u & 0xFFFF0000u);
+  }
+  return a + b;
+}
+
 // ---------------------------------------------------------------- 1. router
 template <int TB>  // token capacity: T <= TB
 __global__ void __launch_bounds__(kBThreads) batch_router_kernel(const __grid_constant__ BatchParams p) {
@@ -154,6 +170,15 @@ __global__ void __launch_bounds__(kBThreads, 2) batch_gateup_kernel(const __grid
   int* s_ids = reinterpret_cast<int*>(xsum + (size_t)T * ng);                      // [T][k]
   uint32_t* keys = reinterpret_cast<uint32_t*>(s_ids + T * k);                     // [T][E] order keys
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int kKB = 8;  // experts per lane per batch of the top-k, all partials loaded first
+  // the router bias of this lane's first batch of experts (weights, not
+  // written by the previous kernel): loaded before the dependency wait
+  float bias0[kKB];
+#pragma unroll
+  for (int m = 0; m < kKB; ++m) {
+    const int e = lane + m * 32;
+    bias0[m] = p.w.router_bias && warp < T && e < E ? p.w.router_bias[e] : 0.f;
+  }
   pdl_wait_b();
   pdl_launch_b();
   for (int i = tid; i < T * d / 8; i += kBThreads) {  // piece i: row i / (d/8), group (i % (d/8)) / 8
@@ -165,7 +190,6 @@ __global__ void __launch_bounds__(kBThreads, 2) batch_gateup_kernel(const __grid
   if (warp < T) {
     const int t = warp;
     uint32_t* kr = keys + (size_t)t * E;  // order keys of this token's experts
-    constexpr int kKB = 8;                // experts per lane per batch, all partials loaded first
     for (int e0 = lane; e0 < E; e0 += kKB * 32) {
       float z[kKB][kBatchKS];
 #pragma unroll
@@ -183,7 +207,7 @@ __global__ void __launch_bounds__(kBThreads, 2) batch_gateup_kernel(const __grid
 #pragma unroll
         for (int q = 0; q < kBatchKS; ++q) v += z[m][q];  // fixed order
         if (blockIdx.x == 0) p.logits[(size_t)t * E + e] = v;
-        if (p.w.router_bias) v = v + p.w.router_bias[e];
+        if (p.w.router_bias) v = v + (e0 == lane ? bias0[m] : p.w.router_bias[e]);
         kr[e] = order_key(v);
       }
     }
@@ -228,13 +252,12 @@ __global__ void __launch_bounds__(kBThreads, 2) batch_gateup_kernel(const __grid
     }
   }
   __syncthreads();
+  const int n_routed = T * k * f, n_tasks = n_routed + (p.shared ? T * f : 0);
+  const int gw = blockIdx.x * kBWarps + warp, nw = gridDim.x * kBWarps;
+  const int per = (n_tasks + nw - 1) / nw;
+  const int i_lo = min(n_tasks, gw * per), i_hi = min(n_tasks, i_lo + per);
   // group sums of x per token
-  for (int i = tid; i < T * ng; i += kBThreads) {
-    const uint16_t* v = xs + (size_t)(i / ng) * d + (i % ng) * 64;
-    float s = 0.f;
-    for (int j = 0; j < 64; ++j) s += bf16f(v[j]);
-    xsum[i] = s;
-  }
+  for (int i = tid; i < T * ng; i += kBThreads) xsum[i] = group_sum64(xs + (size_t)(i / ng) * d + (i % ng) * 64);
   __syncthreads();
   // tasks: (slot i of T*k, row r): token i / k times its expert's row r;
   // then (shared row r, token t) at T*k*f + t*f + r. Each warp takes a
@@ -243,10 +266,6 @@ __global__ void __launch_bounds__(kBThreads, 2) batch_gateup_kernel(const __grid
   // matrix, one group, per pass). Rows of an expert that two tokens select
   // are read once per token (the second read mostly from L2).
   constexpr int kIB = 3;
-  const int n_routed = T * k * f, n_tasks = n_routed + (p.shared ? T * f : 0);
-  const int gw = blockIdx.x * kBWarps + warp, nw = gridDim.x * kBWarps;
-  const int per = (n_tasks + nw - 1) / nw;
-  const int i_lo = min(n_tasks, gw * per), i_hi = min(n_tasks, i_lo + per);
   for (int i0 = i_lo; i0 < i_hi; i0 += kIB) {
     int tok[kIB], srow[kIB];
     bool live[kIB], shr[kIB];
@@ -328,12 +347,13 @@ __global__ void __launch_bounds__(kBThreads, 2) batch_down_kernel(const __grid_c
   float* s_w = hsum + (size_t)T * S * ngf;                                          // [T][S]
   int* s_ids = reinterpret_cast<int*>(s_w + T * S);                                 // [T][k]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gw = blockIdx.x * kBWarps + warp, nw = gridDim.x * kBWarps;
   pdl_wait_b();
   pdl_launch_b();
   // h as bf16 (the operand precision of the down projection; swizzled like
   // x above), group sums, routing weights and ids
   {
-    constexpr int kHB = 4;  // pieces (8 values, two float4) per thread per batch, loads first
+    constexpr int kHB = 6;  // pieces (8 values, two float4) per thread per batch, loads first
     const int n8 = T * S * f / 8;
     for (int i0 = tid; i0 < n8; i0 += kHB * kBThreads) {
       float4 v[kHB][2];
@@ -367,17 +387,11 @@ __global__ void __launch_bounds__(kBThreads, 2) batch_down_kernel(const __grid_c
   for (int i = tid; i < T * S; i += kBThreads) s_w[i] = p.wts[i];
   for (int i = tid; i < T * k; i += kBThreads) s_ids[i] = p.ids[i];
   __syncthreads();
-  for (int i = tid; i < T * S * ngf; i += kBThreads) {
-    const uint16_t* v = hs + (size_t)i * 64;
-    float s = 0.f;
-    for (int j = 0; j < 64; ++j) s += bf16f(v[j]);
-    hsum[i] = s;
-  }
+  for (int i = tid; i < T * S * ngf; i += kBThreads) hsum[i] = group_sum64(hs + (size_t)i * 64);
   __syncthreads();
   // one warp per output column; its lanes share the (token, slot, group)
   // items of the routed rows, then the groups of the shared expert's row
   // (which serves every token)
-  const int gw = blockIdx.x * kBWarps + warp, nw = gridDim.x * kBWarps;
   const int n_routed = T * k * ngf;
   constexpr int kDB = 8;  // routed items per lane per batch, loads issued first
   for (int j = gw; j < d; j += nw) {
@@ -387,12 +401,14 @@ __global__ void __launch_bounds__(kBThreads, 2) batch_down_kernel(const __grid_c
     for (int u0 = lane; u0 < n_routed; u0 += kDB * 32) {
       uint4 qa[kDB], qb[kDB];
       float sc[kDB], bi[kDB];
+      int tk[kDB];  // the item's token, found once
 #pragma unroll
       for (int m = 0; m < kDB; ++m) {
         const int u = u0 + m * 32;
         if (u >= n_routed) break;
-        const int ts0 = u / ngf, g = u % ngf, t = ts0 / k, s = ts0 % k;
-        const size_t row = (size_t)s_ids[t * k + s] * d + j;
+        const int ts0 = u / ngf, g = u - ts0 * ngf, t = ts0 / k, s = ts0 - t * k;
+        tk[m] = t;
+        const size_t row = (size_t)s_ids[ts0] * d + j;
         const uint4* q = reinterpret_cast<const uint4*>(p.w.down.q + row * (f / 8) + g * 8);
         qa[m] = q[0];
         qb[m] = q[1];
@@ -404,7 +420,7 @@ __global__ void __launch_bounds__(kBThreads, 2) batch_down_kernel(const __grid_c
       for (int m = 0; m < kDB; ++m) {
         const int u = u0 + m * 32;
         if (u >= n_routed) break;
-        const int ts0 = u / ngf, g = u % ngf, t = ts0 / k, s = ts0 % k, ts = t * S + s;
+        const int ts0 = u / ngf, g = u - ts0 * ngf, t = tk[m], ts = ts0 + t;  // t * k + s + t = t * S + s
         const uint32_t w[8] = {qa[m].x, qa[m].y, qa[m].z, qa[m].w, qb[m].x, qb[m].y, qb[m].z, qb[m].w};
         const float dot = fmaf(16.f * sc[m], group_fdot(w, hs + ((size_t)ts * f + g * 64), g),
                                (bi[m] - 16.f * sc[m]) * hsum[ts * ngf + g]);
