@@ -50,7 +50,9 @@ def close(got, ref):
 
 @pytest.mark.parametrize("T,Hk,Hv,dk,dv", [(1, 2, 4, 128, 128), (5, 2, 4, 128, 64),
                                            (64, 2, 4, 64, 128), (64, 1, 3, 128, 8),
-                                           (300, 4, 8, 128, 128)])
+                                           (300, 4, 8, 128, 128),
+                                           # 2 rows per warp (dv % 32 != 0); chunk edges at 32, 64
+                                           (65, 2, 2, 64, 48), (33, 1, 2, 128, 16)])
 def test_scan_matches_oracle(T, Hk, Hv, dk, dv):
     from bit_moe_expert_route_gb300 import ops
     host = inputs(T, Hk, Hv, dk, dv, seed=T + dk)
