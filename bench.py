@@ -367,8 +367,9 @@ def run_gdn(args, peaks):
                                    peak=round(fp32_peak, 1), unit="TFLOP/s",
                                    frac=round(flop / t_pre / 1e12 / fp32_peak, 4),
                                    flop_per_token=6 * Hv * dv * dk,
-                                   kernel="gdn_scan_kernel: one warp per state row, the row in "
-                                          "registers for all T tokens",
+                                   kernel="gdn_scan_kernel: each state row in the registers of 8 "
+                                          "lanes (4 rows per warp) for all T tokens; one butterfly "
+                                          "per token",
                                    peak_source="SM count x 128 fp32 lanes x 2 x max SM clock")),
         decode=dict(us_per_layer=round(t_dec * 1e6, 3),
                     tokens_per_s_30_layers=round(1 / (t_dec * GDN_LAYERS), 1),
