@@ -13,9 +13,9 @@
 // j = j0 + w, j0 + w + 8, ... of its slice. Lane l holds elements
 // l*E .. l*E+E-1 (E = d / 32) of q (pre-scaled), of the current k and v rows
 // and of the running output of every query head. Per position: the group's
-// scores (E-term partial dots, butterfly warp sums), then the online softmax
-// update per head (running max m, running sum l, output rescaled when the max
-// grows). Each warp writes its (m, l, unnormalised output) per head as one
+// scores (E-term partial dots, one transpose reduction for all heads), then
+// the online softmax update per head (running max m, running sum l; the
+// output is rescaled only when the max grows). Each warp writes its (m, l, unnormalised output) per head as one
 // partial. Combine kernel: per query head and 64 output elements, all
 // partials merged with weights exp(m_part - max m) and divided by the merged
 // sum (block-wide reductions in a fixed order).
@@ -54,7 +54,7 @@ MOE_DEVINL void load_row(const uint16_t* p, float (&f)[E]) {
   }
 }
 
-constexpr int kRing = 8;  // positions in flight per warp
+constexpr int kRing = 16;  // positions in flight per warp
 
 // 16-, 8- or 4-byte cp.async global -> shared (the lane's own elements of a row)
 template <int B>
@@ -88,10 +88,32 @@ MOE_DEVINL void load_row_smem(const uint8_t* p, float (&f)[E]) {
   }
 }
 
-MOE_DEVINL float attn_warp_sum(float v) {
+// The group's 8 scores from each lane's partial dots x[h]: a transpose
+// reduction (at the step across lane bit b, a lane keeps half of its values
+// and adds the partner's copies of them: 4 + 2 + 1 shuffles), the remaining
+// two steps of a butterfly, then each head's sum broadcast from a lane that
+// holds it: 17 shuffles instead of 8 butterflies of 5. x[h] becomes head h's
+// full sum on every lane.
+MOE_DEVINL void group_scores(float (&x)[kAttnMaxGroup], int lane) {
+  constexpr unsigned kAll = 0xffffffffu;
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+  float y[4], z[2];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
+  for (int i = 0; i < 4; ++i) {  // heads 4 b4 + i
+    const float send = b4 ? x[i] : x[i + 4], keep = b4 ? x[i + 4] : x[i];
+    y[i] = keep + __shfl_xor_sync(kAll, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {  // heads 4 b4 + 2 b3 + i
+    const float send = b3 ? y[i] : y[i + 2], keep = b3 ? y[i + 2] : y[i];
+    z[i] = keep + __shfl_xor_sync(kAll, send, 8);
+  }
+  float w = (b2 ? z[1] : z[0]) + __shfl_xor_sync(kAll, b2 ? z[0] : z[1], 4);  // head 4 b4 + 2 b3 + b2
+  w += __shfl_xor_sync(kAll, w, 2);
+  w += __shfl_xor_sync(kAll, w, 1);
+#pragma unroll
+  for (int h = 0; h < kAttnMaxGroup; ++h)
+    x[h] = __shfl_sync(kAll, w, ((h >> 2) << 4) | (((h >> 1) & 1) << 3) | ((h & 1) << 2));
 }
 
 template <int E>
@@ -101,6 +123,24 @@ __global__ void __launch_bounds__(32 * kAttnWarps, 1) attn_split_kernel(const At
   const int G = p.Hq / p.Hkv, d = 32 * E;
   const int per = (p.L + gridDim.y - 1) / gridDim.y;
   const int j0 = split * per, j1 = min(p.L, j0 + per);
+  // K and V rows of the warp's next kRing positions in flight: each lane
+  // copies (cp.async) exactly the E elements of each row it later reads, into
+  // its own slots of a per-warp shared-memory ring, so the ring needs no
+  // synchronisation beyond the lane's own wait_group
+  extern __shared__ __align__(16) uint8_t attn_ring[];
+  uint8_t* ring = attn_ring + (size_t)warp * kRing * 2 * (32 * E * 2);
+  auto slot = [&](int r, int kv) { return smem_u32(ring + ((size_t)(r * 2 + kv) * 32 + lane) * (E * 2)); };
+  auto issue = [&](int j, int r) {
+    if (j < j1) {
+      const int64_t row = ((int64_t)j * p.Hkv + g) * d + lane * E;
+      cp_async_bytes<E * 2>(slot(r, 0), p.K + row);
+      cp_async_bytes<E * 2>(slot(r, 1), p.V + row);
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int r = 0; r < kRing; ++r) issue(j0 + warp + r * kAttnWarps, r);
+  // q and the running state (after the first copies are on their way)
   float q[kAttnMaxGroup][E], acc[kAttnMaxGroup][E], m[kAttnMaxGroup], l[kAttnMaxGroup];
 #pragma unroll
   for (int h = 0; h < kAttnMaxGroup; ++h) {
@@ -119,23 +159,6 @@ __global__ void __launch_bounds__(32 * kAttnWarps, 1) attn_split_kernel(const At
     m[h] = -INFINITY;
     l[h] = 0.f;
   }
-  // K and V rows of the warp's next kRing positions in flight: each lane
-  // copies (cp.async) exactly the E elements of each row it later reads, into
-  // its own slots of a per-warp shared-memory ring, so the ring needs no
-  // synchronisation beyond the lane's own wait_group
-  extern __shared__ __align__(16) uint8_t attn_ring[];
-  uint8_t* ring = attn_ring + (size_t)warp * kRing * 2 * (32 * E * 2);
-  auto slot = [&](int r, int kv) { return smem_u32(ring + ((size_t)(r * 2 + kv) * 32 + lane) * (E * 2)); };
-  auto issue = [&](int j, int r) {
-    if (j < j1) {
-      const int64_t row = ((int64_t)j * p.Hkv + g) * d + lane * E;
-      cp_async_bytes<E * 2>(slot(r, 0), p.K + row);
-      cp_async_bytes<E * 2>(slot(r, 1), p.V + row);
-    }
-    cp_async_commit();
-  };
-#pragma unroll
-  for (int r = 0; r < kRing; ++r) issue(j0 + warp + r * kAttnWarps, r);
   int r = 0;
 #pragma unroll 1
   for (int j = j0 + warp; j < j1; j += kAttnWarps, r = (r + 1) % kRing) {
@@ -144,20 +167,29 @@ __global__ void __launch_bounds__(32 * kAttnWarps, 1) attn_split_kernel(const At
     load_row_smem<E>(ring + ((size_t)(r * 2 + 0) * 32 + lane) * (E * 2), k);
     load_row_smem<E>(ring + ((size_t)(r * 2 + 1) * 32 + lane) * (E * 2), v);
     issue(j + kRing * kAttnWarps, r);  // the slot is read: refill it
+    float sc[kAttnMaxGroup];  // (q of the heads past G is zero)
+#pragma unroll
+    for (int h = 0; h < kAttnMaxGroup; ++h) {
+      sc[h] = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) sc[h] = fmaf(q[h][e], k[e], sc[h]);
+    }
+    group_scores(sc, lane);
 #pragma unroll
     for (int h = 0; h < kAttnMaxGroup; ++h) {
       if (h >= G) break;
-      float s = 0.f;
+      const float s = sc[h];
+      if (s > m[h]) {  // the running max moves (the same on every lane): rescale; 0 while m is -inf
+        const float c = __expf(m[h] - s);
+        l[h] *= c;
 #pragma unroll
-      for (int e = 0; e < E; ++e) s = fmaf(q[h][e], k[e], s);
-      s = attn_warp_sum(s);
-      const float m_new = fmaxf(m[h], s);
-      const float c = __expf(m[h] - m_new);  // 0 while m is still -inf
-      const float w = __expf(s - m_new);
-      l[h] = fmaf(l[h], c, w);
+        for (int e = 0; e < E; ++e) acc[h][e] *= c;
+        m[h] = s;
+      }
+      const float w = __expf(s - m[h]);
+      l[h] += w;
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[h][e] = fmaf(acc[h][e], c, w * v[e]);
-      m[h] = m_new;
+      for (int e = 0; e < E; ++e) acc[h][e] = fmaf(w, v[e], acc[h][e]);
     }
   }
   // one partial per (warp, query head): running max, running sum, output
@@ -237,39 +269,49 @@ bool attn_shape_supported(int L, int Hq, int Hkv, int d) {
          Hq / Hkv <= kAttnMaxGroup;
 }
 
-int attn_splits(int L, int Hkv, int sms) {
-  const int by_len = (L + 63) / 64;             // at least 8 positions per warp
-  const int by_grid = std::max(1, 2 * sms / Hkv);  // about two blocks per SM
+// slots: blocks resident at once on the GPU (blocks per SM x SMs).
+int attn_splits(int L, int Hkv, int slots) {
+  const int by_len = (L + 63) / 64;                // at least 8 positions per warp
+  const int by_grid = std::max(1, slots / Hkv);    // one wave of resident blocks
   return std::max(1, std::min(by_len, by_grid));
 }
 
-size_t attn_workspace_floats(int L, int Hq, int Hkv, int d, int sms) {
-  const size_t P = (size_t)attn_splits(L, Hkv, sms) * kAttnWarps;
+size_t attn_workspace_floats(int L, int Hq, int Hkv, int d, int slots) {
+  const size_t P = (size_t)attn_splits(L, Hkv, slots) * kAttnWarps;
   return (size_t)Hq * P * (2 + (size_t)d);
+}
+
+template <int E>
+cudaError_t split_setup(size_t ring, int sms, int* slots) {
+  cudaError_t err = cudaFuncSetAttribute(attn_split_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
+  if (err != cudaSuccess) return err;
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_split_kernel<E>, 32 * kAttnWarps, ring);
+  *slots = std::max(1, per_sm) * sms;
+  return err;
 }
 
 cudaError_t attn_decode_launch(const AttnParams& pin, int sms, cudaStream_t s) {
   if (!attn_shape_supported(pin.L, pin.Hq, pin.Hkv, pin.d) || !pin.ws) return cudaErrorInvalidValue;
-  const int splits = attn_splits(pin.L, pin.Hkv, sms);
+  const size_t ring = (size_t)kAttnWarps * kRing * 2 * pin.d * 2;  // bf16 K and V rows per warp slot
+  int slots = sms;
+  cudaError_t err = pin.d == 256 ? split_setup<8>(ring, sms, &slots)
+                    : pin.d == 128 ? split_setup<4>(ring, sms, &slots)
+                                   : split_setup<2>(ring, sms, &slots);
+  if (err != cudaSuccess) return err;
+  const int splits = attn_splits(pin.L, pin.Hkv, slots);
   const size_t P = (size_t)splits * kAttnWarps;  // partials per query head
   AttnParams p = pin;
   p.part_m = p.ws;
   p.part_l = p.ws + (size_t)p.Hq * P;
   p.part_o = p.ws + 2 * (size_t)p.Hq * P;
   const dim3 grid(p.Hkv, splits);
-  const size_t ring = (size_t)kAttnWarps * kRing * 2 * p.d * 2;  // bf16 K and V rows per warp slot
-  cudaError_t err = cudaSuccess;
-  if (p.d == 256) {
-    err = cudaFuncSetAttribute(attn_split_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
-    if (err == cudaSuccess) attn_split_kernel<8><<<grid, 32 * kAttnWarps, ring, s>>>(p);
-  } else if (p.d == 128) {
-    err = cudaFuncSetAttribute(attn_split_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
-    if (err == cudaSuccess) attn_split_kernel<4><<<grid, 32 * kAttnWarps, ring, s>>>(p);
-  } else {
-    err = cudaFuncSetAttribute(attn_split_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
-    if (err == cudaSuccess) attn_split_kernel<2><<<grid, 32 * kAttnWarps, ring, s>>>(p);
-  }
-  if (err != cudaSuccess) return err;
+  if (p.d == 256)
+    attn_split_kernel<8><<<grid, 32 * kAttnWarps, ring, s>>>(p);
+  else if (p.d == 128)
+    attn_split_kernel<4><<<grid, 32 * kAttnWarps, ring, s>>>(p);
+  else
+    attn_split_kernel<2><<<grid, 32 * kAttnWarps, ring, s>>>(p);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const int P2 = splits * kAttnWarps;

@@ -190,8 +190,8 @@ struct AttnParams {
   float* out;
 };
 bool attn_shape_supported(int L, int Hq, int Hkv, int d);
-int attn_splits(int L, int Hkv, int sms);
-size_t attn_workspace_floats(int L, int Hq, int Hkv, int d, int sms);
+int attn_splits(int L, int Hkv, int slots);  // slots: blocks resident at once
+size_t attn_workspace_floats(int L, int Hq, int Hkv, int d, int slots);
 cudaError_t attn_decode_launch(const AttnParams& p, int sms, cudaStream_t s);
 
 // Deterministic combine: acc[t] = sum, in slot order (routed slots, then the
