@@ -271,7 +271,7 @@ bool attn_shape_supported(int L, int Hq, int Hkv, int d) {
 
 // slots: blocks resident at once on the GPU (blocks per SM x SMs).
 int attn_splits(int L, int Hkv, int slots) {
-  const int by_len = (L + 63) / 64;                // at least 8 positions per warp
+  const int by_len = (L + 127) / 128;              // at least 16 positions per warp
   const int by_grid = std::max(1, slots / Hkv);    // one wave of resident blocks
   return std::max(1, std::min(by_len, by_grid));
 }
