@@ -658,15 +658,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
           }
         } else if constexpr (EPI == MOE_EPI_SWIGLU) {
           // straight from registers: per token row, the warp's 32 outputs are
-          // 64 contiguous bytes of h (no staging, barriers or bulk copies)
+          // 64 contiguous bytes of h (no staging, barriers or bulk copies).
+          // Every column is computed first (columns past the tile's rows are
+          // never stored, whatever they hold), so the chunk's exp/reciprocal
+          // chains overlap instead of running one token row at a time behind
+          // a row-count branch.
           uint16_t* hrow = static_cast<uint16_t*>(g.C) + (int64_t)t.row0 * g.ldc + col0 + lane;
 #pragma unroll
           for (int i = 0; i < CH; ++i) {
-            const int n = c0 + i;
-            if (n >= t.rows) break;
             const float a = __uint_as_float(v0[i]);
-            hrow[(int64_t)n * g.ldc] = to_operand<F16>(__fdividef(a, 1.f + __expf(-a)) * __uint_as_float(v1[i]));
+            v0[i] = to_operand<F16>(__fdividef(a, 1.f + __expf(-a)) * __uint_as_float(v1[i]));
           }
+          const int nv = t.rows - c0;  // token rows of this chunk inside the tile
+#pragma unroll
+          for (int i = 0; i < CH; ++i)
+            if (i < nv) hrow[(int64_t)(c0 + i) * g.ldc] = (uint16_t)v0[i];
         } else {
           const int sb = chunk & 1;
           // the copies issued from this buffer two chunks ago have read it
