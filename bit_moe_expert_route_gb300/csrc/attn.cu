@@ -10,15 +10,16 @@
 //   o_h = sum_j softmax_j(scale * q_h . k_{g,j}) v_{g,j},   g = h / (Hq / Hkv)
 //
 // Split kernel: grid (Hkv, splits); 8 warps per block, warp w takes positions
-// j = j0 + w, j0 + w + 8, ... of its slice. Lane l holds elements
-// l*E .. l*E+E-1 (E = d / 32) of q (pre-scaled), of the current k and v rows
-// and of the running output of every query head. Per position: the group's
-// scores (E-term partial dots, one transpose reduction for all heads), then
-// the online softmax update per head (running max m, running sum l; the
-// output is rescaled only when the max grows). Each warp writes its (m, l, unnormalised output) per head as one
-// partial. Combine kernel: per query head and 64 output elements, all
-// partials merged with weights exp(m_part - max m) and divided by the merged
-// sum (block-wide reductions in a fixed order).
+// j = j0 + w, j0 + w + 8, ... of its slice, two per step. Lane l holds
+// elements l*E .. l*E+E-1 (E = d / 32) of q (pre-scaled), of the current k and
+// v rows and of the running output of every query head. Per position: the
+// group's scores (E-term partial dots, one transpose reduction for all
+// heads), then the online softmax update per head (running max m, running sum
+// l; the output is rescaled only when the max grows). The block's 8 warp
+// states merge (in warp order) into one partial (m, l, unnormalised output)
+// per query head. Combine kernel: per query head and 64 output elements, the
+// blocks' partials merged with weights exp(m_part - max m) and divided by the
+// merged sum (block-wide reductions in a fixed order).
 #include <algorithm>
 #include <cmath>
 
@@ -159,26 +160,43 @@ __global__ void __launch_bounds__(32 * kAttnWarps, 1) attn_split_kernel(const At
     m[h] = -INFINITY;
     l[h] = 0.f;
   }
+  // Two positions per step (j and j + 8, ring slots r and r + 1): their
+  // score reductions and softmax updates are independent chains that
+  // overlap. A second position past the slice's end counts as score -inf
+  // with its v taken as zero (its ring slot was never filled).
   int r = 0;
 #pragma unroll 1
-  for (int j = j0 + warp; j < j1; j += kAttnWarps, r = (r + 1) % kRing) {
-    cp_async_wait<kRing - 1>();
-    float k[E], v[E];
-    load_row_smem<E>(ring + ((size_t)(r * 2 + 0) * 32 + lane) * (E * 2), k);
-    load_row_smem<E>(ring + ((size_t)(r * 2 + 1) * 32 + lane) * (E * 2), v);
-    issue(j + kRing * kAttnWarps, r);  // the slot is read: refill it
-    float sc[kAttnMaxGroup];  // (q of the heads past G is zero)
+  for (int j = j0 + warp; j < j1; j += 2 * kAttnWarps, r = (r + 2) % kRing) {
+    const bool two = j + kAttnWarps < j1;
+    cp_async_wait<kRing - 2>();
+    float k[2][E], v[2][E];
 #pragma unroll
-    for (int h = 0; h < kAttnMaxGroup; ++h) {
-      sc[h] = 0.f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) sc[h] = fmaf(q[h][e], k[e], sc[h]);
+    for (int t = 0; t < 2; ++t) {
+      load_row_smem<E>(ring + ((size_t)((r + t) * 2 + 0) * 32 + lane) * (E * 2), k[t]);
+      load_row_smem<E>(ring + ((size_t)((r + t) * 2 + 1) * 32 + lane) * (E * 2), v[t]);
     }
-    group_scores(sc, lane);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) issue(j + (kRing + t) * kAttnWarps, r + t);  // the slots are read: refill them
+    if (!two) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[1][e] = 0.f;
+    }
+    float sc[2][kAttnMaxGroup];  // (q of the heads past G is zero)
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int h = 0; h < kAttnMaxGroup; ++h) {
+        sc[t][h] = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) sc[t][h] = fmaf(q[h][e], k[t][e], sc[t][h]);
+      }
+    group_scores(sc[0], lane);
+    group_scores(sc[1], lane);
 #pragma unroll
     for (int h = 0; h < kAttnMaxGroup; ++h) {
       if (h >= G) break;
-      const float s = sc[h];
+      const float s0 = sc[0][h], s1 = two ? sc[1][h] : -INFINITY;
+      const float s = fmaxf(s0, s1);
       if (s > m[h]) {  // the running max moves (the same on every lane): rescale; 0 while m is -inf
         const float c = __expf(m[h] - s);
         l[h] *= c;
@@ -186,25 +204,50 @@ __global__ void __launch_bounds__(32 * kAttnWarps, 1) attn_split_kernel(const At
         for (int e = 0; e < E; ++e) acc[h][e] *= c;
         m[h] = s;
       }
-      const float w = __expf(s - m[h]);
-      l[h] += w;
+      const float w0 = __expf(s0 - m[h]), w1 = __expf(s1 - m[h]);
+      l[h] += w0 + w1;
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[h][e] = fmaf(w, v[e], acc[h][e]);
+      for (int e = 0; e < E; ++e) acc[h][e] = fmaf(w1, v[1][e], fmaf(w0, v[0][e], acc[h][e]));
     }
   }
-  // one partial per (warp, query head): running max, running sum, output
-  const int P = gridDim.y * kAttnWarps, part = split * kAttnWarps + warp;
+  // the warps' states merge into one partial per (block, query head): each
+  // warp's (m, l, output) goes to shared memory (the ring, once every copy
+  // has landed), then each (head, element) is merged over the warps in order
+  cp_async_wait<0>();
+  __syncthreads();
+  float* st = reinterpret_cast<float*>(attn_ring);  // [warp][head][2 + d]
 #pragma unroll
   for (int h = 0; h < kAttnMaxGroup; ++h) {
     if (h >= G) break;
-    const int qh = g * G + h;
+    float* w = st + (size_t)(warp * G + h) * (2 + d);
     if (lane == 0) {
-      p.part_m[(int64_t)qh * P + part] = m[h];
-      p.part_l[(int64_t)qh * P + part] = l[h];
+      w[0] = m[h];
+      w[1] = l[h];
     }
-    float* o = p.part_o + ((int64_t)qh * P + part) * d + lane * E;
 #pragma unroll
-    for (int e = 0; e < E; ++e) o[e] = acc[h][e];
+    for (int e = 0; e < E; ++e) w[2 + lane * E + e] = acc[h][e];
+  }
+  __syncthreads();
+  const int P = gridDim.y;
+  for (int i = threadIdx.x; i < G * d; i += blockDim.x) {
+    const int h = i / d, e = i - h * d;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, st[(size_t)(w * G + h) * (2 + d)]);
+    float sl = 0.f, so = 0.f;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) {
+      const float* ws = st + (size_t)(w * G + h) * (2 + d);
+      const float c = ws[0] > -INFINITY ? __expf(ws[0] - M) : 0.f;
+      sl = fmaf(ws[1], c, sl);
+      so = fmaf(ws[2 + e], c, so);
+    }
+    const int qh = g * G + h;
+    if (e == 0) {
+      p.part_m[(int64_t)qh * P + split] = M;
+      p.part_l[(int64_t)qh * P + split] = sl;
+    }
+    p.part_o[((int64_t)qh * P + split) * d + e] = so;
   }
 }
 
@@ -271,13 +314,13 @@ bool attn_shape_supported(int L, int Hq, int Hkv, int d) {
 
 // slots: blocks resident at once on the GPU (blocks per SM x SMs).
 int attn_splits(int L, int Hkv, int slots) {
-  const int by_len = (L + 127) / 128;              // at least 16 positions per warp
+  const int by_len = (L + 63) / 64;                // at least 8 positions per warp
   const int by_grid = std::max(1, slots / Hkv);    // one wave of resident blocks
   return std::max(1, std::min(by_len, by_grid));
 }
 
 size_t attn_workspace_floats(int L, int Hq, int Hkv, int d, int slots) {
-  const size_t P = (size_t)attn_splits(L, Hkv, slots) * kAttnWarps;
+  const size_t P = (size_t)attn_splits(L, Hkv, slots);
   return (size_t)Hq * P * (2 + (size_t)d);
 }
 
@@ -300,7 +343,7 @@ cudaError_t attn_decode_launch(const AttnParams& pin, int sms, cudaStream_t s) {
                                    : split_setup<2>(ring, sms, &slots);
   if (err != cudaSuccess) return err;
   const int splits = attn_splits(pin.L, pin.Hkv, slots);
-  const size_t P = (size_t)splits * kAttnWarps;  // partials per query head
+  const size_t P = (size_t)splits;  // partials per query head: one per block
   AttnParams p = pin;
   p.part_m = p.ws;
   p.part_l = p.ws + (size_t)p.Hq * P;
@@ -314,7 +357,7 @@ cudaError_t attn_decode_launch(const AttnParams& pin, int sms, cudaStream_t s) {
     attn_split_kernel<2><<<grid, 32 * kAttnWarps, ring, s>>>(p);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const int P2 = splits * kAttnWarps;
+  const int P2 = splits;
   const size_t comb_smem = ((size_t)P2 + 4 * 64 + kCombThreads / 32) * sizeof(float);
   if (comb_smem > 48 * 1024) {
     err = cudaFuncSetAttribute(attn_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)comb_smem);

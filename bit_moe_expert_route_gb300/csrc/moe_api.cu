@@ -767,7 +767,7 @@ int moe_gdn_scan(const uint16_t* q, const uint16_t* k, const uint16_t* v, const 
 
 size_t moe_decode_attention_workspace_bytes(int L, int n_q_heads, int n_kv_heads, int d) {
   if (!moe::attn_shape_supported(L, n_q_heads, n_kv_heads, d)) return 0;
-  // the split count never exceeds one per 128 positions, whatever the SM count
+  // the split count never exceeds one per 64 positions, whatever the SM count
   return moe::attn_workspace_floats(L, n_q_heads, n_kv_heads, d, 1 << 20) * sizeof(float);
 }
 

@@ -39,9 +39,11 @@ size_t moe_decode_attention_workspace_bytes(int L, int n_q_heads, int n_kv_heads
  * L >= 1; d in {64, 128, 256}; n_q_heads a multiple of n_kv_heads with at most
  * 8 query heads per KV head. Others: MOE_ERR_SHAPE. Two launches: a split
  * kernel (one block per KV head and slice of the cache, all of the head's
- * query heads together; online softmax per warp, at least 16 positions per
- * warp) and a combine kernel (one block per query head and 64 outputs,
- * merging the partials with fixed-order block reductions). fp32 arithmetic.
+ * query heads together; online softmax per warp, at least 8 positions per
+ * warp, the warps' states merged in a fixed order into one partial per block
+ * and query head) and a combine kernel (one block per query head and 64
+ * outputs, merging the partials with fixed-order block reductions). fp32
+ * arithmetic.
  */
 int moe_decode_attention(const uint16_t* q, const uint16_t* K, const uint16_t* V, int L,
                          int n_q_heads, int n_kv_heads, int d, float scale, float* out, void* ws,

@@ -178,8 +178,8 @@ def test_gdn_scan_arguments_are_checked_on_the_host(L):
 def test_decode_attention_arguments_are_checked_on_the_host(L):
     vp = ctypes.c_void_p
     ws_n = L.moe_decode_attention_workspace_bytes(4096, 16, 2, 256)
-    # partials: (m, l, 256 outputs) per query head, 8 per 64-position slice at most
-    assert ws_n == 16 * (4096 // 128) * 8 * (2 + 256) * 4
+    # partials: (m, l, 256 outputs) per query head, one per 64-position slice at most
+    assert ws_n == 16 * (4096 // 64) * (2 + 256) * 4
     for args in ((0, 16, 2, 256), (10, 16, 2, 96), (10, 16, 3, 256), (10, 32, 2, 128)):
         assert L.moe_decode_attention_workspace_bytes(*args) == 0, args  # 16 per KV head > 8
     buf = ctypes.create_string_buffer(1 << 20)

@@ -2,7 +2,8 @@
 
 Inputs: bf16 q [Hq, d] and K, V caches [L, Hkv, d] drawn N(0, 1); the oracle
 sees the same values exactly. The kernel computes the scores and the softmax
-in fp32 and merges per-warp partial softmaxes; the output is a convex
+in fp32 (two positions per warp step, a lone last one masked), merges the
+warps' partial softmaxes inside each block and then the blocks'; the output is a convex
 combination of value rows. Bar: |err| <= 1e-4 * (rms(ref) + |ref|) per element.
 """
 import numpy as np
@@ -40,7 +41,8 @@ def run(L, Hq, Hkv, d, seed, scale=0.0):
 
 
 @pytest.mark.parametrize("L,Hq,Hkv,d", [(1, 16, 2, 256), (37, 16, 2, 256), (1000, 16, 2, 128),
-                                        (300, 4, 4, 64), (4097, 8, 1, 256)])
+                                        (300, 4, 4, 64), (4097, 8, 1, 256), (129, 6, 2, 64),
+                                        (12, 8, 2, 128)])
 def test_matches_oracle(L, Hq, Hkv, d):
     got, ref = run(L, Hq, Hkv, d, seed=L + d)
     close(got, ref)
