@@ -15,7 +15,8 @@
 // v rows and of the running output of every query head. Per position: the
 // group's scores (E-term partial dots, one transpose reduction for all
 // heads), then the online softmax update per head (running max m, running sum
-// l; the output is rescaled only when the max grows). The block's 8 warp
+// l; the output is scaled by exp(m_old - m_new), exactly 1 when the max
+// stays, with no branch). The block's 8 warp
 // states merge (in warp order) into one partial (m, l, unnormalised output)
 // per query head. Combine kernel: per query head and 64 output elements, the
 // blocks' partials merged with weights exp(m_part - max m) and divided by the
@@ -196,18 +197,13 @@ __global__ void __launch_bounds__(32 * kAttnWarps, 1) attn_split_kernel(const At
     for (int h = 0; h < kAttnMaxGroup; ++h) {
       if (h >= G) break;
       const float s0 = sc[0][h], s1 = two ? sc[1][h] : -INFINITY;
-      const float s = fmaxf(s0, s1);
-      if (s > m[h]) {  // the running max moves (the same on every lane): rescale; 0 while m is -inf
-        const float c = __expf(m[h] - s);
-        l[h] *= c;
+      const float mn = fmaxf(m[h], fmaxf(s0, s1));
+      const float c = __expf(m[h] - mn);  // 1 when the max stays; 0 while m is -inf
+      m[h] = mn;
+      const float w0 = __expf(s0 - mn), w1 = __expf(s1 - mn);
+      l[h] = fmaf(l[h], c, w0 + w1);
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[h][e] *= c;
-        m[h] = s;
-      }
-      const float w0 = __expf(s0 - m[h]), w1 = __expf(s1 - m[h]);
-      l[h] += w0 + w1;
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[h][e] = fmaf(w1, v[1][e], fmaf(w0, v[0][e], acc[h][e]));
+      for (int e = 0; e < E; ++e) acc[h][e] = fmaf(w1, v[1][e], fmaf(w0, v[0][e], acc[h][e] * c));
     }
   }
   // the warps' states merge into one partial per (block, query head): each
