@@ -9,16 +9,17 @@
 //
 //   o_h = sum_j softmax_j(scale * q_h . k_{g,j}) v_{g,j},   g = h / (Hq / Hkv)
 //
-// Split kernel: grid (Hkv, splits); 8 warps per block, warp w takes positions
-// j = j0 + w, j0 + w + 8, ... of its slice, two per step. Lane l holds
-// elements l*E .. l*E+E-1 (E = d / 32) of q (pre-scaled), of the current k and
-// v rows and of the running output of every query head. Per position: the
-// group's scores (E-term partial dots, one transpose reduction for all
-// heads), then the online softmax update per head (running max m, running sum
-// l; the output is scaled by exp(m_old - m_new), exactly 1 when the max
-// stays, with no branch). The block's 8 warp
-// states merge (in warp order) into one partial (m, l, unnormalised output)
-// per query head. Combine kernel: per query head and 64 output elements, the
+// Split kernel: grid (Hkv, splits); 8 position sets per block, each walked by
+// one warp per group of 4 query heads (8 or 16 warps): the warps of set w take
+// positions j = j0 + w, j0 + w + 8, ... of the slice, two per step. Lane l
+// holds elements l*E .. l*E+E-1 (E = d / 32) of q (pre-scaled), of the
+// current k and v rows and of the running output of each of its 4 query
+// heads. Per position: the heads' scores (E-term partial dots, one transpose
+// reduction for the 4 heads), then the online softmax update per head
+// (running max m, running sum l; the output is scaled by exp(m_old - m_new),
+// exactly 1 when the max stays, with no branch). Each head's 8 position-set
+// states merge (in set order) into one partial (m, l, unnormalised output)
+// per block and query head. Combine kernel: per query head and 64 output elements, the
 // blocks' partials merged with weights exp(m_part - max m) and divided by the
 // merged sum (block-wide reductions in a fixed order).
 #include <algorithm>
@@ -90,47 +91,42 @@ MOE_DEVINL void load_row_smem(const uint8_t* p, float (&f)[E]) {
   }
 }
 
-// The group's 8 scores from each lane's partial dots x[h]: a transpose
-// reduction (at the step across lane bit b, a lane keeps half of its values
-// and adds the partner's copies of them: 4 + 2 + 1 shuffles), the remaining
-// two steps of a butterfly, then each head's sum broadcast from a lane that
-// holds it: 17 shuffles instead of 8 butterflies of 5. x[h] becomes head h's
-// full sum on every lane.
-MOE_DEVINL void group_scores(float (&x)[kAttnMaxGroup], int lane) {
+// Four heads' scores from each lane's partial dots x[h]: a transpose
+// reduction over lane bits 4 and 3 (2 + 1 shuffles), a butterfly over bits
+// 2..0, then each head's sum broadcast from a lane that holds it.
+MOE_DEVINL void group_scores4(float (&x)[4], int lane) {
   constexpr unsigned kAll = 0xffffffffu;
-  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-  float y[4], z[2];
+  const bool b4 = lane & 16, b3 = lane & 8;
+  float y[2];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {  // heads 4 b4 + i
-    const float send = b4 ? x[i] : x[i + 4], keep = b4 ? x[i + 4] : x[i];
+  for (int i = 0; i < 2; ++i) {  // heads 2 b4 + i
+    const float send = b4 ? x[i] : x[i + 2], keep = b4 ? x[i + 2] : x[i];
     y[i] = keep + __shfl_xor_sync(kAll, send, 16);
   }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {  // heads 4 b4 + 2 b3 + i
-    const float send = b3 ? y[i] : y[i + 2], keep = b3 ? y[i + 2] : y[i];
-    z[i] = keep + __shfl_xor_sync(kAll, send, 8);
-  }
-  float w = (b2 ? z[1] : z[0]) + __shfl_xor_sync(kAll, b2 ? z[0] : z[1], 4);  // head 4 b4 + 2 b3 + b2
+  float w = (b3 ? y[1] : y[0]) + __shfl_xor_sync(kAll, b3 ? y[0] : y[1], 8);  // head 2 b4 + b3
+  w += __shfl_xor_sync(kAll, w, 4);
   w += __shfl_xor_sync(kAll, w, 2);
   w += __shfl_xor_sync(kAll, w, 1);
 #pragma unroll
-  for (int h = 0; h < kAttnMaxGroup; ++h)
-    x[h] = __shfl_sync(kAll, w, ((h >> 2) << 4) | (((h >> 1) & 1) << 3) | ((h & 1) << 2));
+  for (int h = 0; h < 4; ++h) x[h] = __shfl_sync(kAll, w, ((h >> 1) << 4) | ((h & 1) << 3));
 }
 
+constexpr int kHeadsPerWarp = 4;
+
+// Block: 8 position sets x HG head groups of 4 (HG = 1 for up to 4 query
+// heads per KV head, else 2): warp w walks positions j0 + (w % 8) + 8 i for
+// heads 4 (w / 8) .. 4 (w / 8) + 3, with a ring of R = 16 / HG positions.
 template <int E>
-__global__ void __launch_bounds__(32 * kAttnWarps, 1) attn_split_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(32 * kAttnWarps * 2, 1) attn_split_kernel(const AttnParams p) {
   const int g = blockIdx.x, split = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pw = warp % kAttnWarps, hg = warp / kAttnWarps;
+  const int HG = blockDim.x / (32 * kAttnWarps), R = kRing / HG;
   const int G = p.Hq / p.Hkv, d = 32 * E;
   const int per = (p.L + gridDim.y - 1) / gridDim.y;
   const int j0 = split * per, j1 = min(p.L, j0 + per);
-  // K and V rows of the warp's next kRing positions in flight: each lane
-  // copies (cp.async) exactly the E elements of each row it later reads, into
-  // its own slots of a per-warp shared-memory ring, so the ring needs no
-  // synchronisation beyond the lane's own wait_group
   extern __shared__ __align__(16) uint8_t attn_ring[];
-  uint8_t* ring = attn_ring + (size_t)warp * kRing * 2 * (32 * E * 2);
+  uint8_t* ring = attn_ring + (size_t)warp * R * 2 * (32 * E * 2);
   auto slot = [&](int r, int kv) { return smem_u32(ring + ((size_t)(r * 2 + kv) * 32 + lane) * (E * 2)); };
   auto issue = [&](int j, int r) {
     if (j < j1) {
@@ -140,12 +136,12 @@ __global__ void __launch_bounds__(32 * kAttnWarps, 1) attn_split_kernel(const At
     }
     cp_async_commit();
   };
+  for (int r = 0; r < R; ++r) issue(j0 + pw + r * kAttnWarps, r);
+  constexpr int NH = kHeadsPerWarp;
+  float q[NH][E], acc[NH][E], m[NH], l[NH];
 #pragma unroll
-  for (int r = 0; r < kRing; ++r) issue(j0 + warp + r * kAttnWarps, r);
-  // q and the running state (after the first copies are on their way)
-  float q[kAttnMaxGroup][E], acc[kAttnMaxGroup][E], m[kAttnMaxGroup], l[kAttnMaxGroup];
-#pragma unroll
-  for (int h = 0; h < kAttnMaxGroup; ++h) {
+  for (int hh = 0; hh < NH; ++hh) {
+    const int h = hg * NH + hh;
     float f[E];
     if (h < G) {
       load_row<E>(p.q + (int64_t)(g * G + h) * d + lane * E, f);
@@ -155,85 +151,83 @@ __global__ void __launch_bounds__(32 * kAttnWarps, 1) attn_split_kernel(const At
     }
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      q[h][e] = f[e] * p.scale;
-      acc[h][e] = 0.f;
+      q[hh][e] = f[e] * p.scale;
+      acc[hh][e] = 0.f;
     }
-    m[h] = -INFINITY;
-    l[h] = 0.f;
+    m[hh] = -INFINITY;
+    l[hh] = 0.f;
   }
-  // Two positions per step (j and j + 8, ring slots r and r + 1): their
-  // score reductions and softmax updates are independent chains that
-  // overlap. A second position past the slice's end counts as score -inf
-  // with its v taken as zero (its ring slot was never filled).
   int r = 0;
 #pragma unroll 1
-  for (int j = j0 + warp; j < j1; j += 2 * kAttnWarps, r = (r + 2) % kRing) {
+  for (int j = j0 + pw; j < j1; j += 2 * kAttnWarps, r = (r + 2 == R) ? 0 : r + 2) {
     const bool two = j + kAttnWarps < j1;
-    cp_async_wait<kRing - 2>();
-    float k[2][E], v[2][E];
+    if (R == kRing) cp_async_wait<kRing - 2>(); else cp_async_wait<kRing / 2 - 2>();
+    float sc[2][NH];  // (q of the heads past G is zero)
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      load_row_smem<E>(ring + ((size_t)((r + t) * 2 + 0) * 32 + lane) * (E * 2), k[t]);
-      load_row_smem<E>(ring + ((size_t)((r + t) * 2 + 1) * 32 + lane) * (E * 2), v[t]);
-    }
+      float k[E];
+      load_row_smem<E>(ring + ((size_t)((r + t) * 2 + 0) * 32 + lane) * (E * 2), k);
 #pragma unroll
-    for (int t = 0; t < 2; ++t) issue(j + (kRing + t) * kAttnWarps, r + t);  // the slots are read: refill them
+      for (int hh = 0; hh < NH; ++hh) {
+        sc[t][hh] = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) sc[t][hh] = fmaf(q[hh][e], k[e], sc[t][hh]);
+      }
+    }
+    float v[2][E];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) load_row_smem<E>(ring + ((size_t)((r + t) * 2 + 1) * 32 + lane) * (E * 2), v[t]);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) issue(j + (R + t) * kAttnWarps, r + t);  // the slots are read: refill them
     if (!two) {
 #pragma unroll
       for (int e = 0; e < E; ++e) v[1][e] = 0.f;
     }
-    float sc[2][kAttnMaxGroup];  // (q of the heads past G is zero)
+    group_scores4(sc[0], lane);
+    group_scores4(sc[1], lane);
 #pragma unroll
-    for (int t = 0; t < 2; ++t)
-#pragma unroll
-      for (int h = 0; h < kAttnMaxGroup; ++h) {
-        sc[t][h] = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) sc[t][h] = fmaf(q[h][e], k[t][e], sc[t][h]);
-      }
-    group_scores(sc[0], lane);
-    group_scores(sc[1], lane);
-#pragma unroll
-    for (int h = 0; h < kAttnMaxGroup; ++h) {
-      if (h >= G) break;
-      const float s0 = sc[0][h], s1 = two ? sc[1][h] : -INFINITY;
-      const float mn = fmaxf(m[h], fmaxf(s0, s1));
-      const float c = __expf(m[h] - mn);  // 1 when the max stays; 0 while m is -inf
-      m[h] = mn;
+    for (int hh = 0; hh < NH; ++hh) {
+      const float s0 = sc[0][hh], s1 = two ? sc[1][hh] : -INFINITY;
+      const float mn = fmaxf(m[hh], fmaxf(s0, s1));
+      const float c = __expf(m[hh] - mn);  // 1 when the max stays; 0 while m is -inf
+      m[hh] = mn;
       const float w0 = __expf(s0 - mn), w1 = __expf(s1 - mn);
-      l[h] = fmaf(l[h], c, w0 + w1);
+      l[hh] = fmaf(l[hh], c, w0 + w1);
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[h][e] = fmaf(w1, v[1][e], fmaf(w0, v[0][e], acc[h][e] * c));
+      for (int e = 0; e < E; ++e) acc[hh][e] = fmaf(w1, v[1][e], fmaf(w0, v[0][e], acc[hh][e] * c));
     }
   }
   // the warps' states merge into one partial per (block, query head): each
   // warp's (m, l, output) goes to shared memory (the ring, once every copy
-  // has landed), then each (head, element) is merged over the warps in order
+  // has landed), then each (head, element) is merged over the 8 position
+  // sets in order
   cp_async_wait<0>();
   __syncthreads();
-  float* st = reinterpret_cast<float*>(attn_ring);  // [warp][head][2 + d]
+  float* st = reinterpret_cast<float*>(attn_ring);  // [head][position set][2 + d]
 #pragma unroll
-  for (int h = 0; h < kAttnMaxGroup; ++h) {
+  for (int hh = 0; hh < NH; ++hh) {
+    const int h = hg * NH + hh;
     if (h >= G) break;
-    float* w = st + (size_t)(warp * G + h) * (2 + d);
+    float* w = st + (size_t)(h * kAttnWarps + pw) * (2 + d);
     if (lane == 0) {
-      w[0] = m[h];
-      w[1] = l[h];
+      w[0] = m[hh];
+      w[1] = l[hh];
     }
 #pragma unroll
-    for (int e = 0; e < E; ++e) w[2 + lane * E + e] = acc[h][e];
+    for (int e = 0; e < E; ++e) w[2 + lane * E + e] = acc[hh][e];
   }
   __syncthreads();
   const int P = gridDim.y;
   for (int i = threadIdx.x; i < G * d; i += blockDim.x) {
     const int h = i / d, e = i - h * d;
+    const float* sh = st + (size_t)h * kAttnWarps * (2 + d);
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, st[(size_t)(w * G + h) * (2 + d)]);
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, sh[(size_t)w * (2 + d)]);
     float sl = 0.f, so = 0.f;
 #pragma unroll
     for (int w = 0; w < kAttnWarps; ++w) {
-      const float* ws = st + (size_t)(w * G + h) * (2 + d);
+      const float* ws = sh + (size_t)w * (2 + d);
       const float c = ws[0] > -INFINITY ? __expf(ws[0] - M) : 0.f;
       sl = fmaf(ws[1], c, sl);
       so = fmaf(ws[2 + e], c, so);
@@ -321,11 +315,11 @@ size_t attn_workspace_floats(int L, int Hq, int Hkv, int d, int slots) {
 }
 
 template <int E>
-cudaError_t split_setup(size_t ring, int sms, int* slots) {
+cudaError_t split_setup(size_t ring, int threads, int sms, int* slots) {
   cudaError_t err = cudaFuncSetAttribute(attn_split_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
   if (err != cudaSuccess) return err;
   int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_split_kernel<E>, 32 * kAttnWarps, ring);
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_split_kernel<E>, threads, ring);
   *slots = std::max(1, per_sm) * sms;
   return err;
 }
@@ -333,10 +327,12 @@ cudaError_t split_setup(size_t ring, int sms, int* slots) {
 cudaError_t attn_decode_launch(const AttnParams& pin, int sms, cudaStream_t s) {
   if (!attn_shape_supported(pin.L, pin.Hq, pin.Hkv, pin.d) || !pin.ws) return cudaErrorInvalidValue;
   const size_t ring = (size_t)kAttnWarps * kRing * 2 * pin.d * 2;  // bf16 K and V rows per warp slot
+  const int HG = pin.Hq / pin.Hkv > kHeadsPerWarp ? 2 : 1;         // head groups of 4 per block
+  const int threads = 32 * kAttnWarps * HG;
   int slots = sms;
-  cudaError_t err = pin.d == 256 ? split_setup<8>(ring, sms, &slots)
-                    : pin.d == 128 ? split_setup<4>(ring, sms, &slots)
-                                   : split_setup<2>(ring, sms, &slots);
+  cudaError_t err = pin.d == 256 ? split_setup<8>(ring, threads, sms, &slots)
+                    : pin.d == 128 ? split_setup<4>(ring, threads, sms, &slots)
+                                   : split_setup<2>(ring, threads, sms, &slots);
   if (err != cudaSuccess) return err;
   const int splits = attn_splits(pin.L, pin.Hkv, slots);
   const size_t P = (size_t)splits;  // partials per query head: one per block
@@ -346,11 +342,11 @@ cudaError_t attn_decode_launch(const AttnParams& pin, int sms, cudaStream_t s) {
   p.part_o = p.ws + 2 * (size_t)p.Hq * P;
   const dim3 grid(p.Hkv, splits);
   if (p.d == 256)
-    attn_split_kernel<8><<<grid, 32 * kAttnWarps, ring, s>>>(p);
+    attn_split_kernel<8><<<grid, threads, ring, s>>>(p);
   else if (p.d == 128)
-    attn_split_kernel<4><<<grid, 32 * kAttnWarps, ring, s>>>(p);
+    attn_split_kernel<4><<<grid, threads, ring, s>>>(p);
   else
-    attn_split_kernel<2><<<grid, 32 * kAttnWarps, ring, s>>>(p);
+    attn_split_kernel<2><<<grid, threads, ring, s>>>(p);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const int P2 = splits;
