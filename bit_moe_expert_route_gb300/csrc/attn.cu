@@ -12,12 +12,14 @@
 // Split kernel: grid (Hkv, splits); 8 position sets per block, each walked by
 // one warp per group of 4 query heads (8 or 16 warps): the warps of set w take
 // positions j = j0 + w, j0 + w + 8, ... of the slice, two per step. Lane l
-// holds elements l*E .. l*E+E-1 (E = d / 32) of q (pre-scaled), of the
+// holds elements l*E .. l*E+E-1 (E = d / 32) of q (its bf16 pairs), of the
 // current k and v rows and of the running output of each of its 4 query
-// heads. Per position: the heads' scores (E-term partial dots, one transpose
-// reduction for the 4 heads), then the online softmax update per head
-// (running max m, running sum l; the output is scaled by exp(m_old - m_new),
-// exactly 1 when the max stays, with no branch). Each head's 8 position-set
+// heads. Per position: the heads' scores (E-term partial dots of bf16 pairs
+// in mixed-precision FMAs, exact products; one transpose reduction for the 4
+// heads; then the scale), then the online softmax update per head (reference
+// max m, running sum l: m moves, and the output and l are rescaled by
+// exp(m_old - m_new), only when a score exceeds m by more than 8, so the
+// weights exp(s - m) stay below e^8 and rescales are rare). Each head's 8 position-set
 // states merge (in set order) into one partial (m, l, unnormalised output)
 // per block and query head. Combine kernel: per query head and 64 output elements, the
 // blocks' partials merged with weights exp(m_part - max m) and divided by the
@@ -26,6 +28,7 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "gemv_dot.cuh"
 #include "kernels.h"
 
 namespace moe {
@@ -112,6 +115,9 @@ MOE_DEVINL void group_scores4(float (&x)[4], int lane) {
 }
 
 constexpr int kHeadsPerWarp = 4;
+// a head's reference max m moves only when a score exceeds it by more than
+// this (natural-log units): the weights exp(s - m) stay below e^8
+constexpr float kLazy = 8.f;
 
 // Block: 8 position sets x HG head groups of 4 (HG = 1 for up to 4 query
 // heads per KV head, else 2): warp w walks positions j0 + (w % 8) + 8 i for
@@ -138,22 +144,17 @@ __global__ void __launch_bounds__(32 * kAttnWarps * 2, 1) attn_split_kernel(cons
   };
   for (int r = 0; r < R; ++r) issue(j0 + pw + r * kAttnWarps, r);
   constexpr int NH = kHeadsPerWarp;
-  float q[NH][E], acc[NH][E], m[NH], l[NH];
+  // q as the lane's bf16 pairs (exact: the scale multiplies the reduced score)
+  uint32_t qp[NH][E / 2];
+  float acc[NH][E], m[NH], l[NH];
 #pragma unroll
   for (int hh = 0; hh < NH; ++hh) {
     const int h = hg * NH + hh;
-    float f[E];
-    if (h < G) {
-      load_row<E>(p.q + (int64_t)(g * G + h) * d + lane * E, f);
-    } else {
 #pragma unroll
-      for (int e = 0; e < E; ++e) f[e] = 0.f;
-    }
+    for (int i = 0; i < E / 2; ++i)
+      qp[hh][i] = h < G ? __ldg(reinterpret_cast<const uint32_t*>(p.q + (int64_t)(g * G + h) * d + lane * E) + i) : 0u;
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      q[hh][e] = f[e] * p.scale;
-      acc[hh][e] = 0.f;
-    }
+    for (int e = 0; e < E; ++e) acc[hh][e] = 0.f;
     m[hh] = -INFINITY;
     l[hh] = 0.f;
   }
@@ -165,13 +166,16 @@ __global__ void __launch_bounds__(32 * kAttnWarps * 2, 1) attn_split_kernel(cons
     float sc[2][NH];  // (q of the heads past G is zero)
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      float k[E];
-      load_row_smem<E>(ring + ((size_t)((r + t) * 2 + 0) * 32 + lane) * (E * 2), k);
+      uint32_t kw[E / 2];
+      const uint8_t* kr = ring + ((size_t)((r + t) * 2 + 0) * 32 + lane) * (E * 2);
+#pragma unroll
+      for (int i = 0; i < E / 2; ++i) kw[i] = reinterpret_cast<const uint32_t*>(kr)[i];
 #pragma unroll
       for (int hh = 0; hh < NH; ++hh) {
-        sc[t][hh] = 0.f;
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-        for (int e = 0; e < E; ++e) sc[t][hh] = fmaf(q[hh][e], k[e], sc[t][hh]);
+        for (int i = 0; i < E / 2; ++i) fma_pair<true>(a0, a1, qp[hh][i], kw[i]);
+        sc[t][hh] = a0 + a1;
       }
     }
     float v[2][E];
@@ -186,15 +190,24 @@ __global__ void __launch_bounds__(32 * kAttnWarps * 2, 1) attn_split_kernel(cons
     group_scores4(sc[0], lane);
     group_scores4(sc[1], lane);
 #pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int hh = 0; hh < NH; ++hh) sc[t][hh] *= p.scale;
+#pragma unroll
     for (int hh = 0; hh < NH; ++hh) {
       const float s0 = sc[0][hh], s1 = two ? sc[1][hh] : -INFINITY;
-      const float mn = fmaxf(m[hh], fmaxf(s0, s1));
-      const float c = __expf(m[hh] - mn);  // 1 when the max stays; 0 while m is -inf
-      m[hh] = mn;
-      const float w0 = __expf(s0 - mn), w1 = __expf(s1 - mn);
-      l[hh] = fmaf(l[hh], c, w0 + w1);
+      const float smax = fmaxf(s0, s1);
+      if (smax > m[hh] + kLazy) {  // same on every lane; rare once the max has settled
+        const float c = __expf(m[hh] - smax);  // 0 while m is -inf
+        l[hh] *= c;
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[hh][e] = fmaf(w1, v[1][e], fmaf(w0, v[0][e], acc[hh][e] * c));
+        for (int e = 0; e < E; ++e) acc[hh][e] *= c;
+        m[hh] = smax;
+      }
+      const float w0 = __expf(s0 - m[hh]), w1 = __expf(s1 - m[hh]);
+      l[hh] += w0 + w1;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[hh][e] = fmaf(w1, v[1][e], fmaf(w0, v[0][e], acc[hh][e]));
     }
   }
   // the warps' states merge into one partial per (block, query head): each

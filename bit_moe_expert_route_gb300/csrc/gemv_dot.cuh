@@ -1,4 +1,5 @@
-// Packed 4-bit dot products on the vector ALUs, shared by the decode kernels.
+// Packed 4-bit dot products on the vector ALUs, shared by the decode kernels
+// (fma_pair also serves the decode attention's bf16 q.k dots).
 //
 // A code q becomes the 16-bit float f = 1 + q/16 exactly (bf16 bits
 // 0x3F80 | q << 3, f16 bits 0x3C00 | q << 6), two codes per shift-and-mask,
