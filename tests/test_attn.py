@@ -55,3 +55,24 @@ def test_long_context_and_explicit_scale():
     close(got, ref)
     got, ref = run(2048, 16, 2, 128, seed=4, scale=0.25)
     close(got, ref)
+
+
+def test_late_large_scores_move_the_max():
+    """Keys planted late in the cache give query head 0 (and its group) scores
+    far above the rest, twice, so the running max moves mid-sequence and the
+    partial outputs are rescaled; the result is still the oracle's softmax."""
+    from bit_moe_expert_route_gb300 import ops
+    L, Hq, Hkv, d = 3001, 16, 2, 128
+    rng = np.random.default_rng(11)
+    q = bf16_round(rng.standard_normal((Hq, d)))
+    K = bf16_round(rng.standard_normal((L, Hkv, d)))
+    V = bf16_round(rng.standard_normal((L, Hkv, d)))
+    u = q[0] / np.linalg.norm(q[0])
+    for j, c in ((1500, 60.0), (2900, 120.0), (2901, 121.0)):
+        K[j, 0] = bf16_round(c * u)  # head 0's score about c * |q0| / sqrt(d)
+
+    def dev(a):
+        return torch.from_numpy(a).cuda().to(torch.bfloat16)
+    got = ops.decode_attention(dev(q), dev(K), dev(V))
+    torch.cuda.synchronize()
+    close(got.cpu().numpy(), decode_attention(q, K, V, None))
