@@ -254,13 +254,18 @@ __global__ void __launch_bounds__(32 * kAttnWarps * 2, 1) attn_split_kernel(cons
   }
 }
 
-// Merge of the partials: one block per (query head, 64 output elements).
+// Merge of the partials: one block per (query head, 32 output elements).
 // The merged max over the P partials and the weights w_i = exp(m_i - max)
 // come from block-wide reductions in a fixed order (each thread's share in
 // index order, then the warps' butterfly, then warps in order), so the result
 // does not depend on timing; then each output element is summed over the
-// partials by 4 threads (quarters of the index range, added in order).
+// partials by 8 threads, one per warp (eighths of the index range, added in
+// order). A thread loads its first 16 partial outputs before the reductions
+// (they do not depend on the weights), so those loads overlap them.
 constexpr int kCombThreads = 256;
+constexpr int kCombCols = 32;                          // output elements per block
+constexpr int kCombSlices = kCombThreads / kCombCols;  // partial ranges per element
+constexpr int kCombAhead = 16;                         // partial outputs loaded early
 MOE_DEVINL float block_reduce(float v, bool is_max, float* red) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
@@ -277,10 +282,17 @@ MOE_DEVINL float block_reduce(float v, bool is_max, float* red) {
 }
 
 __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const AttnParams p, int P) {
-  extern __shared__ float s_w[];  // [P] merge weights, then [4][64] quarter sums, then [8] reduction slots
-  float* quart = s_w + P;
-  float* red = quart + 4 * 64;
-  const int qh = blockIdx.x, e0 = blockIdx.y * 64, d = p.d;
+  extern __shared__ float s_w[];  // [P] merge weights, [8][32] slice sums, [8] reduction slots
+  float* slice = s_w + P;
+  float* red = slice + kCombSlices * kCombCols;
+  const int qh = blockIdx.x, e0 = blockIdx.y * kCombCols, d = p.d;
+  const int t = threadIdx.x % kCombCols, q = threadIdx.x / kCombCols;  // element, slice of the partials
+  const int i0 = P * q / kCombSlices, i1 = P * (q + 1) / kCombSlices;
+  const bool col = e0 + t < d;
+  const float* po = p.part_o + ((int64_t)qh * P) * d + e0 + t;
+  float ahead[kCombAhead];
+#pragma unroll
+  for (int k = 0; k < kCombAhead; ++k) ahead[k] = col && i0 + k < i1 ? po[(int64_t)(i0 + k) * d] : 0.f;
   const float* pm = p.part_m + (int64_t)qh * P;
   const float* pl = p.part_l + (int64_t)qh * P;
   float m = -INFINITY;
@@ -294,18 +306,20 @@ __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const AttnPa
     l = fmaf(pl[i], w, l);
   }
   const float inv = 1.f / block_reduce(l, false, red);  // also orders the s_w writes before the reads
-  const int t = threadIdx.x & 63, q = threadIdx.x >> 6;  // element, quarter of the partials
-  const int i0 = P * q / 4, i1 = P * (q + 1) / 4;
   float o = 0.f;
-  if (e0 + t < d) {
-    const float* po = p.part_o + ((int64_t)qh * P) * d + e0 + t;
-#pragma unroll 4
-    for (int i = i0; i < i1; ++i) o = fmaf(po[(int64_t)i * d], s_w[i], o);
-  }
-  quart[q * 64 + t] = o;
+#pragma unroll
+  for (int k = 0; k < kCombAhead; ++k)
+    if (i0 + k < i1) o = fmaf(ahead[k], s_w[i0 + k], o);
+  if (col)
+    for (int i = i0 + kCombAhead; i < i1; ++i) o = fmaf(po[(int64_t)i * d], s_w[i], o);
+  slice[q * kCombCols + t] = o;
   __syncthreads();
-  if (threadIdx.x < 64 && e0 + t < d)
-    p.out[(int64_t)qh * d + e0 + t] = (((quart[t] + quart[64 + t]) + quart[128 + t]) + quart[192 + t]) * inv;
+  if (threadIdx.x < kCombCols && col) {
+    float r = slice[t];
+#pragma unroll
+    for (int k = 1; k < kCombSlices; ++k) r += slice[k * kCombCols + t];
+    p.out[(int64_t)qh * d + e0 + t] = r * inv;
+  }
 }
 
 }  // namespace
@@ -363,12 +377,12 @@ cudaError_t attn_decode_launch(const AttnParams& pin, int sms, cudaStream_t s) {
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const int P2 = splits;
-  const size_t comb_smem = ((size_t)P2 + 4 * 64 + kCombThreads / 32) * sizeof(float);
+  const size_t comb_smem = ((size_t)P2 + kCombSlices * kCombCols + kCombThreads / 32) * sizeof(float);
   if (comb_smem > 48 * 1024) {
     err = cudaFuncSetAttribute(attn_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)comb_smem);
     if (err != cudaSuccess) return err;
   }
-  attn_combine_kernel<<<dim3(p.Hq, (p.d + 63) / 64), kCombThreads, comb_smem, s>>>(p, P2);
+  attn_combine_kernel<<<dim3(p.Hq, (p.d + kCombCols - 1) / kCombCols), kCombThreads, comb_smem, s>>>(p, P2);
   return cudaGetLastError();
 }
 

@@ -41,7 +41,7 @@ size_t moe_decode_attention_workspace_bytes(int L, int n_q_heads, int n_kv_heads
  * kernel (one block per KV head and slice of the cache, all of the head's
  * query heads together; online softmax per warp, at least 8 positions per
  * warp, the warps' states merged in a fixed order into one partial per block
- * and query head) and a combine kernel (one block per query head and 64
+ * and query head) and a combine kernel (one block per query head and 32
  * outputs, merging the partials with fixed-order block reductions). fp32
  * arithmetic.
  */
