@@ -49,12 +49,12 @@ def parse():
     ap.add_argument("--no-gdn", action="store_true", help="skip the Gated DeltaNet scan lines")
     ap.add_argument("--no-attn", action="store_true", help="skip the decode-attention lines")
     ap.add_argument("--profile", choices=["decode", "prefill", "prefill-det", "prefill-fused",
-                                          "decode-batch", "attn"],
+                                          "decode-batch", "attn", "gdn"],
                     help="no measurement: run one layer repeatedly (decode: 20 + 200 calls; prefill: "
                          "3 forwards at --profile-T tokens; prefill-det / prefill-fused: the same "
                          "with MOE_FWD_DETERMINISTIC / MOE_FWD_FUSED; decode-batch: 8 calls at each "
                          "of T = 2, 4, 8; attn: 4 decode-attention calls over 32768 cached "
-                         "positions) for a profiler to attach to")
+                         "positions; gdn: 4 Gated DeltaNet scans over 4096 tokens) for a profiler to attach to")
     ap.add_argument("--profile-T", type=int, default=4096)
     return ap.parse_args()
 
@@ -745,6 +745,21 @@ def profile_run(args):
         V = torch.randn(L, Hkv, d, device="cuda", generator=gen).to(torch.bfloat16)
         for _ in range(4):
             ops.decode_attention(q, K, V)
+    elif args.profile == "gdn":
+        Hk, Hv, dk, dv = (GDN_SHAPE[n] for n in ("Hk", "Hv", "dk", "dv"))
+        gen = torch.Generator(device="cuda").manual_seed(0)
+        T = 4096
+
+        def unit(*shp):
+            a = torch.randn(*shp, device="cuda", generator=gen)
+            return (a / a.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+        q, k = unit(T, Hk, dk), unit(T, Hk, dk)
+        v = torch.randn(T, Hv, dv, device="cuda", generator=gen).to(torch.bfloat16)
+        al = 0.8 + 0.2 * torch.rand(T, Hv, device="cuda", generator=gen)
+        be = torch.rand(T, Hv, device="cuda", generator=gen)
+        S = 0.1 * torch.randn(Hv, dv, dk, device="cuda", generator=gen)
+        for _ in range(4):
+            ops.gdn_scan(q, k, v, al, be, S)
     elif args.profile == "decode-batch":
         for T in (2, 4, 8):
             dec = ops.DecodeBatch(dl, T)

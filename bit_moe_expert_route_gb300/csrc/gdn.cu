@@ -225,28 +225,38 @@ __global__ void __launch_bounds__(32 * kGdnWarps) gdn_scan_kernel(const GdnParam
       load_row_f32<PS, R>(cf.k[0], sl, kc);
       pk = group_sum<L>(lane_dot<PS, R>(s, kc));
     }
-#pragma unroll 1
-    for (int j = 0; j < n; ++j) {
+    // one token: k_t in kcur, k_{t+1} loaded into knext (the two arrays swap
+    // roles from token to token, so no copy between them)
+    auto token = [&](int j, const float (&kcur)[DKL], float (&knext)[DKL]) {
       const int t = t0 + j;
-      float q[DKL], kn[DKL];
+      float q[DKL];
       load_row_f32<PS, R>(cf.q[j], sl, q);
       if (t + 1 < p.T) {
-        load_row_f32<PS, R>(cf.k[j + 1], sl, kn);
+        load_row_f32<PS, R>(cf.k[j + 1], sl, knext);
       } else {
 #pragma unroll
-        for (int i = 0; i < DKL; ++i) kn[i] = 0.f;
+        for (int i = 0; i < DKL; ++i) knext[i] = 0.f;
       }
       const float v = __uint_as_float((uint32_t)ch.v[j][rr] << 16);
       const float a = ch.a[j], b = ch.b[j];
       const float u = b * (v - a * pk);  // beta (v - alpha s.k)
 #pragma unroll
-      for (int i = 0; i < DKL; ++i) s[i] = fmaf(a, s[i], u * kc[i]);  // alpha s + u k
-      float po = lane_dot<PS, R>(s, q), pn = lane_dot<PS, R>(s, kn);
+      for (int i = 0; i < DKL; ++i) s[i] = fmaf(a, s[i], u * kcur[i]);  // alpha s + u k
+      float po = lane_dot<PS, R>(s, q), pn = lane_dot<PS, R>(s, knext);
       group_sum2<L>(po, pn);  // o_t[row] = s . q_t and the next token's s . k
       if (sl == 0) p.out[((int64_t)t * p.Hv + h) * p.dv + row] = po;
       pk = pn;
+    };
+    float kn[DKL];
+#pragma unroll 1
+    for (int j = 0; j < n; j += 2) {
+      token(j, kc, kn);
+      if (j + 1 < n) {
+        token(j + 1, kn, kc);
+      } else {  // an odd last token: the next k goes back to kc
 #pragma unroll
-      for (int i = 0; i < DKL; ++i) kc[i] = kn[i];
+        for (int i = 0; i < DKL; ++i) kc[i] = kn[i];
+      }
     }
     __syncthreads();  // every warp is done with this buffer before it is refilled
   }
