@@ -97,6 +97,7 @@ struct Cfg {
                     kRowInfoBytes - kSA * kAStage) /
                        kBBytes;
   static constexpr int kSB = kSB0 > 8 ? 8 : kSB0;
+  static constexpr int kSD = kSA > kSB ? kSA : kSB;  // k-block completion barriers
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kSA * kAStage;
   static constexpr int kOffQ = kOffB + kSB * kBBytes;
@@ -227,10 +228,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
   uint64_t* q_full = bars;
   uint64_t* q_empty = q_full + kSQ;
   uint64_t* a_full = q_empty + kSQ;
-  uint64_t* a_empty = a_full + C::kSA;
-  uint64_t* b_full = a_empty + C::kSA;
-  uint64_t* b_empty = b_full + C::kSB;
-  uint64_t* acc_full = b_empty + C::kSB;   // [2]
+  uint64_t* b_full = a_full + C::kSA;
+  // done[i % kSD] completes when the MMAs of k-block i have read their A and
+  // B stages: one commit per k-block frees both (the A producer at k-block i
+  // waits for k-block i - kSA, the B producer for i - kSB; the MMA cannot run
+  // kSD k-blocks past either, so no barrier is two phases ahead of a waiter)
+  uint64_t* done = b_full + C::kSB;
+  uint64_t* acc_full = done + C::kSD;      // [2]
   uint64_t* acc_empty = acc_full + 2;      // [2]
   uint64_t* drain = acc_empty + 2;         // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -248,12 +252,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
     }
     for (int i = 0; i < C::kSA; ++i) {
       mbar_init(&a_full[i], 8);     // dequant warps
-      mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < C::kSB; ++i) {
       mbar_init(&b_full[i], b_by_tma ? 1 : 2);  // TMA, or the gather warps
-      mbar_init(&b_empty[i], 1);
     }
+    for (int i = 0; i < C::kSD; ++i) mbar_init(&done[i], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 4);  // epilogue warps
@@ -311,7 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
           }
           if (b_by_tma) {
             const int sb = it % C::kSB;
-            if (!mbar_wait(&b_empty[sb], ((it / C::kSB) & 1) ^ 1, abort_flag, g.status, 10)) {
+            if (it >= (uint32_t)C::kSB &&
+                !mbar_wait(&done[(it - C::kSB) % C::kSD], ((it - C::kSB) / C::kSD) & 1, abort_flag, g.status, 10)) {
               alive = false;
               ++it;
               break;
@@ -372,8 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
                             smem_desc_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0);
             }
           }
-          tc_commit(&a_empty[s]);
-          tc_commit(&b_empty[sb]);
+          tc_commit(&done[it % C::kSD]);
         }
         if (!alive) break;
         tc_commit(&acc_full[buf]);
@@ -408,7 +411,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
       for (int j = 0; j < NMAT; ++j)
         qw[j] = *reinterpret_cast<const uint4*>(smem + C::kOffQ + (sq * NMAT + j) * C::kQStage + qoff);
       const int sa = it % C::kSA;
-      if (!mbar_wait(&a_empty[sa], ((it / C::kSA) & 1) ^ 1, abort_flag, g.status, 7)) return false;
+      if (it >= (uint32_t)C::kSA &&
+          !mbar_wait(&done[(it - C::kSA) % C::kSD], ((it - C::kSA) / C::kSD) & 1, abort_flag, g.status, 7))
+        return false;
 #pragma unroll
       for (int j = 0; j < NMAT; ++j) {
         const uint32_t words[4] = {qw[j].x, qw[j].y, qw[j].z, qw[j].w};
@@ -557,7 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
       }
       for (int kb = 0; kb < KB; ++kb, ++it) {
         const int sb = it % C::kSB;
-        if (!mbar_wait(&b_empty[sb], ((it / C::kSB) & 1) ^ 1, abort_flag, g.status, 8)) {
+        if (it >= (uint32_t)C::kSB &&
+            !mbar_wait(&done[(it - C::kSB) % C::kSD], ((it - C::kSB) / C::kSD) & 1, abort_flag, g.status, 8)) {
           alive = false;
           break;
         }
