@@ -319,7 +319,8 @@ def run_gdn(args, peaks):
     """moe_gdn_scan on seeded synthetic inputs (unit-norm bf16 q and k, N(0,1) bf16 v,
     alpha in [0.8, 1), beta in [0, 1), fp32 state): prefill, one scan over T = 4096
     tokens; decode, one token through each of 30 layers (distinct states) captured in one
-    CUDA graph. L2 flushed before every timed replay."""
+    CUDA graph, each launch reading its layer's state before waiting for the previous
+    layer (MOE_GDN_STATE_EARLY). L2 flushed before every timed replay."""
     import torch
     from bit_moe_expert_route_gb300 import ops
     Hk, Hv, dk, dv = (GDN_SHAPE[n] for n in ("Hk", "Hv", "dk", "dv"))
@@ -352,7 +353,7 @@ def run_gdn(args, peaks):
 
     def step():
         for lq, lk, lv, la, lb, lS, lo in layers:
-            ops.gdn_scan(lq, lk, lv, la, lb, lS, out=lo)
+            ops.gdn_scan(lq, lk, lv, la, lb, lS, out=lo, state_early=True)
     gd = gpu_graph(step, stream)
     for _ in range(3):
         gd.replay()

@@ -192,18 +192,24 @@ __global__ void __launch_bounds__(32 * kGdnWarps) gdn_scan_kernel(const GdnParam
   const int row0 = (blockIdx.x % rows_per_head) * RB;
   const int rr = warp * R + sub, row = row0 + rr;  // this lane's row
   const int hk = h / (p.Hv / p.Hk);
-  // launched as a programmatic dependent: wait for the previous kernel's
-  // memory before the first global access, then let the next one launch
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" :::);
   float* srow = p.state + ((int64_t)h * p.dv + row) * p.dk;
   float s[DKL];
+  auto load_state = [&]() {
 #pragma unroll
-  for (int i = 0; i < DKL; i += 2) {  // 8-byte pieces: the state need only be 8-byte aligned
-    const float2 v = *reinterpret_cast<const float2*>(srow + lane_elem<PS, L>(sl, i));
-    s[i] = v.x;
-    s[i + 1] = v.y;
-  }
+    for (int i = 0; i < DKL; i += 2) {  // 8-byte pieces: the state need only be 8-byte aligned
+      const float2 v = *reinterpret_cast<const float2*>(srow + lane_elem<PS, L>(sl, i));
+      s[i] = v.x;
+      s[i + 1] = v.y;
+    }
+  };
+  // launched as a programmatic dependent: wait for the previous kernel's
+  // memory before the first global access (the state may come first when the
+  // caller states that the previous launch does not write it), then let the
+  // next one launch
+  if (p.state_early) load_state();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" :::);
+  if (!p.state_early) load_state();
   const int n_chunks = (p.T + kGdnChunk - 1) / kGdnChunk;
   float kc[DKL], pk = 0.f;
 #pragma unroll 1

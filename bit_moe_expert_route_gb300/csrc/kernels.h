@@ -170,6 +170,7 @@ struct GdnParams {
   int T, Hk, Hv, dk, dv;
   float* state;
   float* out;
+  int state_early;  // the state may be read before waiting for the previous launch
 };
 bool gdn_shape_supported(int dk, int dv, int Hk, int Hv);
 cudaError_t gdn_scan_launch(const GdnParams& p, cudaStream_t s);

@@ -737,6 +737,14 @@ int moe_get_device_status(const void* ws, void* stream, int32_t* device_status) 
 int moe_gdn_scan(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* alpha,
                  const float* beta, int T, int n_k_heads, int n_v_heads, int d_k, int d_v,
                  float* state, float* out, void* stream) {
+  return moe_gdn_scan_ex(q, k, v, alpha, beta, T, n_k_heads, n_v_heads, d_k, d_v, state, out, 0,
+                         stream);
+}
+
+int moe_gdn_scan_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* alpha,
+                    const float* beta, int T, int n_k_heads, int n_v_heads, int d_k, int d_v,
+                    float* state, float* out, int flags, void* stream) {
+  if ((flags & ~MOE_GDN_STATE_EARLY) != 0) return MOE_ERR_SHAPE;
   if (T < 0 || !moe::gdn_shape_supported(d_k, d_v, n_k_heads, n_v_heads)) return MOE_ERR_SHAPE;
   if ((int64_t)T * n_v_heads * d_v >= (int64_t)1 << 40) return MOE_ERR_SHAPE;
   if (!state) return MOE_ERR_NULL;
@@ -762,6 +770,7 @@ int moe_gdn_scan(const uint16_t* q, const uint16_t* k, const uint16_t* v, const 
   p.dv = d_v;
   p.state = state;
   p.out = out;
+  p.state_early = (flags & MOE_GDN_STATE_EARLY) != 0;
   return cuda_status(moe::gdn_scan_launch(p, static_cast<cudaStream_t>(stream)));
 }
 

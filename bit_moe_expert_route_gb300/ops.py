@@ -96,6 +96,7 @@ def lib():
         L.moe_forward_views_ex.argtypes = [vp, sz, vp, i32, i32, vp]
         L.moe_forward_ex.argtypes = [vp, vp, vp, i32, i32, vp, vp, sz, vp]
         L.moe_gdn_scan.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
+        L.moe_gdn_scan_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp]
         L.moe_decode_attention_workspace_bytes.restype = sz
         L.moe_decode_attention_workspace_bytes.argtypes = [i32, i32, i32, i32]
         L.moe_decode_attention.argtypes = [vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, vp, vp,
@@ -263,19 +264,24 @@ def grouped_gemm_w4a16(A, W, n_groups, N, block_map, num_tiles, max_tiles_, bloc
     return C, ws
 
 
+GDN_STATE_EARLY = 1
+
+
 def gdn_scan(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Tensor,
              beta: torch.Tensor, state: torch.Tensor, out: torch.Tensor | None = None,
-             stream=None) -> torch.Tensor:
-    """moe_gdn_scan (include/gdn.h): q, k bf16 [T, Hk, dk]; v bf16 [T, Hv, dv]; alpha,
+             stream=None, state_early: bool = False) -> torch.Tensor:
+    """moe_gdn_scan_ex (include/gdn.h): q, k bf16 [T, Hk, dk]; v bf16 [T, Hv, dv]; alpha,
     beta fp32 [T, Hv]; state fp32 [Hv, dv, dk], advanced in place over the T tokens.
-    Returns out fp32 [T, Hv, dv]."""
+    state_early (MOE_GDN_STATE_EARLY): the previous launch on the stream does not write
+    this state, so it is read before waiting for that launch. Returns out fp32 [T, Hv, dv]."""
     T, Hk, dk = k.shape
     Hv, dv = v.shape[1], v.shape[2]
     if out is None:
         out = torch.empty(T, Hv, dv, dtype=torch.float32, device=state.device)
-    rc = lib().moe_gdn_scan(_p(q), _p(k), _p(v), _p(alpha), _p(beta), T, Hk, Hv, dk, dv,
-                            _p(state), _p(out), _stream(stream))
-    _check("moe_gdn_scan", rc)
+    rc = lib().moe_gdn_scan_ex(_p(q), _p(k), _p(v), _p(alpha), _p(beta), T, Hk, Hv, dk, dv,
+                               _p(state), _p(out), GDN_STATE_EARLY if state_early else 0,
+                               _stream(stream))
+    _check("moe_gdn_scan_ex", rc)
     return out
 
 

@@ -39,14 +39,34 @@ extern "C" {
  * d_k in {64, 128}; d_v a multiple of 8; n_v_heads a multiple of n_k_heads;
  * T >= 0 (T == 0 leaves the state unchanged and launches nothing). Others:
  * MOE_ERR_SHAPE. NULL pointers: MOE_ERR_NULL; misaligned ones: MOE_ERR_ALIGN.
- * One launch of one 8-warp block per 8 state rows; every warp carries its row
- * through all T tokens in registers (state traffic: one read and one write of
- * the state per call), the block staging 32 tokens of inputs at a time in
- * shared memory. fp32 arithmetic throughout.
+ * One launch of one 8-warp block per 8 R state rows (R rows per warp: 4 for
+ * T >= 64 when d_v is a multiple of 32, else 2 or 1; 1 for T < 64); every warp
+ * carries its rows through all T tokens in registers (state traffic: one read
+ * and one write of the state per call), the block staging 32 tokens of inputs
+ * at a time in shared memory. fp32 arithmetic throughout. The launch is a
+ * programmatic dependent of the previous one on the stream: it reads nothing
+ * before that launch's memory is visible.
  */
 int moe_gdn_scan(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* alpha,
                  const float* beta, int T, int n_k_heads, int n_v_heads, int d_k, int d_v,
                  float* state, float* out, void* stream);
+
+/* flags of moe_gdn_scan_ex */
+#define MOE_GDN_STATE_EARLY 1 /* the launch just before this one on the stream does not write
+                                 `state`: the state is read before waiting for that launch */
+
+/*
+ * moe_gdn_scan_ex: moe_gdn_scan with flags (0 gives moe_gdn_scan). With
+ * MOE_GDN_STATE_EARLY each block loads its state rows before it waits for the
+ * previous launch on the stream (q, k, v, alpha, beta and out are still only
+ * touched after the wait), so a chain of layers with distinct states overlaps
+ * each layer's state read with the layer before it. The caller guarantees
+ * that the previous launch does not write `state`; otherwise the result is
+ * undefined. Unknown flag bits: MOE_ERR_SHAPE.
+ */
+int moe_gdn_scan_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* alpha,
+                    const float* beta, int T, int n_k_heads, int n_v_heads, int d_k, int d_v,
+                    float* state, float* out, int flags, void* stream);
 
 #ifdef __cplusplus
 }

@@ -174,6 +174,15 @@ def test_gdn_scan_arguments_are_checked_on_the_host(L):
     assert call(dk=64, st=a + 8) != -2  # an 8-byte aligned state suffices at d_k 64
     assert call(T=0, q=None, k=None, v=None, al=None, be=None, out=None) == 0  # no work
 
+    def call_ex(flags, **kw):
+        c = dict(ok, **kw)
+        return L.moe_gdn_scan_ex(vp(c["q"]), vp(c["k"]), vp(c["v"]), vp(c["al"]), vp(c["be"]),
+                                 c["T"], c["Hk"], c["Hv"], c["dk"], c["dv"], vp(c["st"]),
+                                 vp(c["out"]), flags, None)
+    assert call_ex(2) == -3 and call_ex(-1) == -3  # unknown flag bits
+    assert call_ex(1, T=-1) == -3 and call_ex(1, st=None) == -1 and call_ex(1, st=a + 8) == -2
+    assert call_ex(1, T=0, q=None, k=None, v=None, al=None, be=None, out=None) == 0
+
 
 def test_decode_attention_arguments_are_checked_on_the_host(L):
     vp = ctypes.c_void_p

@@ -120,3 +120,28 @@ def test_empty_sequence_and_graph_replay():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, eager) and torch.equal(work, eager_S)
+
+
+def test_state_read_early_in_a_chain_of_layers():
+    """A chain of single-token scans over distinct states (decode through several
+    layers), each launch marked MOE_GDN_STATE_EARLY (its state is read before it waits
+    for the previous launch, which writes another layer's state), captured in one
+    graph: the same bits as the chain run eagerly without the flag."""
+    from bit_moe_expert_route_gb300 import ops
+    Hk, Hv, dk, dv, n_layers = 2, 4, 128, 128, 6
+    layers = [to_dev(*inputs(1, Hk, Hv, dk, dv, seed=40 + i)) for i in range(n_layers)]
+    ref_S = [lay[5].clone() for lay in layers]
+    ref_out = [ops.gdn_scan(*lay[:5], ref_S[i]) for i, lay in enumerate(layers)]
+    work_S = [lay[5].clone() for lay in layers]
+    outs = [torch.empty_like(o) for o in ref_out]
+    st = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        for i, lay in enumerate(layers):
+            ops.gdn_scan(*lay[:5], work_S[i], out=outs[i], state_early=True)
+    for i, lay in enumerate(layers):
+        work_S[i].copy_(lay[5])
+    g.replay()
+    torch.cuda.synchronize()
+    for i in range(n_layers):
+        assert torch.equal(outs[i], ref_out[i]) and torch.equal(work_S[i], ref_S[i]), i
