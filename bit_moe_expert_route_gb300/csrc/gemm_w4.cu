@@ -96,7 +96,13 @@ struct Cfg {
                  : (232448 - 1024 - 8 * (2 * kSQ + 2 * kSA + 2 * 8 + 5) - 16 - kQRing - kEpiBytes -
                     kRowInfoBytes - kSA * kAStage) /
                        kBBytes;
-  static constexpr int kSB = kSB0 > 8 ? 8 : kSB0;
+  // Tiles of up to 64 rows with A in TMEM: the token ring takes the A ring's
+  // depth and its producer arrives on the A stage's barrier, so the MMA tests
+  // one barrier per k-block instead of two (a test costs about 100 cycles of
+  // the MMA thread, the busiest role at these sizes; taller tiles keep the
+  // deeper token ring).
+  static constexpr bool kMerge = kATmem && kSA >= 3 && BN <= 64;
+  static constexpr int kSB = kMerge ? kSA : (kSB0 > 8 ? 8 : kSB0);
   static constexpr int kSD = kSA > kSB ? kSA : kSB;  // k-block completion barriers
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kSA * kAStage;
@@ -234,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
   // waits for k-block i - kSA, the B producer for i - kSB; the MMA cannot run
   // kSD k-blocks past either, so no barrier is two phases ahead of a waiter)
   uint64_t* done = b_full + C::kSB;
+  uint64_t* b_ready = C::kMerge ? a_full : b_full;  // where token tiles are signalled
   uint64_t* acc_full = done + C::kSD;      // [2]
   uint64_t* acc_empty = acc_full + 2;      // [2]
   uint64_t* drain = acc_empty + 2;         // [1]
@@ -250,9 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 8);    // dequant warps
     }
-    for (int i = 0; i < C::kSA; ++i) {
-      mbar_init(&a_full[i], 8);     // dequant warps
-    }
+    for (int i = 0; i < C::kSA; ++i)  // dequant warps (+ the token tile's producer when merged)
+      mbar_init(&a_full[i], 8 + (C::kMerge ? (b_by_tma ? 1 : 2) : 0));
     for (int i = 0; i < C::kSB; ++i) {
       mbar_init(&b_full[i], b_by_tma ? 1 : 2);  // TMA, or the gather warps
     }
@@ -320,8 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
               ++it;
               break;
             }
-            mbar_arrive_expect_tx(&b_full[sb], C::kBBytes);
-            tma_load_2d(smem + C::kOffB + sb * C::kBBytes, &kp.tm[4], kb * kKB, t.row0, &b_full[sb],
+            mbar_arrive_expect_tx(&b_ready[sb], C::kBBytes);
+            tma_load_2d(smem + C::kOffB + sb * C::kBBytes, &kp.tm[4], kb * kKB, t.row0, &b_ready[sb],
                         policy);
           }
         }
@@ -332,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
       const uint32_t n_issued = it;
       if (b_by_tma)
         for (uint32_t j = n_issued > (uint32_t)C::kSB ? n_issued - C::kSB : 0; j < n_issued; ++j)
-          mbar_wait(&b_full[j % C::kSB], (j / C::kSB) & 1, abort_flag, g.status, 2);
+          mbar_wait(&b_ready[j % C::kSB], (j / C::kSB) & 1, abort_flag, g.status, 2);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -351,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % C::kSA, sb = it % C::kSB;
           if (!mbar_wait(&a_full[s], (it / C::kSA) & 1, abort_flag, g.status, 4) ||
-              !mbar_wait(&b_full[sb], (it / C::kSB) & 1, abort_flag, g.status, 4)) {
+              (!C::kMerge && !mbar_wait(&b_full[sb], (it / C::kSB) & 1, abort_flag, g.status, 4))) {
             alive = false;
             break;
           }
@@ -580,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
         if (it + 1 - arrived > (uint32_t)kD) {  // step `arrived` is kD steps old: complete it
           cp_async_wait<kD>();
           fence_proxy_async_smem();
-          mbar_arrive_warp(&b_full[arrived % C::kSB]);
+          mbar_arrive_warp(&b_ready[arrived % C::kSB]);
           ++arrived;
         }
       }
@@ -590,11 +596,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_w4_kernel(const __grid_const
       // (several thousand cycles per tile, seen in per-role timestamps).
       cp_async_wait<0>();
       fence_proxy_async_smem();
-      for (; arrived < it; ++arrived) mbar_arrive_warp(&b_full[arrived % C::kSB]);
+      for (; arrived < it; ++arrived) mbar_arrive_warp(&b_ready[arrived % C::kSB]);
     }
     cp_async_wait<0>();
     fence_proxy_async_smem();
-    for (; arrived < it; ++arrived) mbar_arrive_warp(&b_full[arrived % C::kSB]);
+    for (; arrived < it; ++arrived) mbar_arrive_warp(&b_ready[arrived % C::kSB]);
   } else if (warp >= 12) {
     // ------------------------------------------------------------ epilogue
     // TMEM -> registers -> (NONE) direct fp32 stores; (SWIGLU) silu(g)*u in
