@@ -28,6 +28,8 @@
 // FMAs; for a group with scale s and bias b,
 //   sum_k (s*q_k + b) v_k = 16 s * sum_k f_k v_k + (b - 16 s) * sum_k v_k,
 // with the activation group sums taken once per token.
+#include <algorithm>
+
 #include "common.cuh"
 #include "gemv_dot.cuh"
 #include "kernels.h"
@@ -160,6 +162,15 @@ __global__ void __launch_bounds__(kBThreads) batch_router_kernel(const __grid_co
 }
 
 // ---------------------------------------------------------------- 2. top-k, gate/up
+constexpr int kRD = 4;  // gate/up tasks in flight per warp (the ring path)
+
+// The gate/up kernel's task ring: after x, its group sums and the ids, 16-byte
+// aligned, over the top-k keys (dead once the tasks start).
+MOE_DEVINL uint8_t* gateup_ring(uint8_t* base, int T, int d, int k) {
+  const size_t off = (size_t)T * d * 2 + (size_t)T * (d / 64) * 4 + (size_t)T * k * 4;
+  return base + ((off + 15) & ~(size_t)15);
+}
+
 template <int TB>
 __global__ void __launch_bounds__(kBThreads, 2) batch_gateup_kernel(const __grid_constant__ BatchParams p) {
   extern __shared__ __align__(16) uint8_t bsm[];
@@ -261,10 +272,106 @@ __global__ void __launch_bounds__(kBThreads, 2) batch_gateup_kernel(const __grid
   __syncthreads();
   // tasks: (slot i of T*k, row r): token i / k times its expert's row r;
   // then (shared row r, token t) at T*k*f + t*f + r. Each warp takes a
-  // contiguous run of tasks and works through it kIB at a time, every load of
-  // a batch issued before its arithmetic (a lane holds 64 codes of each
-  // matrix, one group, per pass). Rows of an expert that two tokens select
-  // are read once per token (the second read mostly from L2).
+  // contiguous run of tasks. Rows of an expert that two tokens select are
+  // read once per token (the second read mostly from L2).
+  auto task_of = [&](int it, int& tk_, int& row_, bool& sh_) {
+    sh_ = it >= n_routed;
+    tk_ = sh_ ? (it - n_routed) / f : (it / f) / k;
+    row_ = sh_ ? (it - n_routed) % f : s_ids[it / f] * f + it % f;
+  };
+  if (TB == 2 && d % 512 == 0) {
+    // Up to 2 tokens: each warp streams its tasks' gate and up rows (codes,
+    // then scale and bias rows) into its own shared-memory ring, kRD tasks
+    // ahead, with 16-byte cp.async, so the copies of the next tasks are in
+    // flight while two are computed; a lane reads its group (64 codes of each
+    // matrix) from the ring. (With more tokens per layer the batches below
+    // measured faster.)
+    const int rb = d + d / 8;  // bytes per task: two code rows, four scale/bias rows
+    uint8_t* ring = gateup_ring(bsm, T, d, k) + (size_t)warp * kRD * rb;
+    const int nq = d / 32, ns = d / 512;  // 16-byte chunks of a code row / of a scale row
+    auto issue = [&](int it, int slot) {
+      if (it < i_hi) {
+        int tk_, row_;
+        bool sh_;
+        task_of(it, tk_, row_, sh_);
+        const moe_w4_t& G = sh_ ? p.w.sh_gate : p.w.gate;
+        const moe_w4_t& U = sh_ ? p.w.sh_up : p.w.up;
+        uint8_t* dst = ring + (size_t)slot * rb;
+        const uint8_t* gq = reinterpret_cast<const uint8_t*>(G.q) + (size_t)row_ * (d / 2);
+        const uint8_t* uq = reinterpret_cast<const uint8_t*>(U.q) + (size_t)row_ * (d / 2);
+        for (int c = lane; c < nq; c += 32) {
+          cp_async_16(smem_u32(dst + c * 16), gq + c * 16, 16);
+          cp_async_16(smem_u32(dst + d / 2 + c * 16), uq + c * 16, 16);
+        }
+        for (int c = lane; c < 4 * ns; c += 32) {
+          const int a = c / ns, o = c - a * ns;  // gate scale, gate bias, up scale, up bias
+          const uint16_t* src = a == 0 ? G.scale : a == 1 ? G.bias : a == 2 ? U.scale : U.bias;
+          cp_async_16(smem_u32(dst + d + a * (d / 32) + o * 16),
+                      reinterpret_cast<const uint8_t*>(src + (size_t)row_ * ng) + o * 16, 16);
+        }
+      }
+      cp_async_commit();
+    };
+#pragma unroll 1
+    for (int r = 0; r < kRD; ++r) issue(i_lo + r, r);
+#pragma unroll 1
+    for (int it = i_lo; it < i_hi; it += 2) {  // two tasks per step: two independent chains
+      const bool two = it + 1 < i_hi;
+      cp_async_wait<kRD - 2>();
+      __syncwarp();  // every lane's copies of these tasks have landed
+      int tk_[2], row_[2];
+      bool sh_[2];
+      float ag[2] = {0.f, 0.f}, au[2] = {0.f, 0.f};
+      const uint8_t* src[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        task_of(t == 0 || two ? it + t : it, tk_[t], row_[t], sh_[t]);
+        src[t] = ring + (size_t)((it - i_lo + t) % kRD) * rb;
+      }
+      for (int g = lane; g < ng; g += 32) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (t == 1 && !two) break;
+          const uint8_t* sr = src[t];
+          const uint16_t* sb = reinterpret_cast<const uint16_t*>(sr + d);
+          const uint4 g0 = reinterpret_cast<const uint4*>(sr + g * 32)[0];
+          const uint4 g1 = reinterpret_cast<const uint4*>(sr + g * 32)[1];
+          const uint4 u0 = reinterpret_cast<const uint4*>(sr + d / 2 + g * 32)[0];
+          const uint4 u1 = reinterpret_cast<const uint4*>(sr + d / 2 + g * 32)[1];
+          const uint32_t wg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+          const uint32_t wu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+          const float gs = bf16f(sb[g]), gb = bf16f(sb[ng + g]), us = bf16f(sb[2 * ng + g]),
+                      ub = bf16f(sb[3 * ng + g]);
+          const uint16_t* v = xs + (size_t)tk_[t] * d + g * 64;
+          const float xsm = xsum[tk_[t] * ng + g];
+          ag[t] = fmaf(16.f * gs, group_fdot(wg, v, g), fmaf(gb - 16.f * gs, xsm, ag[t]));
+          au[t] = fmaf(16.f * us, group_fdot(wu, v, g), fmaf(ub - 16.f * us, xsm, au[t]));
+        }
+      }
+      __syncwarp();  // every lane is done with the two slots
+#pragma unroll
+      for (int t = 0; t < 2; ++t) issue(it + kRD + t, (it - i_lo + t) % kRD);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          ag[t] += __shfl_xor_sync(kFullMask, ag[t], off);
+          au[t] += __shfl_xor_sync(kFullMask, au[t], off);
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (lane == 0 && (t == 0 || two)) {
+          const float hv = ag[t] / (1.f + expf(-ag[t])) * au[t];
+          const int slot_h = sh_[t] ? k : ((it + t) / f) % k;  // routed: slot of the token's selection
+          p.h[((size_t)tk_[t] * S + slot_h) * f + row_[t] % f] = hv;
+        }
+    }
+    cp_async_wait<0>();
+    return;
+  }
+  // other row lengths: batches of kIB tasks, every load of a batch issued
+  // before its arithmetic (a lane holds 64 codes of each matrix per pass)
   constexpr int kIB = 3;
   for (int i0 = i_lo; i0 < i_hi; i0 += kIB) {
     int tok[kIB], srow[kIB];
@@ -485,7 +592,9 @@ cudaError_t launch_pdl(K kern, int grid, size_t smem, cudaStream_t s, const Batc
 
 size_t batch_smem_router(int T, int d) { return (size_t)T * d * 2 + (size_t)kBWarps * kBatchMaxT * 8 * 4; }
 size_t batch_smem_gateup(int T, int d, int E, int k) {
-  return (size_t)T * d * 2 + (size_t)T * (d / 64) * 4 + (size_t)T * k * 4 + (size_t)T * E * 4;
+  const size_t head = (size_t)T * d * 2 + (size_t)T * (d / 64) * 4 + (size_t)T * k * 4;
+  const size_t ring = T <= 2 && d % 512 == 0 ? 15 + (size_t)kBWarps * kRD * (d + d / 8) : 0;
+  return head + std::max((size_t)T * E * 4, ring);
 }
 size_t batch_smem_down(int T, int k, int f) {
   const int S = k + 1;
