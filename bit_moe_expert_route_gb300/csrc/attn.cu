@@ -34,8 +34,8 @@
 namespace moe {
 namespace {
 
-constexpr int kAttnWarps = 8;
-constexpr int kAttnMaxGroup = 8;
+constexpr int kAttnWarps = 8;     // position sets per block (one warp per set and head group)
+constexpr int kAttnMaxGroup = 8;  // query heads per KV head
 
 template <int E>
 MOE_DEVINL void load_row(const uint16_t* p, float (&f)[E]) {
@@ -60,7 +60,7 @@ MOE_DEVINL void load_row(const uint16_t* p, float (&f)[E]) {
   }
 }
 
-constexpr int kRing = 16;  // positions in flight per warp
+constexpr int kRing = 16;  // positions in flight per position set (per warp: 16 / head groups)
 
 // 16-, 8- or 4-byte cp.async global -> shared (the lane's own elements of a row)
 template <int B>
@@ -353,7 +353,8 @@ cudaError_t split_setup(size_t ring, int threads, int sms, int* slots) {
 
 cudaError_t attn_decode_launch(const AttnParams& pin, int sms, cudaStream_t s) {
   if (!attn_shape_supported(pin.L, pin.Hq, pin.Hkv, pin.d) || !pin.ws) return cudaErrorInvalidValue;
-  const size_t ring = (size_t)kAttnWarps * kRing * 2 * pin.d * 2;  // bf16 K and V rows per warp slot
+  // bf16 K and V rows: kRing slots per position set (shared out among its warps)
+  const size_t ring = (size_t)kAttnWarps * kRing * 2 * pin.d * 2;
   const int HG = pin.Hq / pin.Hkv > kHeadsPerWarp ? 2 : 1;         // head groups of 4 per block
   const int threads = 32 * kAttnWarps * HG;
   int slots = sms;
