@@ -302,9 +302,14 @@ __device__ __noinline__ void rows_h(const DecodeParams& p, const uint8_t* Y, int
 // hp, chunk sums in hsum), two columns per warp per pass (the same h words
 // serve both): over the flattened (slot, chunk) index idx = lane + 32 i,
 // each slot's part weighted by its routing weight; rounded once to bf16.
+// FCH: 32-code chunks per down row as a compile-time constant (the chunk
+// index splits into slot and chunk with a shift instead of a division by a
+// run-time value in every step), or 0: f / 32 at run time.
+template <int FCH>
 __device__ __noinline__ void down_cols(const DecodeParams& p, const uint8_t* X, const uint4* hp,
                                        const float* hsum, const float* s_w, int total, int j0, int nj) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, f = p.f, fch = f / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, f = FCH ? FCH * 32 : p.f,
+            fch = FCH ? FCH : f / 32;
   const size_t half_row = f / 2, groups = f / 64;
   const size_t slot_bytes = (size_t)p.capX * (half_row + 4 * groups);
 #pragma unroll 1
@@ -762,7 +767,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_layer_kernel(const __gr
     }
     bar_wait(sm.barX, x_phase & 1, p.wait_ns, p.status, 45);
     ++x_phase;
-    down_cols(p, sm.X, hp, hsum, sm.s_w, total, j0, nj);
+    if (p.f == 512)
+      down_cols<16>(p, sm.X, hp, hsum, sm.s_w, total, j0, nj);
+    else
+      down_cols<0>(p, sm.X, hp, hsum, sm.s_w, total, j0, nj);
   }
 
   // ---- block 0 records this call's epoch for the next call (every block
