@@ -240,10 +240,12 @@ MOE_DEVINL float silu(float v) { return v * __frcp_rn(1.f + expf(-v)); }
 // stored plainly for the workspace view and published. Lanes take the
 // 32-code chunks c = lane, lane + 32, ...; 8 independent FMA chains each.
 constexpr int kRowsPerPass = 2;
+template <int NCH>  // 32-code chunks per row as a compile-time constant, or 0: d / 32 at run time
 __device__ __noinline__ void rows_h(const DecodeParams& p, const uint8_t* Y, int cap, const uint4* xp,
                                     const float* xsum, int i0, int i1, int r0, int w0, int nw,
                                     uint32_t epoch) {
-  const int lane = threadIdx.x & 31, wr = (int)(threadIdx.x >> 5) - w0, d = p.d, nch = d / 32;
+  const int lane = threadIdx.x & 31, wr = (int)(threadIdx.x >> 5) - w0, d = NCH ? NCH * 32 : p.d,
+            nch = NCH ? NCH : d / 32;
 #pragma unroll 1
   for (int i = i0 + kRowsPerPass * wr; i < i1; i += kRowsPerPass * nw) {
     RowPairSmem r[kRowsPerPass];
@@ -252,7 +254,7 @@ __device__ __noinline__ void rows_h(const DecodeParams& p, const uint8_t* Y, int
     float acc[2 * kRowsPerPass];  // gate, up of each row
 #pragma unroll
     for (int m = 0; m < 2 * kRowsPerPass; ++m) acc[m] = 0.f;
-#pragma unroll 1
+#pragma unroll(NCH ? NCH / 32 : 1)
     for (int c = lane; c < nch; c += 32) {
       uint4 q[2 * kRowsPerPass];
 #pragma unroll
@@ -689,14 +691,20 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_layer_kernel(const __gr
           }
           bar_wait(sm.barZ, z_phase & 1, p.wait_ns, p.status, 40);
           ++z_phase;
-          rows_h(p, sm.Z, p.capS, sm.xp, sm.xsum, 0, n, k * f + s0, kIssueWarp - 2, 2, epoch);
+          if (d == 2048)
+            rows_h<64>(p, sm.Z, p.capS, sm.xp, sm.xsum, 0, n, k * f + s0, kIssueWarp - 2, 2, epoch);
+          else
+            rows_h<0>(p, sm.Z, p.capS, sm.xp, sm.xsum, 0, n, k * f + s0, kIssueWarp - 2, 2, epoch);
         }
       }
 #pragma unroll 1
       for (int g = 0; g < kYGroups; ++g) {
         if (gb[g + 1] == gb[g]) continue;
         bar_wait(sm.barY + g, y_phase & 1, p.wait_ns, p.status, 43);
-        rows_h(p, sm.Y, p.capY, sm.xp, sm.xsum, gb[g], gb[g + 1], c0, 0, kIssueWarp, epoch);
+        if (d == 2048)
+          rows_h<64>(p, sm.Y, p.capY, sm.xp, sm.xsum, gb[g], gb[g + 1], c0, 0, kIssueWarp, epoch);
+        else
+          rows_h<0>(p, sm.Y, p.capY, sm.xp, sm.xsum, gb[g], gb[g + 1], c0, 0, kIssueWarp, epoch);
       }
     }
     ++y_phase;
