@@ -171,10 +171,13 @@ MOE_DEVINL uint8_t* gateup_ring(uint8_t* base, int T, int d, int k) {
   return base + ((off + 15) & ~(size_t)15);
 }
 
-template <int TB>
+// SD: the standard layer shape (d_model 2048, d_ff 512, top-8) as compile-time
+// constants, so that the task and item indices split with shifts and
+// multiplications instead of divisions by run-time values; otherwise 0.
+template <int TB, int SD>
 __global__ void __launch_bounds__(kBThreads, 2) batch_gateup_kernel(const __grid_constant__ BatchParams p) {
   extern __shared__ __align__(16) uint8_t bsm[];
-  const int T = p.T, d = p.d, E = p.E, k = p.k, f = p.f, S = k + 1;
+  const int T = p.T, d = SD ? 2048 : p.d, E = p.E, k = SD ? 8 : p.k, f = SD ? 512 : p.f, S = k + 1;
   const int ng = d / 64;  // groups per row
   uint16_t* xs = reinterpret_cast<uint16_t*>(bsm);                                 // [T][d]
   float* xsum = reinterpret_cast<float*>(bsm + (size_t)T * d * 2);                 // [T][ng]
@@ -444,10 +447,10 @@ __global__ void __launch_bounds__(kBThreads, 2) batch_gateup_kernel(const __grid
 }
 
 // ---------------------------------------------------------------- 3. down + combine
-template <int TB>
+template <int TB, int SD>  // SD: as for the gate/up kernel
 __global__ void __launch_bounds__(kBThreads, 2) batch_down_kernel(const __grid_constant__ BatchParams p) {
   extern __shared__ __align__(16) uint8_t bsm[];
-  const int T = p.T, d = p.d, k = p.k, f = p.f, S = k + 1;
+  const int T = p.T, d = SD ? 2048 : p.d, k = SD ? 8 : p.k, f = SD ? 512 : p.f, S = k + 1;
   const int nslots = p.shared ? S : k, ngf = f / 64;
   uint16_t* hs = reinterpret_cast<uint16_t*>(bsm);                                   // bf16 [T][S][f]
   float* hsum = reinterpret_cast<float*>(bsm + (size_t)T * S * f * 2);              // [T][S][ngf]
@@ -614,10 +617,13 @@ cudaError_t launch_tb(const BatchParams& p, cudaStream_t s) {
                                batch_smem_router(p.T, p.d), s, p);
   if (err != cudaSuccess) return err;
   const int G = 2 * sm_count_b();  // two blocks per SM
-  if ((err = launch_pdl(batch_gateup_kernel<TB>, G, batch_smem_gateup(p.T, p.d, p.E, p.k), s, p)) !=
+  const bool sd = p.d == 2048 && p.f == 512 && p.k == 8;  // the standard layer shape
+  if ((err = sd ? launch_pdl(batch_gateup_kernel<TB, 1>, G, batch_smem_gateup(p.T, p.d, p.E, p.k), s, p)
+                : launch_pdl(batch_gateup_kernel<TB, 0>, G, batch_smem_gateup(p.T, p.d, p.E, p.k), s, p)) !=
       cudaSuccess)
     return err;
-  return launch_pdl(batch_down_kernel<TB>, G, batch_smem_down(p.T, p.k, p.f), s, p);
+  return sd ? launch_pdl(batch_down_kernel<TB, 1>, G, batch_smem_down(p.T, p.k, p.f), s, p)
+            : launch_pdl(batch_down_kernel<TB, 0>, G, batch_smem_down(p.T, p.k, p.f), s, p);
 }
 
 cudaError_t decode_batch_launch(const BatchParams& p, cudaStream_t s) {
