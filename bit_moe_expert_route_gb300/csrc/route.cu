@@ -240,11 +240,20 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(RouteParams p, int nbl
   const int e = threadIdx.x;
   int total = 0;
   if (e < p.E) {
-    for (int b = 0; b < nblk; ++b) {
-      const size_t i = (size_t)b * p.E + e;
-      const int c = p.blk[i];
-      p.blk[i] = total;  // exclusive base of block b inside expert e
-      total += c;
+    // 16 blocks' counts are loaded before any base is stored back (a store
+    // to the same array would otherwise hold every next load behind it: one
+    // L2 round trip per block)
+    constexpr int kB = 16;
+    for (int b0 = 0; b0 < nblk; b0 += kB) {
+      int c[kB];
+#pragma unroll
+      for (int j = 0; j < kB; ++j) c[j] = b0 + j < nblk ? p.blk[(size_t)(b0 + j) * p.E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < kB; ++j)
+        if (b0 + j < nblk) {
+          p.blk[(size_t)(b0 + j) * p.E + e] = total;  // exclusive base of block b inside expert e
+          total += c[j];
+        }
     }
     p.counts[e] = total;
     s_cnt[e] = total;
@@ -309,7 +318,7 @@ __global__ void __launch_bounds__(kThreads) route_scatter_kernel(RouteParams p) 
       pos = mine[e] + __popc(m & lanemask_lt());
       p.perm[pos] = (int32_t)a;
       p.inv_perm[a] = pos;
-      p.row_token[pos] = (int32_t)(a / p.k);
+      p.row_token[pos] = (int32_t)((uint32_t)a / (uint32_t)p.k);  // a < T * k < 2^31
       if (p.row_weight) p.row_weight[pos] = p.w[a];
     }
     __syncwarp();
