@@ -426,12 +426,16 @@ MOE_DEVINL void y_groups(int n, int q, int* gb) {
 }
 
 // ---------------------------------------------------------------- kernel
+// SD: the standard layer shape (d_model 2048, 256 experts, top-8, d_ff 512)
+// as compile-time constants, so that loops over experts, candidates and
+// chunks have known trip counts; otherwise 0 (the sizes come from p).
+template <int SD>
 __global__ void __launch_bounds__(kDecThreads, 2) decode_layer_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) uint8_t dsmem[];
   const DecSmem sm = carve_dec_smem(dsmem, p);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, b = blockIdx.x;
-  const int d = p.d, E = p.E, k = p.k, f = p.f;
+  const int d = SD ? 2048 : p.d, E = SD ? 256 : p.E, k = SD ? 8 : p.k, f = SD ? 512 : p.f;
   const int S = k + (p.shared ? 1 : 0);
   const int ncg = E / 8, n_items = ncg * p.KS, rs = (d + p.KS - 1) / p.KS;
   const uint32_t rp_bytes = d + d / 8;          // one row pair in Y
@@ -441,7 +445,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_layer_kernel(const __gr
   const int2 orng = block_range(d / p.qout, b, G, p.qout);                          // outputs
   const int nj0 = min(orng.y - orng.x, p.capX);
   const int nr0 = min(rr.y - rr.x, p.capY);
-  const int kc = cand_per_warp(p);
+  const int kc = SD ? 8 : cand_per_warp(p);
   int gb[kYGroups + 1];
   y_groups(nr0, p.qrow, gb);
 
@@ -775,7 +779,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_layer_kernel(const __gr
     }
     bar_wait(sm.barX, x_phase & 1, p.wait_ns, p.status, 45);
     ++x_phase;
-    if (p.f == 512)
+    if (f == 512)
       down_cols<16>(p, sm.X, hp, hsum, sm.s_w, total, j0, nj);
     else
       down_cols<0>(p, sm.X, hp, hsum, sm.s_w, total, j0, nj);
@@ -847,17 +851,18 @@ cudaError_t launch_pdl(K kernel, dim3 grid, size_t smem, cudaStream_t s, Args...
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int G, size_t smem, cudaStream_t s) {
+template <int SD>
+cudaError_t launch_decode_t(const DecodeParams& p, int G, size_t smem, cudaStream_t s) {
   static std::mutex mu;
   static bool attr_set = false;
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!attr_set) {
-      cudaError_t err = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kDecSmemLimit);
+      cudaError_t err = cudaFuncSetAttribute(decode_layer_kernel<SD>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecSmemLimit);
       if (err != cudaSuccess) return err;
       // all of the SM's configurable memory as shared memory (two blocks' worth)
-      err = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      err = cudaFuncSetAttribute(decode_layer_kernel<SD>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
       if (err != cudaSuccess) return err;
       attr_set = true;
     }
@@ -867,10 +872,15 @@ cudaError_t launch_decode(const DecodeParams& p, int G, size_t smem, cudaStream_
   // occupancy query must allow two blocks per SM, else the launch is refused.
   int per_sm = 0;
   const cudaError_t err =
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel, kDecThreads, smem);
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel<SD>, kDecThreads, smem);
   if (err != cudaSuccess) return err;
   if (per_sm < 2 || G > per_sm * sm_count()) return cudaErrorInvalidConfiguration;
-  return launch_pdl(decode_layer_kernel, dim3(G), smem, s, p);
+  return launch_pdl(decode_layer_kernel<SD>, dim3(G), smem, s, p);
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int G, size_t smem, cudaStream_t s) {
+  const bool sd = p.d == 2048 && p.E == 256 && p.k == 8 && p.f == 512;  // the standard layer shape
+  return sd ? launch_decode_t<1>(p, G, smem, s) : launch_decode_t<0>(p, G, smem, s);
 }
 
 // Row granularity of the block ranges: bulk copies move whole 16-byte units
