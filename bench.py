@@ -711,15 +711,16 @@ CONFIG = {
     "parallelism": "replicas",
 }
 
-# dram__bytes_read.sum + dram__bytes_write.sum per launch unit, from the ncu captures
-# summarised under profiles/: the decode kernel on one layer (cold cache: all of its
-# weights come from HBM), and both grouped GEMMs of one forward at T = 512, 4096 and
-# 32768 (mean of three forwards). None where no capture of the current kernel exists.
+# dram__bytes_read.sum + dram__bytes_write.sum per launch unit, from ncu captures of the
+# current kernels summarised under profiles/: the decode kernel on one layer (cold
+# cache: all of its weights come from HBM), and both grouped GEMMs of the third forward
+# at T = 512, 4096 and 32768 (gate/up read + write, then down read + write). None where
+# no capture of the current kernel exists.
 TRAFFIC: dict = {
-    "decode_layer": 18_132_992,
-    "gemm_T512": 307_492_437 + 3_958_528 + 160_701_013 + 271_872,
-    "gemm_T4096": 345_934_592 + 25_333_333 + 231_090_347 + 12_661_504,
-    "gemm_T32768": 1_175_549_525 + 287_004_501 + 2_233_447_339 + 1_945_131_691,
+    "decode_layer": 18_125_824,
+    "gemm_T512": 307_554_560 + 5_821_696 + 160_693_248 + 445_440,
+    "gemm_T4096": 346_443_520 + 28_443_648 + 230_775_296 + 15_150_336,
+    "gemm_T32768": 1_172_207_360 + 287_205_376 + 2_235_480_320 + 1_945_010_176,
 }
 
 
