@@ -282,13 +282,12 @@ __global__ void __launch_bounds__(kBThreads, 2) batch_gateup_kernel(const __grid
     tk_ = sh_ ? (it - n_routed) / f : (it / f) / k;
     row_ = sh_ ? (it - n_routed) % f : s_ids[it / f] * f + it % f;
   };
-  if (TB == 2 && d % 512 == 0) {
-    // Up to 2 tokens: each warp streams its tasks' gate and up rows (codes,
-    // then scale and bias rows) into its own shared-memory ring, kRD tasks
-    // ahead, with 16-byte cp.async, so the copies of the next tasks are in
-    // flight while two are computed; a lane reads its group (64 codes of each
-    // matrix) from the ring. (With more tokens per layer the batches below
-    // measured faster.)
+  if (d % 512 == 0) {
+    // Each warp streams its tasks' gate and up rows (codes, then scale and
+    // bias rows) into its own shared-memory ring, kRD tasks ahead, with
+    // 16-byte cp.async, so the copies of the next tasks are in flight while
+    // two are computed; a lane reads its group (64 codes of each matrix)
+    // from the ring.
     const int rb = d + d / 8;  // bytes per task: two code rows, four scale/bias rows
     uint8_t* ring = gateup_ring(bsm, T, d, k) + (size_t)warp * kRD * rb;
     const int nq = d / 32, ns = d / 512;  // 16-byte chunks of a code row / of a scale row
@@ -596,7 +595,7 @@ cudaError_t launch_pdl(K kern, int grid, size_t smem, cudaStream_t s, const Batc
 size_t batch_smem_router(int T, int d) { return (size_t)T * d * 2 + (size_t)kBWarps * kBatchMaxT * 8 * 4; }
 size_t batch_smem_gateup(int T, int d, int E, int k) {
   const size_t head = (size_t)T * d * 2 + (size_t)T * (d / 64) * 4 + (size_t)T * k * 4;
-  const size_t ring = T <= 2 && d % 512 == 0 ? 15 + (size_t)kBWarps * kRD * (d + d / 8) : 0;
+  const size_t ring = d % 512 == 0 ? 15 + (size_t)kBWarps * kRD * (d + d / 8) : 0;
   return head + std::max((size_t)T * E * 4, ring);
 }
 size_t batch_smem_down(int T, int k, int f) {
