@@ -293,16 +293,15 @@ cudaError_t gdn_launch_r(const GdnParams& p, int blocks, cudaStream_t s) {
 }
 
 // Rows per warp: 4 where the value rows split into blocks of 32, else 2, else
-// 1; 1 for short sequences, which are bound by the state's traffic (more
-// blocks in flight) rather than by the per-token chain.
-int gdn_rows_per_warp(int T, int dv) {
-  if (T < 64) return 1;
+// 1, at any length (a single decode token measured 2.80 us per layer with 4
+// rows per warp against 2.88 with 1 or 2 and 30 layers in one graph).
+int gdn_rows_per_warp(int dv) {
   return dv % (kGdnWarps * 4) == 0 ? 4 : dv % (kGdnWarps * 2) == 0 ? 2 : 1;
 }
 
 template <int DK>
 cudaError_t gdn_launch_dk(const GdnParams& p, cudaStream_t s) {
-  const int R = gdn_rows_per_warp(p.T, p.dv);
+  const int R = gdn_rows_per_warp(p.dv);
   const int64_t blocks = (int64_t)p.Hv * (p.dv / (kGdnWarps * R));
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
   if (R == 4) return gdn_launch_r<DK, 4>(p, (int)blocks, s);

@@ -39,8 +39,8 @@ extern "C" {
  * d_k in {64, 128}; d_v a multiple of 8; n_v_heads a multiple of n_k_heads;
  * T >= 0 (T == 0 leaves the state unchanged and launches nothing). Others:
  * MOE_ERR_SHAPE. NULL pointers: MOE_ERR_NULL; misaligned ones: MOE_ERR_ALIGN.
- * One launch of one 8-warp block per 8 R state rows (R rows per warp: 4 for
- * T >= 64 when d_v is a multiple of 32, else 2 or 1; 1 for T < 64); every warp
+ * One launch of one 8-warp block per 8 R state rows (R rows per warp: 4 when
+ * d_v is a multiple of 32, else 2 or 1); every warp
  * carries its rows through all T tokens in registers (state traffic: one read
  * and one write of the state per call), the block staging 32 tokens of inputs
  * at a time in shared memory. fp32 arithmetic throughout. The launch is a
