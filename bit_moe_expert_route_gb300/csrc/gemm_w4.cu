@@ -14,7 +14,9 @@
 //     depends on the routing result.
 //   * warp 0       TMA producer: packed-code tiles (128 rows x 64 codes =
 //                  4 KB per projection) into a ring of shared-memory stages.
-//   * warp 1       allocates TMEM and issues tcgen05.mma (one thread).
+//   * warp 1       allocates TMEM and issues tcgen05.mma (one thread), with
+//                  one commit per k-block to a ring of completion barriers
+//                  that frees both that k-block's A stage and its token tile.
 //   * warps 4-11   dequantise: two threads per weight row, 32 codes each;
 //                  RNE(scale*q + bias) (f16 or bf16) goes into the A operand:
 //                  in tensor memory (tcgen05.st: row = TMEM lane, two K
@@ -28,13 +30,16 @@
 //                  row_index the rows are contiguous and warp 0 loads each
 //                  B tile with one 128-byte-swizzled TMA copy instead.
 //   * warps 12-15  epilogue: tcgen05.ld of the accumulators, then
-//                  NONE (fp32 store), SWIGLU (silu(g)*u in the operand type) or
-//                  COMBINE (row_scale * y added into the output row), the last
-//                  two staged in shared memory and written one token row per
-//                  TMA bulk copy (COMBINE: bulk fp32 add, done at L2).
+//                  NONE (fp32 store), SWIGLU (silu(g)*u in the operand type,
+//                  stored straight from registers) or COMBINE (row_scale * y
+//                  staged in shared memory and added into each token's output
+//                  row by one TMA bulk fp32 reduce per row, done at L2).
 //   Accumulators are double buffered so the epilogue of one tile overlaps the
-//   MMAs of the next. Every wait is bounded; a CTA that gives up records
-//   MOE_DEV_TIMEOUT, drains what it issued, frees TMEM and returns.
+//   MMAs of the next (256-row gate/up tiles fill TMEM with one buffer). At
+//   tiles of up to 64 rows the token tile's producer arrives on the A stage's
+//   barrier, so the MMA tests one barrier per k-block. Every wait is bounded;
+//   a CTA that gives up records MOE_DEV_TIMEOUT, drains what it issued, frees
+//   TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
