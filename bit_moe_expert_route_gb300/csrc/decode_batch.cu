@@ -18,7 +18,11 @@
 //   2. batch_gateup_kernel   every block ranks each token's logits (one warp
 //        per token: value descending, ties to the lower id; softmax over the
 //        selected), block 0 stores ids and weights; then the row pairs of
-//        gate/up, each (row, token) a task: h = silu(x . g) * (x . u) in fp32.
+//        gate/up, each (row, token) a task: h = silu(x . g) * (x . u) in fp32,
+//        each warp streaming its tasks' rows through its own shared-memory
+//        ring (cp.async, four tasks ahead).
+// The gate/up and down kernels also have an instantiation for the standard
+// layer shape (d_model 2048, d_ff 512, top-8) with those sizes as constants.
 //   3. batch_down_kernel     output columns split over the blocks; for each
 //        column and token, every slot's down row weighted by its routing
 //        weight (the shared expert's by sigmoid of the gate logit), summed in
