@@ -38,7 +38,11 @@
 // Every block runs each phase once per launch, so the kernel's instruction
 // footprint, fetched cold from L2 on every SM, matters as much as its
 // arithmetic: each computation has one copy of its code (two rows, or two
-// output columns, per pass; an odd one out runs as a duplicate).
+// output columns, per pass; an odd one out runs as a duplicate). The kernel,
+// the routed rows and the down columns also have instantiations for the
+// standard layer shape (d_model 2048, 256 experts, top-8, d_ff 512) with
+// those sizes as constants: loop trip counts are known and index splits are
+// shifts; a launch runs one instantiation, so only its code is fetched.
 //
 // Dot products per packed word (8 codes; 4 words = 32 codes = half a group):
 // a code q becomes the 16-bit float f = 1 + q/16 exactly (bf16 bits
