@@ -37,29 +37,6 @@ namespace {
 constexpr int kAttnWarps = 8;     // position sets per block (one warp per set and head group)
 constexpr int kAttnMaxGroup = 8;  // query heads per KV head
 
-template <int E>
-MOE_DEVINL void load_row(const uint16_t* p, float (&f)[E]) {
-  if constexpr (E == 8) {
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(p));
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      f[2 * i] = __uint_as_float(u[i] << 16);
-      f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
-    }
-  } else if constexpr (E == 4) {
-    const uint2 w = __ldg(reinterpret_cast<const uint2*>(p));
-    f[0] = __uint_as_float(w.x << 16);
-    f[1] = __uint_as_float(w.x & 0xFFFF0000u);
-    f[2] = __uint_as_float(w.y << 16);
-    f[3] = __uint_as_float(w.y & 0xFFFF0000u);
-  } else {
-    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(p));
-    f[0] = __uint_as_float(w << 16);
-    f[1] = __uint_as_float(w & 0xFFFF0000u);
-  }
-}
-
 constexpr int kRing = 16;  // positions in flight per position set (per warp: 16 / head groups)
 
 // 16-, 8- or 4-byte cp.async global -> shared (the lane's own elements of a row)
